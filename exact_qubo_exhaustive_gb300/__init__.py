@@ -1,0 +1,237 @@
+"""exact_qubo_exhaustive_gb300 -- exhaustive QUBO minimisation on one GB300 (sm_103a).
+
+Thin Python binding of the C ABI in include/qubo.h (argument marshalling only; every step of
+the search runs in the CUDA kernels of libqubo_gb300.so). The library must have been built
+(`python -m exact_qubo_exhaustive_gb300.build` or __graft_entry__.build()); there is no CPU
+fallback, and importing the binding without the library raises ImportError.
+
+    E(x) = sum_{i,j} Q_ij x_i x_j,  x in {0,1}^n   (Terastate-per-second QUBO Brute-Force, §I)
+
+Results are (E_min, argmin x as uint8[n] with x_0 first, number of minimisers); the argmin is
+the minimiser of lowest rank (x_0 the most significant bit).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+__all__ = [
+    "QuboError", "INT32", "FP32", "solve", "solve_slices", "solve_slice_range", "solve_batched",
+    "solve_device", "solve_batched_device", "workspace_bytes", "batched_workspace_bytes", "plan",
+    "probe_alu", "last_launch_count", "status_string", "last_error", "request_abort", "clear_abort",
+    "library_path", "RESULT_DTYPE",
+]
+
+INT32 = 0
+FP32 = 1
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libqubo_gb300.so")
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m exact_qubo_exhaustive_gb300.build` "
+                      "(the CUDA library is required; there is no CPU path)")
+
+_lib = ctypes.CDLL(_LIB_PATH)
+
+_u8p = ctypes.POINTER(ctypes.c_uint8)
+_u64p = ctypes.POINTER(ctypes.c_uint64)
+_f64p = ctypes.POINTER(ctypes.c_double)
+
+
+class _PlanDesc(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int), ("dtype", ctypes.c_int), ("k_prefix", ctypes.c_int),
+                ("cache_bits", ctypes.c_int), ("walked_bits", ctypes.c_int), ("register_bits", ctypes.c_int),
+                ("columns_per_thread", ctypes.c_int), ("threads_per_block", ctypes.c_int), ("blocks", ctypes.c_int),
+                ("variant", ctypes.c_int), ("units", ctypes.c_uint64), ("workspace_bytes", ctypes.c_size_t),
+                ("smem_bytes", ctypes.c_size_t)]
+
+
+# qubo_result record as a numpy dtype (status, reserved, min_energy, argmin_rank, tie_count)
+RESULT_DTYPE = np.dtype([("status", np.int32), ("reserved", np.int32), ("min_energy", np.float64),
+                         ("argmin_rank", np.uint64), ("tie_count", np.uint64)])
+
+_sig = {
+    "qubo_solve": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int, _f64p,
+                                  _u8p, _u64p]),
+    "qubo_solve_slices": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         _u64p, ctypes.c_int, _f64p, _u8p, _u64p]),
+    "qubo_solve_slice_range": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, _f64p, _u8p, _u64p]),
+    "qubo_solve_batched": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int, _f64p, _u8p,
+                                          _u64p]),
+    "qubo_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "qubo_solve_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "qubo_batched_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "qubo_solve_batched_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
+                                                 ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
+                                                 ctypes.c_void_p]),
+    "qubo_plan": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_PlanDesc)]),
+    "qubo_last_launch_count": (ctypes.c_int, []),
+    "qubo_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+    "qubo_last_error": (ctypes.c_char_p, []),
+    "qubo_request_abort": (None, []),
+    "qubo_clear_abort": (None, []),
+    "qubo_probe_alu": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64p, _f64p]),
+}
+for _name, (_res, _args) in _sig.items():
+    _f = getattr(_lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class QuboError(RuntimeError):
+    def __init__(self, status: int):
+        msg = _lib.qubo_status_string(status).decode()
+        if status == -5:
+            msg += ": " + _lib.qubo_last_error().decode()
+        super().__init__(f"qubo status {status}: {msg}")
+        self.status = status
+
+
+def _check(st: int):
+    if st != 0:
+        raise QuboError(st)
+
+
+def _matrix(Q):
+    Q = np.asarray(Q)
+    if Q.ndim != 2 or Q.shape[0] != Q.shape[1]:
+        raise ValueError("Q must be a square matrix")
+    if Q.dtype == np.float32:
+        return np.ascontiguousarray(Q), FP32
+    if Q.dtype.kind in "iu" and Q.dtype.itemsize <= 4:
+        return np.ascontiguousarray(Q, dtype=np.int32), INT32
+    if Q.dtype.kind in "iu":
+        if Q.size and (Q.min() < -(1 << 31) or Q.max() >= (1 << 31)):
+            raise ValueError("integer Q must fit int32")
+        return np.ascontiguousarray(Q, dtype=np.int32), INT32
+    raise TypeError("Q must be int32 or float32")
+
+
+def solve(Q, k_prefix: int = 0, cache_bits: int = 0):
+    """Exhaustive minimum of E(x) = x^T Q x over {0,1}^n: (E_min, argmin x, tie count)."""
+    Q, dt = _matrix(Q)
+    n = Q.shape[0]
+    e = ctypes.c_double()
+    x = np.zeros(n, np.uint8)
+    t = ctypes.c_uint64()
+    _check(_lib.qubo_solve(n, Q.ctypes.data, dt, k_prefix, cache_bits, ctypes.byref(e),
+                           x.ctypes.data_as(_u8p), ctypes.byref(t)))
+    return (int(e.value) if dt == INT32 else float(e.value)), x, int(t.value)
+
+
+def solve_slices(Q, k_prefix: int, slice_ids, cache_bits: int = 0):
+    """Per-slice results for the slices whose first k_prefix variables equal slice_ids (MSB first)."""
+    Q, dt = _matrix(Q)
+    n = Q.shape[0]
+    ids = np.ascontiguousarray(slice_ids, dtype=np.uint64)
+    m = ids.size
+    e = np.zeros(m, np.float64)
+    x = np.zeros((m, n), np.uint8)
+    t = np.zeros(m, np.uint64)
+    _check(_lib.qubo_solve_slices(n, Q.ctypes.data, dt, k_prefix, cache_bits, ids.ctypes.data_as(_u64p), m,
+                                  e.ctypes.data_as(_f64p), x.ctypes.data_as(_u8p), t.ctypes.data_as(_u64p)))
+    if dt == INT32:
+        e = e.astype(np.int64)
+    return e, x, t
+
+
+def solve_slice_range(Q, k_prefix: int, first_slice: int, num_slices: int, cache_bits: int = 0):
+    """One result over the slices [first_slice, first_slice + num_slices) of k_prefix bits."""
+    Q, dt = _matrix(Q)
+    n = Q.shape[0]
+    e = ctypes.c_double()
+    x = np.zeros(n, np.uint8)
+    t = ctypes.c_uint64()
+    _check(_lib.qubo_solve_slice_range(n, Q.ctypes.data, dt, k_prefix, cache_bits, first_slice, num_slices,
+                                       ctypes.byref(e), x.ctypes.data_as(_u8p), ctypes.byref(t)))
+    return (int(e.value) if dt == INT32 else float(e.value)), x, int(t.value)
+
+
+def solve_batched(Qs):
+    """Independent problems Qs[b] (batch x n x n, int32): arrays of E_min, argmin x, ties."""
+    Qs = np.ascontiguousarray(Qs, dtype=np.int32)
+    if Qs.ndim != 3 or Qs.shape[1] != Qs.shape[2]:
+        raise ValueError("Qs must be batch x n x n")
+    b, n = Qs.shape[0], Qs.shape[1]
+    e = np.zeros(b, np.float64)
+    x = np.zeros((b, n), np.uint8)
+    t = np.zeros(b, np.uint64)
+    _check(_lib.qubo_solve_batched(b, n, Qs.ctypes.data, INT32, e.ctypes.data_as(_f64p), x.ctypes.data_as(_u8p),
+                                   t.ctypes.data_as(_u64p)))
+    return e.astype(np.int64), x, t
+
+
+def _ptr(a) -> int:
+    if a is None:
+        return 0
+    if isinstance(a, int):
+        return a
+    return int(a.data_ptr())
+
+
+def workspace_bytes(n: int, dtype: int = INT32, k_prefix: int = 0, cache_bits: int = 0) -> int:
+    return int(_lib.qubo_workspace_bytes(n, dtype, k_prefix, cache_bits))
+
+
+def batched_workspace_bytes(batch: int, n: int, dtype: int = INT32) -> int:
+    return int(_lib.qubo_batched_workspace_bytes(batch, n, dtype))
+
+
+def solve_device(n: int, d_Q, dtype: int, workspace, workspace_nbytes: int, stream, d_result,
+                 k_prefix: int = 0, cache_bits: int = 0) -> None:
+    """Enqueue a search on device memory: d_Q, workspace and d_result are device pointers (ints or
+    tensors with data_ptr()); stream is a cudaStream_t handle (int) or None. Asynchronous."""
+    _check(_lib.qubo_solve_device(n, _ptr(d_Q), dtype, k_prefix, cache_bits, _ptr(workspace), workspace_nbytes,
+                                  _ptr(stream) if stream is not None else 0, _ptr(d_result)))
+
+
+def solve_batched_device(batch: int, n: int, d_Q, workspace, workspace_nbytes: int, stream, d_results) -> None:
+    _check(_lib.qubo_solve_batched_device(batch, n, _ptr(d_Q), INT32, _ptr(workspace), workspace_nbytes,
+                                          _ptr(stream) if stream is not None else 0, _ptr(d_results)))
+
+
+def plan(n: int, dtype: int = INT32, k_prefix: int = 0, cache_bits: int = 0) -> dict:
+    d = _PlanDesc()
+    _check(_lib.qubo_plan(n, dtype, k_prefix, cache_bits, ctypes.byref(d)))
+    return {f: getattr(d, f) for f, _ in _PlanDesc._fields_}
+
+
+def probe_alu(kind: int, iters: int = 20000):
+    """(lane-operations per second, SM MHz) of one ALU operation kind on the current device."""
+    ops, mhz = ctypes.c_double(), ctypes.c_double()
+    _check(_lib.qubo_probe_alu(kind, iters, ctypes.byref(ops), ctypes.byref(mhz)))
+    return ops.value, mhz.value
+
+
+def last_launch_count() -> int:
+    return int(_lib.qubo_last_launch_count())
+
+
+def status_string(status: int) -> str:
+    return _lib.qubo_status_string(status).decode()
+
+
+def last_error() -> str:
+    return _lib.qubo_last_error().decode()
+
+
+def request_abort() -> None:
+    _lib.qubo_request_abort()
+
+
+def clear_abort() -> None:
+    _lib.qubo_clear_abort()
+
+
+def rank_to_bits(n: int, rank: int) -> np.ndarray:
+    return np.array([(int(rank) >> (n - 1 - i)) & 1 for i in range(n)], dtype=np.uint8)

@@ -1,0 +1,109 @@
+// ALU throughput microbenchmark used to state the roofline of the enumeration kernels:
+// 16 independent chains of one operation per thread, 8 blocks of 256 threads per SM, timed with
+// CUDA events; the SM clock is read inside the kernel as clock64 ticks per globaltimer ns.
+#include <vector>
+
+#include "qubo_internal.h"
+
+namespace qgb {
+namespace {
+constexpr int kChains = 16;
+
+template <int KIND>
+__global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int* out, unsigned long long* clk) {
+  int a[kChains];
+  float f[kChains];
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) {
+    a[k] = (threadIdx.x * 7 + k * 13 + seed) & 1023;
+    f[k] = (float)a[k] * 0.5f;
+  }
+  const unsigned long long c0 = clock64();
+  unsigned long long g0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g0));
+#pragma unroll 1
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int k = 0; k < kChains; ++k) {
+      const int x = a[(k + 1) % kChains], y = a[(k + 2) % kChains];
+      if (KIND == 0) a[k] = a[k] + x;
+      if (KIND == 1) a[k] = min(a[k], x);
+      if (KIND == 2) a[k] = __vimin3_s32(a[k], x, y);
+      if (KIND == 3) a[k] = __viaddmin_s32(a[k], x, y);
+      if (KIND == 4) f[k] = __fadd_rn(f[k], f[(k + 1) % kChains]);
+      if (KIND == 5) f[k] = fminf(f[k], f[(k + 1) % kChains]);
+    }
+  }
+  const unsigned long long c1 = clock64();
+  unsigned long long g1;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g1));
+  int s = 0;
+#pragma unroll
+  for (int k = 0; k < kChains; ++k) s += a[k] + (int)f[k];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+  if (threadIdx.x == 0) {
+    clk[2 * blockIdx.x] = c1 - c0;
+    clk[2 * blockIdx.x + 1] = g1 - g0;
+  }
+}
+
+template <int KIND>
+cudaError_t launch(int blocks, int iters, int* out, unsigned long long* clk) {
+  alu_probe_kernel<KIND><<<blocks, 256>>>(iters, 1, out, clk);
+  return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz) {
+  const DevInfo& di = device_info();
+  const int blocks = di.sms * 8;
+  int* out = nullptr;
+  unsigned long long* clk = nullptr;
+  cudaError_t e = cudaMalloc(&out, (size_t)blocks * 256 * 4);
+  if (e != cudaSuccess) return e;
+  e = cudaMalloc(&clk, (size_t)blocks * 16);
+  if (e != cudaSuccess) {
+    cudaFree(out);
+    return e;
+  }
+  auto go = [&](int it) -> cudaError_t {
+    switch (kind) {
+      case 0: return launch<0>(blocks, it, out, clk);
+      case 1: return launch<1>(blocks, it, out, clk);
+      case 2: return launch<2>(blocks, it, out, clk);
+      case 3: return launch<3>(blocks, it, out, clk);
+      case 4: return launch<4>(blocks, it, out, clk);
+      default: return launch<5>(blocks, it, out, clk);
+    }
+  };
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  float ms = 0.f;
+  std::vector<unsigned long long> h((size_t)blocks * 2);
+  if ((e = go(64)) != cudaSuccess) goto done;  // warm-up
+  if ((e = cudaDeviceSynchronize()) != cudaSuccess) goto done;
+  cudaEventCreate(&e0);
+  cudaEventCreate(&e1);
+  cudaEventRecord(e0);
+  if ((e = go(iters)) != cudaSuccess) goto done;
+  cudaEventRecord(e1);
+  if ((e = cudaEventSynchronize(e1)) != cudaSuccess) goto done;
+  cudaEventElapsedTime(&ms, e0, e1);
+  if ((e = cudaMemcpy(h.data(), clk, (size_t)blocks * 16, cudaMemcpyDeviceToHost)) != cudaSuccess) goto done;
+  {
+    double cy = 0, ns = 0;
+    for (int b = 0; b < blocks; ++b) {
+      cy += (double)h[2 * b];
+      ns += (double)h[2 * b + 1];
+    }
+    *sm_mhz = ns > 0 ? cy / ns * 1e3 : 0.0;
+    *ops_per_s = (double)blocks * 256.0 * iters * kChains / (ms * 1e-3);
+  }
+done:
+  if (e0) cudaEventDestroy(e0);
+  if (e1) cudaEventDestroy(e1);
+  cudaFree(out);
+  cudaFree(clk);
+  return e;
+}
+
+}  // namespace qgb

@@ -1,0 +1,107 @@
+// Internal declarations shared by the library's translation units (not part of the C ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/qubo.h"
+
+namespace qgb {
+
+// Largest sum of |U_ij| the int32 search accepts: every value a kernel forms is a sub-sum of U
+// or the difference of two sub-sums, so |value| <= 2 * S <= 2^31 - 2 stays in int32.
+constexpr int64_t kMaxAbsSum = (int64_t(1) << 30) - 1;
+
+// Kernel variants.
+enum Variant : int {
+  kGeneric = 0,  // one column per thread, every walked row in shared memory
+  kFast = 1,     // 16 columns per thread, the lowest kFastR walked rows in registers
+};
+constexpr int kFastCPT = 16;
+constexpr int kFastR = 4;
+constexpr int kGenericMaxC = 10;  // 2^C threads per block
+constexpr int kMaxWalkedBits = 24;
+
+// Written by the device, read back by the host (lives at the start of the workspace).
+struct DevHeader {
+  int32_t status;      // QUBO_OK or an error code found on the device
+  int32_t scale_exp;   // fp32 path: U32 = round(U64 * 2^scale_exp)
+  int32_t band;        // candidates: energy <= group minimum + band (int32 units)
+  uint32_t tied_count; // number of entries in the tied-unit list
+  int64_t abs_sum;     // sum |U_ij| of the int32 image
+  double abs_sum64;    // fp32 path: sum |U_ij| in fp64
+  int32_t pad[8];
+};
+
+// Host-side plan (one call).
+struct Plan {
+  int n = 0, dtype = 0;
+  int variant = kGeneric;
+  int C = 0;       // cached bits
+  int F = 0;       // fixed bits per work unit
+  int w = 0;       // walked bits = n - F - C
+  int R = 0;       // register-row bits of the variant
+  int cpt = 1;     // columns per thread
+  int threads = 32;
+  int blocks = 1;
+  int seg_bits = 0;        // resolve: segments per tied unit = 2^seg_bits
+  int ngroups = 1;
+  uint64_t upg = 1;        // units per group
+  uint64_t total_units = 1;
+  size_t smem_bytes = 0;   // dynamic shared memory of the enumeration kernels
+  bool host_gbase = false; // group bases uploaded by the host (else one group at unit 0)
+};
+
+// Device pointers into one workspace.
+struct Work {
+  DevHeader* hdr = nullptr;
+  int32_t* U = nullptr;     // n x n int32 image of the folded triangle
+  double* U64 = nullptr;    // n x n fp64 folded triangle (fp32 path)
+  int32_t* M = nullptr;     // (n - C) x 2^C: interaction of each non-cached variable with each column
+  int32_t* Ec = nullptr;    // 2^C: energy of the cached variables alone
+  int32_t* T = nullptr;     // 2^w (padded): walked-variable energy, in Gray order
+  int32_t* unit_min = nullptr;
+  uint32_t* tied = nullptr;
+  uint64_t* gbase = nullptr;  // first unit prefix of each group
+  int32_t* gmin = nullptr;
+  uint64_t* grank = nullptr;
+  uint64_t* gties = nullptr;
+  uint64_t* gkey = nullptr;
+  qubo_result* results = nullptr;  // one per group
+  size_t bytes = 0;
+};
+
+// Byte layout of the workspace for a plan (offsets only; base may be null).
+Work layout_workspace(const Plan& p, unsigned char* base);
+
+// Kernel launch sequence for one plan on `stream`. d_Q is the device input, `res` receives
+// one qubo_result per group. Returns cudaSuccess or the first launch error; `launches` counts.
+// A set abort flag stops before the next min-pass launch and sets *aborted.
+cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
+                       int* launches, const volatile int* abort_flag, bool* aborted);
+
+// Batched mode (one block per instance).
+struct BatchPlan {
+  int batch = 0, n = 0, C = 0, w = 0, threads = 0;
+  size_t smem_bytes = 0;
+};
+bool plan_batched(int batch, int n, BatchPlan* bp);
+size_t batched_workspace_bytes(const BatchPlan& bp);
+cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_result* res, cudaStream_t stream,
+                        int* launches);
+
+// Measurement.
+cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz);
+
+// Device properties cached per device.
+struct DevInfo {
+  int device = -1;
+  int sms = 0;
+  size_t smem_optin = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+const DevInfo& device_info();
+
+}  // namespace qgb

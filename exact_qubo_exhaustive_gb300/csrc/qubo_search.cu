@@ -1,0 +1,364 @@
+// Fold/validate, cache construction, reductions and the launch sequence of one search.
+#include <cstring>
+
+#include "qubo_search_kernel.cuh"
+
+namespace qgb {
+
+// ------------------------------------------------------------------------------------------------
+// A1: fold Q to the upper triangle and validate (one block).
+//   int32: U_ii = Q_ii, U_ij = Q_ij + Q_ji (i < j) in int64; S = sum |U_ij| must be <= 2^30 - 1.
+//   fp32:  every entry finite; U64 folded in fp64; the int32 image is round(U64 * 2^s) with the
+//          largest s keeping sum |image| <= 2^30 - 1. A state's image energy then differs from
+//          2^s times its energy by at most (#selected terms)/2 <= n(n+1)/4, so every fp64
+//          minimiser lies within band = n(n+1)/2 image units of the image minimum.
+// ------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void* __restrict__ Qv, DevHeader* hdr,
+                                                   int32_t* U, double* U64, uint64_t* gbase0) {
+  __shared__ unsigned long long s_sum;
+  __shared__ int s_bad;
+  __shared__ double s_part[256];
+  const int tid = threadIdx.x, nt = blockDim.x;
+  const int nn = n * n;
+  if (tid == 0) {
+    s_sum = 0;
+    s_bad = 0;
+    if (gbase0) *gbase0 = 0;
+  }
+  __syncthreads();
+  if (dtype == QUBO_INT32) {
+    const int32_t* Q = static_cast<const int32_t*>(Qv);
+    unsigned long long local = 0;
+    for (int idx = tid; idx < nn; idx += nt) {
+      const int i = idx / n, j = idx - (idx / n) * n;
+      long long u = 0;
+      if (j == i) u = Q[idx];
+      else if (j > i) u = (long long)Q[idx] + (long long)Q[j * n + i];
+      local += (unsigned long long)(u < 0 ? -u : u);
+      U[idx] = (int32_t)u;  // only used when the range check passes
+    }
+    atomicAdd(&s_sum, local);
+    __syncthreads();
+    if (tid == 0) {
+      hdr->abs_sum = (int64_t)s_sum;
+      hdr->abs_sum64 = (double)s_sum;
+      hdr->scale_exp = 0;
+      hdr->band = 0;
+      hdr->tied_count = 0;
+      hdr->status = (s_sum > (unsigned long long)kMaxAbsSum) ? QUBO_ERR_RANGE : QUBO_OK;
+    }
+    return;
+  }
+  // fp32
+  const float* Q = static_cast<const float*>(Qv);
+  double local = 0.0;
+  int bad = 0;
+  for (int idx = tid; idx < nn; idx += nt) {
+    const int i = idx / n, j = idx - (idx / n) * n;
+    const float a = Q[idx];
+    if (!isfinite(a)) bad = 1;
+    double u = 0.0;
+    if (j == i) u = (double)a;
+    else if (j > i) u = __dadd_rn((double)a, (double)Q[j * n + i]);
+    U64[idx] = u;
+    local += fabs(u);
+  }
+  if (bad) atomicOr(&s_bad, 1);
+  s_part[tid] = local;
+  __syncthreads();
+  for (int h = nt / 2; h > 0; h >>= 1) {  // fixed-order tree: deterministic
+    if (tid < h) s_part[tid] += s_part[tid + h];
+    __syncthreads();
+  }
+  const double S64 = s_part[0];
+  __shared__ int s_scale;
+  const int npairs = n * (n + 1) / 2;
+  if (tid == 0) {
+    int sc = 0;
+    if (S64 > 0.0) {
+      int e;
+      frexp((double)(kMaxAbsSum - npairs) / S64, &e);  // ratio = m * 2^e, m in [0.5, 1)
+      sc = e - 1;
+      sc = sc > 1074 ? 1074 : (sc < -1074 ? -1074 : sc);
+    }
+    s_scale = sc;
+  }
+  __syncthreads();
+  // Exact check of the quantised sum; step the scale down until it fits (at most a few times).
+  for (int attempt = 0; attempt < 4; ++attempt) {
+    const int sc = s_scale;
+    unsigned long long q = 0;
+    for (int idx = tid; idx < nn; idx += nt) {
+      const long long v = __double2ll_rn(ldexp(U64[idx], sc));
+      q += (unsigned long long)(v < 0 ? -v : v);
+    }
+    if (tid == 0) s_sum = 0;
+    __syncthreads();
+    atomicAdd(&s_sum, q);
+    __syncthreads();
+    const bool fits = s_sum <= (unsigned long long)kMaxAbsSum;
+    __syncthreads();
+    if (fits) break;
+    if (tid == 0) s_scale = sc - 1;
+    __syncthreads();
+  }
+  const int sc = s_scale;
+  for (int idx = tid; idx < nn; idx += nt) U[idx] = (int32_t)__double2ll_rn(ldexp(U64[idx], sc));
+  if (tid == 0) {
+    hdr->abs_sum = (int64_t)s_sum;
+    hdr->abs_sum64 = S64;
+    hdr->scale_exp = sc;
+    hdr->band = npairs;
+    hdr->tied_count = 0;
+    hdr->status = s_bad ? QUBO_ERR_NONFINITE : (s_sum <= (unsigned long long)kMaxAbsSum ? QUBO_OK : QUBO_ERR_RANGE);
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// A3: the energy-component cache (§II-C Table I, Alg. 2 preprocessing), computed directly:
+//   M[v][j]  = sum_{cached b} U[v][b] x_b(j)        interaction rows M_int, v < n - C
+//   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
+//   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
+// ------------------------------------------------------------------------------------------------
+__global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __restrict__ hdr,
+                              const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint64_t nTpad) {
+  if (hdr->status != QUBO_OK) return;
+  const int ncols = 1 << C;
+  const uint64_t nM = (uint64_t)(n - C) << C;
+  const uint64_t nE = (uint64_t)ncols;
+  const uint64_t total = nM + nE + nTpad;
+  const int base_c = n - C;  // first cached variable
+  for (uint64_t idx = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (uint64_t)gridDim.x * blockDim.x) {
+    if (idx < nM) {
+      const int v = (int)(idx >> C);
+      const int j = (int)(idx & (ncols - 1));
+      int acc = 0;
+      for (int b = 0; b < C; ++b)
+        if ((j >> b) & 1) acc += U[v * n + (n - 1 - b)];
+      M[idx] = acc;
+    } else if (idx < nM + nE) {
+      const int j = (int)(idx - nM);
+      int acc = 0;
+      for (int a = base_c; a < n; ++a) {
+        if (!((j >> (n - 1 - a)) & 1)) continue;
+        for (int b = a; b < n; ++b)
+          if ((j >> (n - 1 - b)) & 1) acc += U[a * n + b];
+      }
+      Ec[j] = acc;
+    } else {
+      const uint64_t i = idx - nM - nE;
+      if (i >= ((uint64_t)1 << w)) {
+        T[i] = 0;
+        continue;
+      }
+      const uint64_t g = i ^ (i >> 1);
+      // Gray position a drives variable n - C - 1 - a; walked variables are F .. n - C - 1.
+      int acc = 0;
+      for (int a = 0; a < w; ++a) {
+        if (!((g >> a) & 1u)) continue;
+        const int va = n - C - 1 - a;
+        for (int b = a; b < w; ++b)
+          if ((g >> b) & 1u) acc += U[(n - C - 1 - b) * n + va];  // n-C-1-b <= va
+      }
+      T[i] = acc;
+    }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// A5: per-group minimum over its units (one block per group), and accumulator reset.
+// ------------------------------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) group_min_kernel(KParams p) {
+  __shared__ int s_red[8];
+  if (p.hdr->status != QUBO_OK) return;
+  for (int g = blockIdx.x; g < p.ngroups; g += gridDim.x) {
+    int m = kIntInf;
+    for (uint64_t x = threadIdx.x; x < p.upg; x += blockDim.x) m = min(m, p.unit_min[(uint64_t)g * p.upg + x]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int k = 1; k < (int)(blockDim.x >> 5); ++k) m = min(m, s_red[k]);
+      p.gmin[g] = m;
+      p.grank[g] = ~0ull;
+      p.gties[g] = 0;
+      p.gkey[g] = ~0ull;
+    }
+    __syncthreads();
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) p.hdr->tied_count = 0;
+}
+
+// Units whose minimum is within the band of their group's minimum (order does not matter:
+// every later combination is commutative).
+__global__ void tie_list_kernel(KParams p, uint64_t total_units) {
+  if (p.hdr->status != QUBO_OK) return;
+  const int band = p.hdr->band;
+  for (uint64_t u = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; u < total_units;
+       u += (uint64_t)gridDim.x * blockDim.x) {
+    const uint64_t g = u / p.upg;
+    if (p.unit_min[u] <= p.gmin[g] + band) {
+      const unsigned idx = atomicAdd(&p.hdr->tied_count, 1u);
+      p.tied[idx] = (uint32_t)u;
+    }
+  }
+}
+
+__global__ void finalize_kernel(KParams p, qubo_result* out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= p.ngroups) return;
+  const int st = p.hdr->status;
+  qubo_result r;
+  r.status = st;
+  r.reserved = 0;
+  r.min_energy = 0.0;
+  r.argmin_rank = 0;
+  r.tie_count = 0;
+  if (st == QUBO_OK) {
+    r.min_energy = (p.dtype == QUBO_INT32) ? (double)p.gmin[g] : key_to_double(p.gkey[g]);
+    r.argmin_rank = p.grank[g];
+    r.tie_count = p.gties[g];
+  }
+  out[g] = r;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Workspace layout.
+// ------------------------------------------------------------------------------------------------
+static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+Work layout_workspace(const Plan& p, unsigned char* base) {
+  Work w;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    unsigned char* ptr = base ? base + off : nullptr;
+    off += align256(bytes);
+    return ptr;
+  };
+  const size_t nn = (size_t)p.n * p.n;
+  const size_t ncols = (size_t)1 << p.C;
+  const size_t nT = ((size_t)1 << p.w) < 4 ? 4 : ((size_t)1 << p.w);
+  w.hdr = reinterpret_cast<DevHeader*>(take(sizeof(DevHeader)));
+  w.U = reinterpret_cast<int32_t*>(take(nn * 4));
+  w.U64 = reinterpret_cast<double*>(take(p.dtype == QUBO_FP32 ? nn * 8 : 8));
+  w.M = reinterpret_cast<int32_t*>(take((size_t)(p.n - p.C > 0 ? p.n - p.C : 1) * ncols * 4));
+  w.Ec = reinterpret_cast<int32_t*>(take(ncols * 4 < 16 ? 16 : ncols * 4));
+  w.T = reinterpret_cast<int32_t*>(take(nT * 4));
+  w.unit_min = reinterpret_cast<int32_t*>(take(p.total_units * 4));
+  w.tied = reinterpret_cast<uint32_t*>(take(p.total_units * 4));
+  w.gbase = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
+  w.gmin = reinterpret_cast<int32_t*>(take((size_t)p.ngroups * 4));
+  w.grank = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
+  w.gties = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
+  w.gkey = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
+  w.results = reinterpret_cast<qubo_result*>(take((size_t)p.ngroups * sizeof(qubo_result)));
+  w.bytes = off;
+  return w;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Launch sequence: prep -> tables -> min pass -> group minima -> tied units -> resolve -> results.
+// ------------------------------------------------------------------------------------------------
+static cudaError_t launch_search(const Plan& p, int mode, const KParams& kp, int blocks, cudaStream_t s) {
+  if (p.variant == kFast) return launch_search_fast(mode, kp, blocks, p.threads, p.smem_bytes, s);
+  return launch_search_generic(mode, kp, blocks, p.threads, p.smem_bytes, s);
+}
+
+cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
+                       int* launches, const volatile int* abort_flag, bool* aborted) {
+  int nl = 0;
+  if (aborted) *aborted = false;
+  cudaError_t e;
+  // gbase: uploaded by the host for slices and ranges; otherwise one group starting at unit 0,
+  // written by the prep kernel.
+  prep_kernel<<<1, 256, 0, stream>>>(p.n, p.dtype, d_Q, w.hdr, w.U, w.U64, p.host_gbase ? nullptr : w.gbase);
+  ++nl;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  const uint64_t nTpad = ((uint64_t)1 << p.w) < 4 ? 4 : ((uint64_t)1 << p.w);
+  const uint64_t tab_work = ((uint64_t)(p.n - p.C) << p.C) + ((uint64_t)1 << p.C) + nTpad;
+  const int tab_blocks = (int)((tab_work + 255) / 256 < 4096 ? (tab_work + 255) / 256 : 4096);
+  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, nTpad);
+  ++nl;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  KParams kp;
+  memset(&kp, 0, sizeof(kp));
+  kp.n = p.n;
+  kp.C = p.C;
+  kp.F = p.F;
+  kp.w = p.w;
+  kp.dtype = p.dtype;
+  kp.seg_bits = p.seg_bits;
+  kp.ngroups = p.ngroups;
+  kp.upg = p.upg;
+  kp.hdr = w.hdr;
+  kp.U = w.U;
+  kp.U64 = w.U64;
+  kp.M = w.M;
+  kp.Ec = w.Ec;
+  kp.T = w.T;
+  kp.gbase = w.gbase;
+  kp.unit_min = w.unit_min;
+  kp.tied = w.tied;
+  kp.gmin = w.gmin;
+  kp.grank = w.grank;
+  kp.gties = w.gties;
+  kp.gkey = w.gkey;
+  kp.results = res;
+
+  // Min pass, in chunks so that a cancellation request is seen between launches of long runs.
+  const uint64_t states_per_unit = (uint64_t)1 << (p.n - p.F);
+  uint64_t chunk = p.total_units;
+  const uint64_t max_states_per_launch = (uint64_t)1 << 41;
+  if (states_per_unit > 0 && p.total_units * states_per_unit > max_states_per_launch) {
+    chunk = max_states_per_launch / states_per_unit;
+    if (chunk < (uint64_t)p.blocks) chunk = p.blocks;
+  }
+  for (uint64_t u0 = 0; u0 < p.total_units; u0 += chunk) {
+    if (abort_flag && *abort_flag) {
+      if (aborted) *aborted = true;
+      if (launches) *launches = nl;
+      return cudaSuccess;
+    }
+    kp.unit_begin = u0;
+    kp.unit_end = (u0 + chunk < p.total_units) ? u0 + chunk : p.total_units;
+    const uint64_t nunits = kp.unit_end - kp.unit_begin;
+    const int blocks = (int)(nunits < (uint64_t)p.blocks ? nunits : (uint64_t)p.blocks);
+    if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) return e;
+    ++nl;
+    if (kp.unit_end < p.total_units && abort_flag) {
+      // long run: wait for this chunk so a cancellation request is honoured promptly
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+    }
+  }
+
+  const int gblocks = p.ngroups < 1024 ? p.ngroups : 1024;
+  group_min_kernel<<<gblocks, 256, 0, stream>>>(kp);
+  ++nl;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const uint64_t tl_blocks64 = (p.total_units + 255) / 256;
+  const int tl_blocks = (int)(tl_blocks64 < 4096 ? tl_blocks64 : 4096);
+  tie_list_kernel<<<tl_blocks, 256, 0, stream>>>(kp, p.total_units);
+  ++nl;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+
+  if (p.dtype == QUBO_INT32) {
+    if ((e = launch_search(p, kModeTiesInt, kp, p.blocks, stream)) != cudaSuccess) return e;
+    ++nl;
+  } else {
+    if ((e = launch_search(p, kModeKeyFp, kp, p.blocks, stream)) != cudaSuccess) return e;
+    ++nl;
+    if ((e = launch_search(p, kModeTiesFp, kp, p.blocks, stream)) != cudaSuccess) return e;
+    ++nl;
+  }
+  finalize_kernel<<<(p.ngroups + 127) / 128, 128, 0, stream>>>(kp, res);
+  ++nl;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (launches) *launches = nl;
+  return cudaSuccess;
+}
+
+}  // namespace qgb

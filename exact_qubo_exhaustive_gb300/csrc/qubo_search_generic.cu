@@ -1,0 +1,33 @@
+// Generic enumeration kernel: one column per thread, every walked row in shared memory;
+// runs any split, including tiny problems and blocks with idle lanes.
+#include "qubo_search_kernel.cuh"
+
+namespace qgb {
+
+template <int MODE>
+static cudaError_t launch_one(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
+  auto k = search_kernel<1, 0, MODE>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<blocks, threads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
+  switch (mode) {
+    case kModeMin: return launch_one<kModeMin>(p, blocks, threads, smem, s);
+    case kModeTiesInt: return launch_one<kModeTiesInt>(p, blocks, threads, smem, s);
+    case kModeKeyFp: return launch_one<kModeKeyFp>(p, blocks, threads, smem, s);
+    case kModeTiesFp: return launch_one<kModeTiesFp>(p, blocks, threads, smem, s);
+  }
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm) {
+  auto k = search_kernel<1, 0, kModeMin>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, threads, smem);
+}
+
+}  // namespace qgb

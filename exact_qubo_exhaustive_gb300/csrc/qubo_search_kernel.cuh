@@ -1,0 +1,182 @@
+// Enumeration kernel: a persistent grid walks work units (fixed prefixes, §III-C1) or, in the
+// resolve modes, segments of the units whose minimum reached their group's minimum.
+#pragma once
+
+#include "qubo_walk.cuh"
+
+namespace qgb {
+
+struct KParams {
+  int n, C, F, w;           // w = walked bits per unit
+  int dtype;
+  int seg_bits;             // resolve: segments per tied unit = 2^seg_bits
+  int ngroups;
+  uint64_t upg;             // units per group
+  uint64_t unit_begin, unit_end;  // kModeMin: global unit range of this launch
+  DevHeader* hdr;
+  const int32_t* U;         // n x n int32 image
+  const double* U64;        // n x n fp64 folded (fp32 path)
+  const int32_t* M;
+  const int32_t* Ec;
+  const int32_t* T;
+  const uint64_t* gbase;
+  int32_t* unit_min;
+  uint32_t* tied;
+  int32_t* gmin;
+  uint64_t* grank;
+  uint64_t* gties;
+  uint64_t* gkey;
+  qubo_result* results;
+};
+
+// Linear terms of a unit with prefix P (F bits, bit F-1-f is x_f):
+//   sL[v] = sum_{f<F, x_f=1} U[f][v]                 for free v >= F (diag(x_f U_fr) of §III-C1),
+//   sL[f] = x_f * sum_{f<=f2<F, x_f2=1} U[f][f2]      for fixed f < F (their sum is c(P)).
+__device__ __forceinline__ void unit_linear_terms(const int32_t* __restrict__ U, int n, int F, uint64_t P, int* sL,
+                                                  int tid) {
+  if (tid < n) {
+    int acc = 0;
+    if (tid >= F) {
+      for (int f = 0; f < F; ++f)
+        if ((P >> (F - 1 - f)) & 1u) acc += U[f * n + tid];
+    } else if ((P >> (F - 1 - tid)) & 1u) {
+      for (int f2 = tid; f2 < F; ++f2)
+        if ((P >> (F - 1 - f2)) & 1u) acc += U[tid * n + f2];
+    }
+    sL[tid] = acc;
+  }
+}
+
+template <int CPT, int R, int MODE>
+__global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const KParams p) {
+  extern __shared__ __align__(16) int4 s_rows4[];
+  __shared__ int sL[64];
+  __shared__ int s_red[32];
+  if (p.hdr->status != QUBO_OK) return;
+
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+  const int n = p.n, C = p.C, F = p.F, w = p.w;
+  const int ncols = 1 << C;
+  const int ndyn = w > R ? w - R : 0;
+
+  // Stage the walked rows of positions >= R (slice-independent) in shared memory.
+  if constexpr (CPT >= 4) {
+    const int nq = ncols >> 2;
+    const int4* M4 = reinterpret_cast<const int4*>(p.M);
+    for (int idx = tid; idx < ndyn * nq; idx += nthreads) {
+      const int rr = idx / nq, q = idx - rr * nq;
+      const int v = n - C - 1 - (R + rr);
+      s_rows4[idx] = M4[(size_t)v * nq + q];
+    }
+  } else {
+    int* s_rows = reinterpret_cast<int*>(s_rows4);
+    for (int idx = tid; idx < ndyn * ncols; idx += nthreads) {
+      const int rr = idx >> C, j = idx & (ncols - 1);
+      const int v = n - C - 1 - (R + rr);
+      s_rows[idx] = p.M[(size_t)v * ncols + j];
+    }
+  }
+
+  WalkCtx c;
+  c.n = n;
+  c.C = C;
+  c.F = F;
+  c.w = w;
+  c.nthreads = nthreads;
+  c.thread = tid;
+  c.sL = sL;
+  c.rows4 = s_rows4;
+  c.rows1 = reinterpret_cast<const int*>(s_rows4);
+  c.T = p.T;
+  c.t_global = true;
+
+  const int64_t niter = walk_iterations<R>(w);
+  const int lane = tid & 31, warp = tid >> 5;
+
+  uint64_t nitems;
+  if constexpr (MODE == kModeMin) nitems = p.unit_end - p.unit_begin;
+  else nitems = static_cast<uint64_t>(p.hdr->tied_count) << p.seg_bits;
+
+  for (uint64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+    uint64_t u;
+    int64_t it0 = 0, it1 = niter;
+    if constexpr (MODE == kModeMin) {
+      u = p.unit_begin + item;
+    } else {
+      u = p.tied[item >> p.seg_bits];
+      const int64_t per = niter >> p.seg_bits;
+      const int64_t seg = static_cast<int64_t>(item & ((uint64_t(1) << p.seg_bits) - 1));
+      it0 = seg * per;
+      it1 = it0 + per;
+    }
+    const uint64_t g = u / p.upg;
+    const uint64_t P = p.gbase[g] + (u - g * p.upg);
+    const uint64_t prank = (F > 0) ? (P << (n - F)) : 0;
+
+    __syncthreads();  // previous item is done with sL; staged rows are visible
+    unit_linear_terms(p.U, n, F, P, sL, tid);
+    __syncthreads();
+    int cP = 0;
+    for (int f = 0; f < F; ++f) cP += sL[f];
+
+    Walker<CPT, R, MODE> W;
+    W.init(c, p.Ec, p.M, cP);
+    W.seek(c, it0);
+    uint64_t gk = 0;
+    if constexpr (MODE == kModeMin) {
+      W.aux = kIntInf;
+    } else {
+      W.aux = p.gmin[g] + p.hdr->band - W.s;
+      if constexpr (MODE == kModeTiesFp) gk = p.gkey[g];
+    }
+
+    if (niter == 0) {
+      // no walked variable (generic variant only): the single walked assignment is 0
+      W.step(c, prank, 0, p.T[0], p.U64, gk);
+    } else {
+      W.walk(c, it0, it1, it1, prank, p.U64, gk);
+    }
+
+    if constexpr (MODE == kModeMin) {
+      int best = W.aux + W.s;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+      if (lane == 0) s_red[warp] = best;
+      __syncthreads();
+      if (tid == 0) {
+        int b = s_red[0];
+        for (int k = 1; k < (nthreads >> 5); ++k) b = min(b, s_red[k]);
+        p.unit_min[u] = b;
+      }
+    } else {
+      uint64_t cnt = W.cnt, rmin = W.rmin, kmin = W.kmin;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        const uint64_t r2 = __shfl_xor_sync(0xffffffffu, rmin, off);
+        rmin = r2 < rmin ? r2 : rmin;
+        const uint64_t k2 = __shfl_xor_sync(0xffffffffu, kmin, off);
+        kmin = k2 < kmin ? k2 : kmin;
+      }
+      if (lane == 0) {
+        if constexpr (MODE == kModeKeyFp) {
+          if (kmin != ~0ull) atomicMin(reinterpret_cast<unsigned long long*>(&p.gkey[g]), kmin);
+        } else {
+          if (cnt) {
+            atomicAdd(reinterpret_cast<unsigned long long*>(&p.gties[g]), cnt);
+            atomicMin(reinterpret_cast<unsigned long long*>(&p.grank[g]), rmin);
+          }
+        }
+      }
+    }
+  }
+}
+
+// Launch helpers (one translation unit per variant).
+cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm);
+cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm);
+
+}  // namespace qgb

@@ -1,0 +1,344 @@
+// Device-side Gray-code walker of the prefix-suffix decomposition (sm_103a).
+//
+// Method (Terastate-per-second QUBO Brute-Force on a Single GPU):
+//  * §III-C1: a work unit fixes the first F variables (prefix P); the rest is an independent
+//    subproblem Q' = U_rr + diag(x_f U_fr) plus the constant c(P).
+//  * §II-A..C: the free variables split into walked variables (the pages' prefix block, A bits)
+//    and cached variables (the suffix block, B bits). For every cached assignment j (a column)
+//    the energy is E = E_walked(g) + E_cached(j) + sum_{k in g} M_int[k][j] (eq. 8); the
+//    interaction rows M_int and E_cached are the energy-component cache.
+//  * §III-B, eq. 9: walked assignments are visited in Gray-code order, so one walked variable
+//    flips per step and every column changes by exactly one row of M_int: one add per state.
+//  * §III-C2: columns are split across threads; each thread keeps its columns' running
+//    energies (and the rows of the lowest walked variables) in registers.
+//  * §IV-B.3: the walked self-energy E_walked is read from a table stored in Gray order, so
+//    the per-step read is sequential; all threads read the same entry (a broadcast).
+//
+// Per state the fast kernel issues one integer add (running energy += row) and half of a
+// 3-input min (the chunk minimum over the thread's columns); per step and thread it adds one
+// fused add-min (chunk minimum + walked energy, into the running best).
+//
+// Notation inside: a unit has n - F free variables = w walked + C cached. Gray position a
+// (0 = fastest) drives walked variable n - C - 1 - a. Column j holds cached variable n - 1 - b
+// in bit b. The state visited at Gray step i and column j has rank
+//     (P << (n - F)) | (gray(i) << C) | j.
+// Running quantities per thread:
+//     V[j] = E_cached(j) + L_c(j) + sum over set walked positions a of M[v_a][j]
+//            (+ L[v_a] for positions a < R, whose rows include the linear term),
+//     s    = c(P) + sum over set walked positions a >= R of L[v_a],
+// so the state's energy is s + T[i] + V[j], with T[i] = E_walked(gray(i)).
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "qubo_internal.h"
+
+namespace qgb {
+
+constexpr int kIntInf = 0x7fffffff;
+
+__device__ __forceinline__ uint64_t gray_code(uint64_t i) { return i ^ (i >> 1); }
+
+__host__ __device__ constexpr int ctz_c(int x) { return (x & 1) ? 0 : 1 + ctz_c(x >> 1); }
+
+// Order-preserving map from a (non-NaN) double to uint64.
+__device__ __forceinline__ uint64_t order_key(double d) {
+  const long long b = __double_as_longlong(d);
+  return b < 0 ? ~static_cast<uint64_t>(b) : (static_cast<uint64_t>(b) | 0x8000000000000000ull);
+}
+__host__ __device__ inline double key_to_double(uint64_t k) {
+  const uint64_t b = (k & 0x8000000000000000ull) ? (k & 0x7fffffffffffffffull) : ~k;
+  double d;
+  memcpy(&d, &b, sizeof(d));
+  return d;
+}
+
+// Energy of the state `rank` from the fp64 folded triangle, fixed order (i ascending, j >= i
+// ascending), correctly rounded additions only: the same sum the fp32 energy is defined by.
+static __device__ __noinline__ double eval64_rank(const double* __restrict__ U64, int n, uint64_t rank) {
+  double e = 0.0;
+  for (int i = 0; i < n; ++i) {
+    if (!((rank >> (n - 1 - i)) & 1u)) continue;
+    for (int j = i; j < n; ++j)
+      if ((rank >> (n - 1 - j)) & 1u) e = __dadd_rn(e, U64[i * n + j]);
+  }
+  return e;
+}
+
+// Minimum of N register values with 3-input mins (one ALU instruction per two values).
+template <int N>
+__device__ __forceinline__ int min_all(const int* v) {
+  if constexpr (N == 1) {
+    return v[0];
+  } else if constexpr (N == 2) {
+    return min(v[0], v[1]);
+  } else {
+    constexpr int G = (N + 2) / 3;
+    int w[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      if (3 * g + 2 < N) w[g] = __vimin3_s32(v[3 * g], v[3 * g + 1], v[3 * g + 2]);
+      else if (3 * g + 1 < N) w[g] = min(v[3 * g], v[3 * g + 1]);
+      else w[g] = v[3 * g];
+    }
+    return min_all<G>(w);
+  }
+}
+
+// Modes of one walk.
+enum WalkMode : int {
+  kModeMin = 0,     // minimum energy of the walked states
+  kModeTiesInt = 1, // count states with energy <= threshold and keep the lowest rank
+  kModeKeyFp = 2,   // lowest fp64 energy (order key) among states within the band
+  kModeTiesFp = 3,  // count states whose fp64 energy equals the group's key, lowest rank
+};
+
+// Everything one walk needs; pointers may be global or shared memory.
+struct WalkCtx {
+  int n, C, F, w;             // w = walked bits of this unit
+  int nthreads;               // columns are distributed over this many threads
+  int thread;                 // this thread's index among them
+  const int* sL;              // linear terms L[v] of the unit (v >= F); L[v] for v < F: c(P) parts
+  const int4* rows4;          // walked rows a >= R (quad layout), or
+  const int* rows1;           //   the same rows, one int per column (generic)
+  const int* T;               // walked energies in Gray order
+  bool t_global;              // T lives in global memory (use the read-only path)
+};
+
+// Column of (thread t, slot jj). Fast layout: quads of 4 consecutive columns, quad k of thread t
+// at index k * nthreads + t, so a warp's 16-byte loads of one row are contiguous.
+template <int CPT>
+__device__ __forceinline__ int column_of(int t, int nthreads, int jj) {
+  if constexpr (CPT == 1) return t;
+  else return ((((jj >> 2) * nthreads) + t) << 2) | (jj & 3);
+}
+
+template <int CPT, int R, int MODE>
+struct Walker {
+  static constexpr int kSteps = 1 << (R + 1);  // Gray steps per loop iteration
+  int V[CPT];
+  int Row[R > 0 ? R : 1][CPT];
+  int s;        // c(P) + sum of L over set walked positions >= R
+  int aux;      // kModeMin: running best minus s; resolve modes: threshold minus s
+  bool valid;   // this thread owns real columns (generic blocks may have idle lanes)
+  int col0;     // generic: this thread's column
+  // resolve accumulators
+  uint64_t cnt, rmin, kmin;
+
+  // --- set-up: running energies of all columns at walked assignment 0, and register rows.
+  __device__ __forceinline__ void init(const WalkCtx& c, const int* __restrict__ Ec, const int* __restrict__ M,
+                                       int cP) {
+    const int t = c.thread, T = c.nthreads, n = c.n, C = c.C;
+    s = cP;
+    cnt = 0;
+    rmin = ~0ull;
+    kmin = ~0ull;
+    if constexpr (CPT == 1) {
+      const int ncols = 1 << C;
+      valid = t < ncols;
+      col0 = valid ? t : ncols - 1;
+      int lc = 0;
+      for (int b = 0; b < C; ++b)
+        if ((col0 >> b) & 1) lc += c.sL[n - 1 - b];
+      V[0] = Ec[col0] + lc;
+    } else {
+      valid = true;
+      col0 = 0;
+      const int lt = 31 - __clz(T);  // log2(threads)
+      constexpr int kq = CPT / 4;    // quads per thread
+      constexpr int lk = ctz_c(kq);
+      int Lt = 0;
+      for (int b = 0; b < lt; ++b)
+        if ((t >> b) & 1) Lt += c.sL[n - 1 - (2 + b)];
+      const int Le1 = c.sL[n - 1], Le2 = c.sL[n - 2];
+      const int4* Ec4 = reinterpret_cast<const int4*>(Ec);
+#pragma unroll
+      for (int k = 0; k < kq; ++k) {
+        int Lk = Lt;
+#pragma unroll
+        for (int b = 0; b < lk; ++b)
+          if ((k >> b) & 1) Lk += c.sL[n - 1 - (2 + lt + b)];
+        const int4 e = Ec4[k * T + t];
+        V[4 * k + 0] = e.x + Lk;
+        V[4 * k + 1] = e.y + Lk + Le1;
+        V[4 * k + 2] = e.z + Lk + Le2;
+        V[4 * k + 3] = e.w + Lk + Le1 + Le2;
+      }
+      const int nq = (1 << C) >> 2;
+      const int4* M4 = reinterpret_cast<const int4*>(M);
+#pragma unroll
+      for (int a = 0; a < R; ++a) {
+        const int v = n - C - 1 - a;
+        const int Lv = c.sL[v];
+#pragma unroll
+        for (int k = 0; k < kq; ++k) {
+          const int4 m = M4[(size_t)v * nq + k * T + t];
+          Row[a][4 * k + 0] = m.x + Lv;
+          Row[a][4 * k + 1] = m.y + Lv;
+          Row[a][4 * k + 2] = m.z + Lv;
+          Row[a][4 * k + 3] = m.w + Lv;
+        }
+      }
+    }
+  }
+
+  // --- one walked row in shared memory (position a >= R) added with sign d.
+  __device__ __forceinline__ void add_dyn_row(const WalkCtx& c, int a, int d) {
+    const int rr = a - R;
+    if constexpr (CPT == 1) {
+      const int m = c.rows1[(rr << c.C) + col0];
+      if (d > 0) V[0] += m;
+      else V[0] -= m;
+    } else {
+      constexpr int kq = CPT / 4;
+      const int nq = (1 << c.C) >> 2;
+      const int4* rp = c.rows4 + (size_t)rr * nq + c.thread;
+      if (d > 0) {
+#pragma unroll
+        for (int k = 0; k < kq; ++k) {
+          const int4 m = rp[k * c.nthreads];
+          V[4 * k + 0] += m.x;
+          V[4 * k + 1] += m.y;
+          V[4 * k + 2] += m.z;
+          V[4 * k + 3] += m.w;
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kq; ++k) {
+          const int4 m = rp[k * c.nthreads];
+          V[4 * k + 0] -= m.x;
+          V[4 * k + 1] -= m.y;
+          V[4 * k + 2] -= m.z;
+          V[4 * k + 3] -= m.w;
+        }
+      }
+    }
+  }
+
+  // Flip of a shared-memory position: rows change V, the linear term moves the offset s.
+  __device__ __forceinline__ void dyn_flip(const WalkCtx& c, int a, int d) {
+    add_dyn_row(c, a, d);
+    const int Lv = c.sL[c.n - c.C - 1 - a];
+    if (d > 0) { s += Lv; aux -= Lv; }
+    else { s -= Lv; aux += Lv; }
+  }
+
+  // Walk state at the start of iteration it0 (gray(i0) has only positions >= R set).
+  __device__ __forceinline__ void seek(const WalkCtx& c, int64_t it0) {
+    if (it0 == 0) return;
+    const uint64_t g0 = gray_code(static_cast<uint64_t>(it0) << (R + 1));
+    for (int a = R; a < c.w; ++a)
+      if ((g0 >> a) & 1u) {
+        add_dyn_row(c, a, +1);
+        s += c.sL[c.n - c.C - 1 - a];
+      }
+  }
+
+  // Resolve-mode visit of one step: candidates have V[j] + t <= aux.
+  __device__ __forceinline__ void visit_candidates(const WalkCtx& c, uint64_t prank, uint64_t i, int tv,
+                                                   const double* __restrict__ U64, uint64_t gkey) {
+    const uint64_t ib = prank | (gray_code(i) << c.C);
+#pragma unroll
+    for (int jj = 0; jj < CPT; ++jj) {
+      if (V[jj] + tv <= aux) {
+        const uint64_t rank = ib | static_cast<uint64_t>(CPT == 1 ? col0 : column_of<CPT>(c.thread, c.nthreads, jj));
+        if constexpr (MODE == kModeTiesInt) {
+          ++cnt;
+          rmin = rank < rmin ? rank : rmin;
+        } else if constexpr (MODE == kModeKeyFp) {
+          const uint64_t k = order_key(eval64_rank(U64, c.n, rank));
+          kmin = k < kmin ? k : kmin;
+        } else if constexpr (MODE == kModeTiesFp) {
+          if (order_key(eval64_rank(U64, c.n, rank)) == gkey) {
+            ++cnt;
+            rmin = rank < rmin ? rank : rmin;
+          }
+        }
+      }
+    }
+  }
+
+  __device__ __forceinline__ void step(const WalkCtx& c, uint64_t prank, uint64_t i, int tv,
+                                       const double* __restrict__ U64, uint64_t gkey) {
+    const int m = min_all<CPT>(V);
+    if constexpr (MODE == kModeMin) {
+      aux = __viaddmin_s32(m, tv, aux);
+    } else {
+      const bool hit = valid && (m + tv <= aux);
+      if (__any_sync(0xffffffffu, hit)) {
+        if (hit) visit_candidates(c, prank, i, tv, U64, gkey);
+      }
+    }
+  }
+
+  // Steps L.. of one iteration, unrolled by recursion so that every register row index and
+  // every flip sign is a compile-time constant.
+  template <int L>
+  __device__ __forceinline__ void steps_from(const WalkCtx& c, uint64_t prank, uint64_t base, int64_t iter,
+                                             const int* tv, const double* __restrict__ U64, uint64_t gkey) {
+    if constexpr (L < kSteps) {
+      step(c, prank, base + L, tv[L], U64, gkey);
+      if constexpr (L + 1 < kSteps) {
+        if constexpr (L + 1 == (1 << R)) {
+          // between the two halves: position R, rising on even iterations
+          dyn_flip(c, R, (iter & 1) ? -1 : +1);
+        } else {
+          // register position a < R; its direction depends on L only
+          constexpr int a = ctz_c(L + 1);
+          constexpr int bit = ((L >> a) ^ (L >> (a + 1))) & 1;
+          if constexpr (bit) {
+#pragma unroll
+            for (int jj = 0; jj < CPT; ++jj) V[jj] -= Row[a][jj];
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < CPT; ++jj) V[jj] += Row[a][jj];
+          }
+        }
+      }
+      steps_from<L + 1>(c, prank, base, iter, tv, U64, gkey);
+    }
+  }
+
+  // Walk Gray iterations [it0, it1) of 2^(R+1) steps each. The flip that leaves an iteration is
+  // applied while iter + 1 < it_flip_end (it1 for a closed walk; later for a walk that a
+  // following call continues).
+  __device__ __forceinline__ void walk(const WalkCtx& c, int64_t it0, int64_t it1, int64_t it_flip_end,
+                                       uint64_t prank, const double* __restrict__ U64, uint64_t gkey) {
+    for (int64_t iter = it0; iter < it1; ++iter) {
+      const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
+      int tv[kSteps];
+      if constexpr (kSteps >= 4) {
+        const int4* T4 = reinterpret_cast<const int4*>(c.T) + (base >> 2);
+#pragma unroll
+        for (int q = 0; q < kSteps / 4; ++q) {
+          const int4 x = c.t_global ? __ldg(T4 + q) : T4[q];
+          tv[4 * q + 0] = x.x;
+          tv[4 * q + 1] = x.y;
+          tv[4 * q + 2] = x.z;
+          tv[4 * q + 3] = x.w;
+        }
+      } else {
+        const int2* T2 = reinterpret_cast<const int2*>(c.T) + (base >> 1);
+        const int2 x = c.t_global ? __ldg(T2) : T2[0];
+        tv[0] = x.x;
+        tv[1] = x.y;
+      }
+      steps_from<0>(c, prank, base, iter, tv, U64, gkey);
+      if (iter + 1 < it_flip_end) {
+        const int a = R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1;
+        const uint64_t ilast = base + kSteps - 1;
+        dyn_flip(c, a, ((gray_code(ilast) >> a) & 1u) ? -1 : +1);
+      }
+    }
+  }
+};
+
+// Iterations of 2^(R+1) steps in a walk over w bits (generic variant: R = 0, w may be 0).
+template <int R>
+__host__ __device__ inline int64_t walk_iterations(int w) {
+  return (w >= R + 1) ? (int64_t(1) << (w - R - 1)) : 0;
+}
+
+}  // namespace qgb

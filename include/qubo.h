@@ -1,0 +1,154 @@
+/*
+ * qubo.h -- C ABI of the GB300 exhaustive QUBO solver.
+ *
+ * The library finds, for a dense QUBO matrix Q (n x n, row-major),
+ *     E_min = min over x in {0,1}^n of E(x) = sum_{i,j} Q_ij x_i x_j
+ * (Terastate-per-second QUBO Brute-Force on a Single GPU, §I objective), the minimiser with the
+ * lowest rank, rank(x) = sum_i x_i 2^(n-1-i) (x_0 is the most significant bit: the lexicographic
+ * order of the state space U_N in §II-B, Fig. 2), and the number of states attaining E_min.
+ * Every one of the 2^n states is evaluated: the search is the prefix-suffix decomposition of
+ * §II-A..C (eq. 4 and 8) walked in Gray-code order (§III-B, Algorithm 2, eq. 9), split into
+ * independent fixed-prefix subproblems (§III-C1) and cached column segments (§III-C2).
+ *
+ * Conventions for every entry point:
+ *  - Q is read only during the call; the caller owns all buffers; the library keeps no pointer.
+ *  - Q need not be triangular: E sums over all i, j. Internally Q is folded to the upper
+ *    triangle U_ii = Q_ii, U_ij = Q_ij + Q_ji (i < j), the form §II-A assumes.
+ *  - dtype QUBO_INT32: results are exact. The call fails with QUBO_ERR_RANGE unless
+ *    S = sum_{i<=j} |U_ij| <= 2^30 - 1 (every partial energy the kernels form is a sum of at
+ *    most two sub-sums of U, so int32 arithmetic never overflows).
+ *  - dtype QUBO_FP32: the energy of a state is the fp64 sum of the fp64-folded triangle in fixed
+ *    order (i ascending, j >= i ascending). The search runs on an exact int32 fixed-point image
+ *    of U with a proven error band, and every state inside the band is re-evaluated in fp64, so
+ *    the returned minimiser is the exact fp64 minimiser (lowest rank among equal fp64 values).
+ *    Non-finite entries fail with QUBO_ERR_NONFINITE.
+ *  - out_min_energy receives E_min (exact for int32), out_argmin_x[n] receives x in {0,1}
+ *    (x_0 first), out_tie_count the number of minimisers (for fp32: states with fp64 energy
+ *    equal to E_min). On error no output is written.
+ *  - n must be in [1, 62]. k_prefix <= 0 and cache_bits <= 0 select the planner's choice;
+ *    explicit values that the kernels cannot run return QUBO_ERR_PLAN.
+ *  - Host entry points block until the result is on the host. Calls are serialised internally.
+ */
+#ifndef QUBO_GB300_H
+#define QUBO_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define QUBO_API __attribute__((visibility("default")))
+#else
+#define QUBO_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* dtype codes */
+#define QUBO_INT32 0
+#define QUBO_FP32 1
+
+/* status codes (0 or negative) */
+#define QUBO_OK 0
+#define QUBO_ERR_ARG (-1)       /* n out of range, null pointer, bad dtype, bad slice id */
+#define QUBO_ERR_RANGE (-2)     /* int32: S > 2^30 - 1 */
+#define QUBO_ERR_NONFINITE (-3) /* fp32: NaN or Inf in Q */
+#define QUBO_ERR_PLAN (-4)      /* explicit k_prefix / cache_bits the kernels cannot run */
+#define QUBO_ERR_CUDA (-5)      /* a CUDA call failed (message via qubo_last_error) */
+#define QUBO_ERR_NODEV (-6)     /* no CUDA device */
+#define QUBO_ERR_ABORTED (-7)   /* the call was cancelled by qubo_request_abort() */
+
+/* Device-side result record: one per solved problem (or slice). */
+typedef struct qubo_result {
+  int32_t status;       /* QUBO_OK or an error code found on the device */
+  int32_t reserved;
+  double min_energy;    /* E_min (int32: exact integer; fp32: fp64 energy of argmin) */
+  uint64_t argmin_rank; /* rank of the lowest-rank minimiser; bit n-1-i is x_i */
+  uint64_t tie_count;   /* number of minimisers */
+} qubo_result;
+
+/* Planner decision, for inspection and tests. */
+typedef struct qubo_plan_desc {
+  int n, dtype;
+  int k_prefix;        /* fixed variables per work unit (slice bits) */
+  int cache_bits;      /* cached variables: 2^cache_bits columns held on chip */
+  int walked_bits;     /* Gray-walked variables per unit: n - k_prefix - cache_bits */
+  int register_bits;   /* walked variables whose rows live in registers */
+  int columns_per_thread;
+  int threads_per_block;
+  int blocks;          /* persistent grid */
+  int variant;         /* 0 = generic kernel, 1 = register-cached fast kernel */
+  uint64_t units;      /* work units (fixed prefixes) per call */
+  size_t workspace_bytes;
+  size_t smem_bytes;
+} qubo_plan_desc;
+
+/* Minimise one QUBO. Q is a HOST pointer to n*n int32 or fp32 values (row-major).
+ * (Algorithm 2 of §III-B with the §III-C1 split; inputs Q, A/B sizes; outputs x_opt, E_min.) */
+QUBO_API int qubo_solve(int n, const void* Q, int dtype, int k_prefix, int cache_bits, double* out_min_energy,
+               uint8_t* out_argmin_x, uint64_t* out_tie_count);
+
+/* Minimise over selected slices only: slice s fixes x_0..x_{k-1} to the bits of slice_ids[s]
+ * (bit k-1-f is x_f), k = k_prefix >= 1 (§III-C1: each fixed prefix is an independent
+ * subproblem). Writes one result per slice: out_min_energy[num_slices],
+ * out_argmin_x[num_slices * n] (full-length states), out_tie_count[num_slices]. */
+QUBO_API int qubo_solve_slices(int n, const void* Q, int dtype, int k_prefix, int cache_bits,
+                      const uint64_t* slice_ids, int num_slices, double* out_min_energy,
+                      uint8_t* out_argmin_x, uint64_t* out_tie_count);
+
+/* Minimise over the contiguous slice range [first_slice, first_slice + num_slices) of k_prefix
+ * bits as ONE problem (one result). This is the shard a process solves when the 2^k_prefix
+ * slices are split across devices; the shard results combine by (min energy, then min rank,
+ * summed ties). */
+QUBO_API int qubo_solve_slice_range(int n, const void* Q, int dtype, int k_prefix, int cache_bits,
+                           uint64_t first_slice, uint64_t num_slices, double* out_min_energy,
+                           uint8_t* out_argmin_x, uint64_t* out_tie_count);
+
+/* Batched mode: `batch` independent problems of equal size n, Q = batch consecutive n*n
+ * matrices (host pointer). One thread block solves one problem. Outputs are per problem:
+ * out_min_energy[batch], out_argmin_x[batch * n], out_tie_count[batch]. int32 only. */
+QUBO_API int qubo_solve_batched(int batch, int n, const void* Q, int dtype, double* out_min_energy,
+                       uint8_t* out_argmin_x, uint64_t* out_tie_count);
+
+/* ---- device-resident entry points (PyTorch or the caller owns memory and streams) ----
+ * d_Q: DEVICE pointer to the input; d_workspace: device buffer of at least the size the
+ * matching *_workspace_bytes call returns (256-byte aligned); cuda_stream: a cudaStream_t
+ * (NULL = legacy default stream). The call only enqueues work and returns; d_result is
+ * written on the stream (status included). Host-detectable errors are returned directly. */
+QUBO_API size_t qubo_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits);
+QUBO_API int qubo_solve_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits, void* d_workspace,
+                      size_t workspace_bytes, void* cuda_stream, qubo_result* d_result);
+
+QUBO_API size_t qubo_batched_workspace_bytes(int batch, int n, int dtype);
+QUBO_API int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void* d_workspace,
+                              size_t workspace_bytes, void* cuda_stream, qubo_result* d_results);
+
+/* Planner decision for qubo_solve(n, ., dtype, k_prefix, cache_bits) on the current device. */
+QUBO_API int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* out);
+
+/* Number of kernel launches the last host or device call enqueued. */
+QUBO_API int qubo_last_launch_count(void);
+
+/* Text for a status code; the last CUDA error text for QUBO_ERR_CUDA. */
+QUBO_API const char* qubo_status_string(int status);
+QUBO_API const char* qubo_last_error(void);
+
+/* Cancellation: a host flag checked between kernel launches of the current and later calls
+ * (never polled inside a kernel). qubo_clear_abort() re-arms. */
+QUBO_API void qubo_request_abort(void);
+QUBO_API void qubo_clear_abort(void);
+
+/* ---- measurement ----
+ * ALU throughput microbenchmark on the current device: runs `iters` iterations of 16
+ * independent chains of one operation per thread on every SM and reports warp-lane
+ * operations per second and the SM clock seen by the kernel (clock64 / globaltimer).
+ * kind: 0 int32 add, 1 int32 min, 2 int32 3-input min, 3 int32 add-then-min (fused),
+ *       4 fp32 add, 5 fp32 min. */
+QUBO_API int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QUBO_GB300_H */

@@ -1,0 +1,285 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on identical seeded inputs.
+
+int32: bit-exact (minimum energy, lowest-rank argmin, tie count).
+fp32:  the returned energy is the fixed-order fp64 energy of the returned state, and it lies
+       within 1e-3 * sum|Q_ij| * 2^-20 of the oracle's fp64 minimum.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import qubo_instances as qi
+
+pytestmark = pytest.mark.gpu
+
+O = oracle.get()
+
+
+@pytest.fixture(scope="module")
+def q():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_qubo_exhaustive_gb300 as lib
+    return lib
+
+
+def fp32_tol(Q):
+    return 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+
+
+def check_int(q, Q, **kw):
+    e, x, t = q.solve(Q, **kw)
+    want = O.solve(Q)
+    assert (e, t) == (want[0], want[2]), (e, t, want)
+    assert (x == want[1]).all()
+    return e, x, t
+
+
+# ---------------------------------------------------------------- exhaustive small sweeps
+
+@pytest.mark.parametrize("n", list(range(1, 17)))
+def test_small_n_sweep(q, n):
+    for seed, (lo, hi) in enumerate([(-100, 100), (-2, 2), (-1, 1), (0, 3)]):
+        check_int(q, qi.random_upper_int(n, lo, hi, 1000 * n + seed))
+    check_int(q, qi.random_full_int(n, -50, 50, 7 * n))  # non-triangular input
+
+
+@pytest.mark.parametrize("n", [1, 2, 7, 12, 17, 20])
+def test_zero_matrix_all_states_tie(q, n):
+    e, x, t = q.solve(np.zeros((n, n), np.int32))
+    assert e == 0 and t == 1 << n and not x.any()
+
+
+@pytest.mark.parametrize("n", [5, 14, 19])
+def test_diagonal_closed_form(q, n):
+    d = qi.Stream(n).integers(-3, 3, n)
+    e, x, t = q.solve(np.diag(d).astype(np.int32))
+    assert e == int(np.minimum(d, 0).sum())
+    assert (x == (d < 0)).all()
+    assert t == 1 << int((d == 0).sum())
+
+
+# every kernel variant and split: explicit (k_prefix, cache_bits)
+@pytest.mark.parametrize("n,k,c", [
+    (16, 0, 9), (17, 0, 12), (18, 1, 12), (20, 3, 12), (20, 0, 9), (21, 4, 10), (22, 2, 11),
+    (20, 6, 9), (14, 2, 6), (12, 0, 10), (13, 5, 3), (15, 14, 1), (10, 4, 6), (18, 8, 10), (9, 9, 0),
+])
+def test_explicit_plans(q, n, k, c):
+    for seed, (lo, hi) in enumerate([(-100, 100), (-1, 1)]):
+        Q = qi.random_upper_int(n, lo, hi, 77 * n + 3 * k + c + seed)
+        check_int(q, Q, k_prefix=k, cache_bits=c)
+
+
+def test_infeasible_explicit_plan_is_an_error(q):
+    Q = qi.random_upper_int(20, -9, 9, 2)
+    with pytest.raises(q.QuboError) as ei:
+        q.solve(Q, k_prefix=2, cache_bits=16)
+    assert ei.value.status == -4
+
+
+def test_plans_pick_fast_kernel_for_large_n(q):
+    p = q.plan(40)
+    assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
+    assert q.plan(8)["variant"] == 0
+
+
+# ---------------------------------------------------------------- configs
+
+def test_n20_config(q):
+    Q = qi.workload_n20()
+    e, x, t = check_int(q, Q)
+    assert O.direct_i64(O.fold_i32(Q)) == (e, oracle.rank_of_bits(x), t)
+
+
+def test_n24_random_and_ties(q):
+    check_int(q, qi.random_upper_int(24, -1000, 1000, 5))
+    check_int(q, qi.random_upper_int(24, -1, 1, 6))
+
+
+def test_n32_config(q):
+    check_int(q, qi.workload_n32())
+
+
+def test_n32_mattis_planted(q):
+    Q, s_star, w, offset = qi.workload_n32_mattis()
+    differ = np.not_equal.outer(s_star, s_star)
+    e_want = -2 * int(np.triu(w * differ, 1).sum())
+    xs = ((1 + s_star) // 2).astype(np.uint8)
+    x_want = xs if xs[0] == 0 else 1 - xs
+    e, x, t = q.solve(Q)
+    assert e == e_want and t == 2 and (x == x_want).all()
+
+
+def test_n40_slices_against_oracle(q):
+    Q = qi.workload_n40()
+    k = 12
+    ids = qi.Stream(4040).integers(0, (1 << k) - 1, 6).astype(np.uint64)
+    e, x, t = q.solve_slices(Q, k, ids)
+    for s, sid in enumerate(ids):
+        want = O.solve_slice(Q, k, int(sid))
+        assert (int(e[s]), int(t[s])) == (want[0], want[2])
+        assert (x[s] == want[1]).all()
+
+
+def test_n40_full_solve_consistent_with_sampled_slices(q):
+    Q = qi.workload_n40()
+    e, x, t = q.solve(Q)
+    assert t >= 1
+    U = O.fold_i32(Q)
+    assert O.energy_i64(U, x) == e  # the reported state has the reported energy
+    k = 12
+    sid = oracle.rank_of_bits(x[:k])
+    want = O.solve_slice(Q, k, sid)  # the slice holding the argmin has the same optimum
+    assert want[0] == e and (want[1] == x).all() and 1 <= want[2] <= t
+    for sid2 in qi.Stream(41).integers(0, (1 << k) - 1, 3):
+        assert O.solve_slice(Q, k, int(sid2))[0] >= e
+
+
+def test_slice_range_shards_combine_to_whole(q):
+    Q = qi.random_upper_int(26, -300, 300, 9)
+    whole = q.solve(Q)
+    k = 6
+    parts = [q.solve_slice_range(Q, k, a, 16) for a in range(0, 64, 16)]
+    best = min(p[0] for p in parts)
+    ties = sum(p[2] for p in parts if p[0] == best)
+    first = min(oracle.rank_of_bits(p[1]) for p in parts if p[0] == best)
+    assert (best, first, ties) == (whole[0], oracle.rank_of_bits(whole[1]), whole[2])
+
+
+# ---------------------------------------------------------------- fp32
+
+@pytest.mark.parametrize("n,seed", [(1, 0), (5, 1), (12, 2), (18, 3), (22, 4), (26, 5)])
+def test_fp32_against_oracle(q, n, seed):
+    Q = qi.random_symmetric_normal_f32(n, seed)
+    e, x, t = q.solve(Q)
+    want = O.solve(Q)
+    U = O.fold_f32(Q)
+    assert O.eval64(U, x) == e
+    assert abs(e - want[0]) <= fp32_tol(Q)
+    assert (x == want[1]).all() and t == want[2]
+
+
+def test_fp32_degenerate_inputs(q):
+    e, x, t = q.solve(np.zeros((10, 10), np.float32))
+    assert e == 0.0 and t == 1024 and not x.any()
+    d = np.array([0.5, -1.25, 0.0, -3.0, 2.0, -0.125], np.float32)
+    e, x, t = q.solve(np.diag(d))
+    assert e == float(np.minimum(d, 0).astype(np.float64).sum()) and t == 2 and (x == (d < 0)).all()
+    tiny = (qi.random_symmetric_normal_f32(9, 3) * np.float32(1e-30)).astype(np.float32)
+    e, x, t = q.solve(tiny)
+    want = O.solve(tiny)
+    assert e == want[0] and (x == want[1]).all()
+
+
+def test_fp32_nonfinite_rejected(q):
+    Q = qi.random_symmetric_normal_f32(6, 1)
+    Q[2, 3] = np.nan
+    with pytest.raises(q.QuboError) as ei:
+        q.solve(Q)
+    assert ei.value.status == -3
+    Q[2, 3] = np.inf
+    with pytest.raises(q.QuboError):
+        q.solve(Q)
+
+
+def test_n36_fp32_config_on_slices(q):
+    Q = qi.workload_n36_f32()
+    e, x, t = q.solve(Q)
+    U = O.fold_f32(Q)
+    assert O.eval64(U, x) == e
+    k = 14
+    sid = oracle.rank_of_bits(x[:k])
+    want = O.solve_slice(Q, k, sid)
+    assert abs(want[0] - e) <= fp32_tol(Q) and (want[1] == x).all()
+    ids = qi.Stream(3636).integers(0, (1 << k) - 1, 4).astype(np.uint64)
+    es, xs, ts = q.solve_slices(Q, k, ids)
+    for s, sid2 in enumerate(ids):
+        w2 = O.solve_slice(Q, k, int(sid2))
+        assert abs(es[s] - w2[0]) <= fp32_tol(Q) and (xs[s] == w2[1]).all()
+        assert w2[0] >= e - fp32_tol(Q)
+
+
+# ---------------------------------------------------------------- errors and edges
+
+def test_int32_range_error(q):
+    Q = np.full((8, 8), 1 << 26, np.int32)
+    with pytest.raises(q.QuboError) as ei:
+        q.solve(Q)
+    assert ei.value.status == -2
+
+
+def test_range_limit_is_exact(q):
+    # sum |U| = 2^30 - 1 passes, one more fails
+    n = 4
+    Q = np.zeros((n, n), np.int32)
+    Q[0, 0] = -((1 << 30) - 1)
+    e, x, t = q.solve(Q)
+    assert e == -((1 << 30) - 1) and x[0] == 1 and t == 1 << (n - 1)
+    Q[1, 1] = 1
+    with pytest.raises(q.QuboError):
+        q.solve(Q)
+
+
+def test_slices_argument_checks(q):
+    Q = qi.random_upper_int(20, -9, 9, 1)
+    with pytest.raises(q.QuboError):
+        q.solve_slices(Q, 4, [16])  # id out of range
+    with pytest.raises(q.QuboError):
+        q.solve_slices(Q, 0, [0])
+
+
+# ---------------------------------------------------------------- batched
+
+def test_batched_against_oracle(q):
+    Qs = qi.batched_upper_int(64, 24, -50, 50, 99)
+    e, x, t = q.solve_batched(Qs)
+    for b in range(0, 64, 4):
+        want = O.solve(Qs[b])
+        assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all()
+    for b in range(64):
+        assert O.energy_i64(O.fold_i32(Qs[b]), x[b]) == e[b] and t[b] >= 1
+
+
+def test_batched_ties_and_other_sizes(q):
+    Qs = np.stack([qi.random_upper_int(20, -1, 1, s) for s in range(6)] + [np.zeros((20, 20), np.int32)])
+    e, x, t = q.solve_batched(Qs)
+    for b in range(Qs.shape[0]):
+        want = O.solve(Qs[b])
+        assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all()
+    Qs = qi.batched_upper_int(5, 9, -20, 20, 5)  # below the block kernel's size: per-instance path
+    e, x, t = q.solve_batched(Qs)
+    for b in range(5):
+        want = O.solve(Qs[b])
+        assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all()
+
+
+# ---------------------------------------------------------------- device-resident entry point
+
+def test_device_entry_point(q):
+    import torch
+    Q = qi.random_upper_int(28, -500, 500, 12)
+    n = 28
+    dq = torch.from_numpy(Q).cuda()
+    nbytes = q.workspace_bytes(n)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    res = torch.zeros(32, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+    q.solve_device(n, dq, q.INT32, ws, nbytes, stream.cuda_stream, res)
+    torch.cuda.synchronize()
+    r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
+    want = O.solve(Q)
+    assert r["status"] == 0
+    assert (int(r["min_energy"]), int(r["tie_count"])) == (want[0], want[2])
+    assert int(r["argmin_rank"]) == oracle.rank_of_bits(want[1])
+    assert q.last_launch_count() >= 5
+
+
+def test_single_slice_and_single_range_use_their_own_prefix(q):
+    Q = qi.random_upper_int(24, -200, 200, 31)
+    for sid in (0, 5, 63):
+        e, x, t = q.solve_slices(Q, 6, [sid])
+        want = O.solve_slice(Q, 6, sid)
+        assert (int(e[0]), int(t[0])) == (want[0], want[2]) and (x[0] == want[1]).all()
+        e1, x1, t1 = q.solve_slice_range(Q, 6, sid, 1)
+        assert (e1, t1) == (want[0], want[2]) and (x1 == want[1]).all()
