@@ -1,0 +1,387 @@
+#!/usr/bin/env python
+"""Benchmark: QUBO states evaluated per second at n=40 (int32) on GB300.
+
+One step = one complete exhaustive search of the n=40 dense int32 workload (2^40 states:
+fold/validate, cache construction, enumeration, group minimum, tie list, resolution, result
+record) through the library's C ABI.
+
+  value : device-resident input (qubo_solve_device), CUDA events on the launching stream around
+          each step, L2 flushed (256 MB write) between steps outside the events.
+  e2e   : the host API (qubo_solve) from pinned host memory: H2D of Q and D2H of the result are
+          inside the timed region (wall clock, synchronised).
+  roofline: the enumeration kernel's own duration (CUDA events the library records around its
+          launches), one int32 add per state, against the INT32 issue roofline of the part:
+          152 SMs x 128 lanes/clk x 2.07 GHz.
+  cpu_baseline / --impl reference: the CPU oracle (test infrastructure, plain C + OpenMP) on a
+          bounded sample of the same workload, on the host's cores.
+
+Multi-GPU (torchrun, one process per GPU): weak scaling -- every rank solves its own independent
+n=40 instance (independent problems need no exchange); value counts the states of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import qubo_instances as qi  # noqa: E402
+
+METRIC = "QUBO states evaluated/sec at n=40 int32 on 1 GB300; % of INT32-add roofline"
+UNIT = "states/s"
+N = 40
+STATES = 1 << N
+WORKLOAD = "n=40 dense QUBO, int32 Q upper-triangular incl. diagonal, entries iid uniform integers in [-1000,1000]"
+SMS = 152
+LANES_PER_CLK = 128          # issue-limited int32 lanes per SM per clock (ALU + FMA-heavy pipes)
+MAX_SM_MHZ = 2070.0
+PROFILE = os.path.join(ROOT, "profiles", "search_kernel_n40.md")
+KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_fast.cu"]
+
+
+def log(*a):
+    print(*a, file=sys.stderr, flush=True)
+
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "exact_qubo_exhaustive_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per enumeration launch from the committed ncu summary, if it describes this kernel."""
+    try:
+        text = open(PROFILE).read()
+    except OSError:
+        return None, "no ncu summary"
+    kv = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            kv[k.strip()] = v.strip().strip("`")
+    if kv.get("kernel_source_sha256") != kernel_source_hash():
+        return None, "kernel changed since the ncu capture"
+    try:
+        return float(kv["traffic_bytes_per_launch_n40"]), "ncu capture (scaled to a full n=40 launch)"
+    except (KeyError, ValueError):
+        return None, "ncu summary without traffic"
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[3:7]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def oracle_sample(seconds: float):
+    """States/s of the CPU oracle on n=40 slices of 2^24 states (k=16), stopping after `seconds`."""
+    import oracle
+    O = oracle.get()
+    Q = qi.workload_n40()
+    U = O.fold_i32(Q)
+    k = 16
+    ids = qi.Stream(2026).integers(0, (1 << k) - 1, 4096)
+    t0 = time.perf_counter()
+    done = 0
+    for sid in ids:
+        O.gray_i64(U, k, int(sid))
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    states = done << (N - k)
+    return {"value": states / dt, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
+            "sample": f"{done} slices x 2^{N - k} states of the n=40 workload (first {k} variables fixed), "
+                      f"{dt:.1f} s, Gray-walk oracle (O(n) per state) on all host threads"}
+
+
+def config_dict(plan=None):
+    cfg = {"workload": WORKLOAD, "n": N, "states_per_step": STATES, "seed": qi.MASTER_SEED + 2,
+           "l2": "flushed between steps (256 MB device write outside the timed events)"}
+    if plan:
+        cfg.update({"k_prefix": plan["k_prefix"], "cache_bits": plan["cache_bits"],
+                    "walked_bits": plan["walked_bits"], "blocks": plan["blocks"],
+                    "threads_per_block": plan["threads_per_block"]})
+    return cfg
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    O = oracle.get()
+    Q = qi.workload_n40()
+    U = O.fold_i32(Q)
+    k = 18  # each step: a bounded sample of 8 slices of 2^22 states
+    ids = qi.Stream(777).integers(0, (1 << k) - 1, 8 * (args.steps + args.warmup))
+    per_step = 8
+    for s in range(args.warmup):
+        for sid in ids[s * per_step:(s + 1) * per_step]:
+            O.gray_i64(U, k, int(sid))
+    t0 = time.perf_counter()
+    for s in range(args.warmup, args.warmup + args.steps):
+        for sid in ids[s * per_step:(s + 1) * per_step]:
+            O.gray_i64(U, k, int(sid))
+    dt = time.perf_counter() - t0
+    states = args.steps * per_step * (1 << (N - k))
+    value = states / dt
+    sample = f"each step: {per_step} slices x 2^{N - k} states of the n=40 workload; CPU oracle, all host threads"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "data": "synthetic", "config": config_dict(),
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    import exact_qubo_exhaustive_gb300 as q
+
+    Q = qi.workload_n40() if rank == 0 else qi.random_upper_int(N, -1000, 1000, qi.MASTER_SEED + 2 + 7919 * rank)
+    plan = q.plan(N)
+    dq = torch.from_numpy(Q).to(dev)
+    nbytes = q.workspace_bytes(N)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    res = torch.zeros(32, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    q.enable_kernel_timing(True)
+
+    def step():
+        q.solve_device(N, dq, q.INT32, ws, nbytes, stream.cuda_stream, res)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    launches_per_step = q.last_launch_count()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    kernel_ms = []
+    barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+        kernel_ms.append(q.kernel_time_ms())
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = sum(step_ms) / args.steps
+    kern = sum(kernel_ms) / len(kernel_ms)
+    r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
+    if int(r["status"]) != 0:
+        raise RuntimeError(f"search failed: status {int(r['status'])}")
+
+    # end to end through the host API, from pinned host memory
+    pinned = torch.empty((N, N), dtype=torch.int32, pin_memory=True)
+    pinned.copy_(torch.from_numpy(Q))
+    Qh = pinned.numpy()
+    q.solve(Qh)
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        q.solve(Qh)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e = sum(e2e_ms) / len(e2e_ms)
+
+    if world > 1:
+        t = torch.tensor([ms, e2e, kern], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms, e2e, kern = (float(v) for v in t.tolist())
+
+    value = world * STATES / (ms * 1e-3)
+    e2e_value = world * STATES / (e2e * 1e-3)
+    achieved = STATES / (kern * 1e-3) / 1e12  # int32 adds (one per state) per second, in T/s
+    peak = SMS * LANES_PER_CLK * MAX_SM_MHZ * 1e6 / 1e12
+    traffic, traffic_src = profiled_traffic()
+
+    extra = {}
+    if rank == 0 and world == 1 and not args.no_extra:
+        extra = other_configs(q, torch, dev, stream)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = oracle_sample(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded uniform integers, no dataset)",
+            "config": config_dict(plan),
+            "result": {"min_energy": float(r["min_energy"]), "argmin_rank": int(r["argmin_rank"]),
+                       "tie_count": int(r["tie_count"])},
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "kernel": "search_kernel<16,4,min> (enumeration)", "kernel_ms": kern,
+                         "peak_basis": "152 SMs x 128 int32 lanes/clk (issue limit; ALU + FMA-heavy pipes, "
+                                       "measured by the add probe) x 2.07 GHz max SM clock",
+                         "traffic_source": traffic_src,
+                         "frac_at_measured_clock": (achieved / (SMS * LANES_PER_CLK * clocks["sm_mhz"] * 1e-6)
+                                                    if clocks.get("sm_mhz") else None)},
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": N * N * 4,
+                    "d2h_bytes_per_step": 32, "ms_per_step": e2e},
+            "cpu_baseline": cpu,
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "other_configs": extra,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def other_configs(q, torch, dev, stream):
+    """Device-timed rates of the other workloads (one timed run each, for context)."""
+    out = {}
+
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    for name, n, Q, dt in (("n36_fp32", 36, qi.workload_n36_f32(), q.FP32), ("n32_int32", 32, qi.workload_n32(), q.INT32),
+                           ("n20_int32", 20, qi.workload_n20(), q.INT32)):
+        dq = torch.from_numpy(Q).to(dev)
+        nb = q.workspace_bytes(n, dt)
+        ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        res = torch.zeros(32, dtype=torch.uint8, device=dev)
+        ms = timed(lambda: q.solve_device(n, dq, dt, ws, nb, stream.cuda_stream, res))
+        out[name] = {"ms": ms, "states_per_s": (1 << n) / (ms * 1e-3)}
+    Qs = qi.workload_batched()
+    dq = torch.from_numpy(Qs).to(dev)
+    nb = max(q.batched_workspace_bytes(4096, 24), 256)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    res = torch.zeros(4096 * 32, dtype=torch.uint8, device=dev)
+    ms = timed(lambda: q.solve_batched_device(4096, 24, dq, ws, nb, stream.cuda_stream, res))
+    out["batched_4096x_n24_int32"] = {"ms": ms, "states_per_s": 4096 * (1 << 24) / (ms * 1e-3)}
+    return out
+
+
+def profile_case(n: int, dtype_name: str):
+    """Two searches of an n-variable instance shaped like the workload (for ncu captures)."""
+    import torch
+    import exact_qubo_exhaustive_gb300 as q
+    if dtype_name == "fp32":
+        Q, dt = qi.random_symmetric_normal_f32(n, qi.MASTER_SEED + 3), q.FP32
+    else:
+        Q, dt = qi.random_upper_int(n, -1000, 1000, qi.MASTER_SEED + 2), q.INT32
+    dq = torch.from_numpy(Q).cuda()
+    nb = q.workspace_bytes(n, dt)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    res = torch.zeros(32, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(2):
+        q.solve_device(n, dq, dt, ws, nb, s.cuda_stream, res)
+    torch.cuda.synchronize()
+    r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
+    log(f"profile case n={n} {dtype_name}: plan={q.plan(n, dt)} result={r}")
+    return 0 if int(r["status"]) == 0 else 1
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--profile-case", type=int, default=0, metavar="N",
+                    help="only run two searches of an N-variable instance (for ncu), print no JSON")
+    ap.add_argument("--profile-dtype", choices=["int32", "fp32"], default="int32")
+    args = ap.parse_args(argv)
+    if args.profile_case:
+        return profile_case(args.profile_case, args.profile_dtype)
+    if args.warmup < 3:
+        log("warmup raised to 3 (timing rule)")
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gb300(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

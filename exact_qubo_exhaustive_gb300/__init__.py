@@ -2,7 +2,7 @@
 
 Thin Python binding of the C ABI in include/qubo.h (argument marshalling only; every step of
 the search runs in the CUDA kernels of libqubo_gb300.so). The library must have been built
-(`python -m exact_qubo_exhaustive_gb300.build` or __graft_entry__.build()); there is no CPU
+(`python exact_qubo_exhaustive_gb300/build.py` or __graft_entry__.build()); there is no CPU
 fallback, and importing the binding without the library raises ImportError.
 
     E(x) = sum_{i,j} Q_ij x_i x_j,  x in {0,1}^n   (Terastate-per-second QUBO Brute-Force, §I)
@@ -20,7 +20,8 @@ import numpy as np
 __all__ = [
     "QuboError", "INT32", "FP32", "solve", "solve_slices", "solve_slice_range", "solve_batched",
     "solve_device", "solve_batched_device", "workspace_bytes", "batched_workspace_bytes", "plan",
-    "probe_alu", "last_launch_count", "status_string", "last_error", "request_abort", "clear_abort",
+    "probe_alu", "last_launch_count", "slice_range_workspace_bytes", "solve_slice_range_device",
+    "enable_kernel_timing", "kernel_time_ms", "status_string", "last_error", "request_abort", "clear_abort",
     "library_path", "RESULT_DTYPE",
 ]
 
@@ -36,7 +37,7 @@ def library_path() -> str:
 
 
 if not os.path.exists(_LIB_PATH):
-    raise ImportError(f"{_LIB_PATH} is missing: build it with `python -m exact_qubo_exhaustive_gb300.build` "
+    raise ImportError(f"{_LIB_PATH} is missing: build it with `python exact_qubo_exhaustive_gb300/build.py` "
                       "(the CUDA library is required; there is no CPU path)")
 
 _lib = ctypes.CDLL(_LIB_PATH)
@@ -71,6 +72,13 @@ _sig = {
     "qubo_solve_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
     "qubo_batched_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int]),
+    "qubo_slice_range_workspace_bytes": (ctypes.c_size_t, [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                                           ctypes.c_uint64]),
+    "qubo_solve_slice_range_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                     ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p,
+                                                     ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "qubo_enable_kernel_timing": (None, [ctypes.c_int]),
+    "qubo_kernel_time_ms": (ctypes.c_double, []),
     "qubo_solve_batched_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                  ctypes.c_void_p]),
@@ -193,6 +201,27 @@ def solve_device(n: int, d_Q, dtype: int, workspace, workspace_nbytes: int, stre
     tensors with data_ptr()); stream is a cudaStream_t handle (int) or None. Asynchronous."""
     _check(_lib.qubo_solve_device(n, _ptr(d_Q), dtype, k_prefix, cache_bits, _ptr(workspace), workspace_nbytes,
                                   _ptr(stream) if stream is not None else 0, _ptr(d_result)))
+
+
+def slice_range_workspace_bytes(n: int, dtype: int, k_prefix: int, num_slices: int, cache_bits: int = 0) -> int:
+    return int(_lib.qubo_slice_range_workspace_bytes(n, dtype, k_prefix, cache_bits, num_slices))
+
+
+def solve_slice_range_device(n: int, d_Q, dtype: int, k_prefix: int, first_slice: int, num_slices: int, workspace,
+                             workspace_nbytes: int, stream, d_result, cache_bits: int = 0) -> None:
+    """Enqueue the search of slices [first_slice, first_slice + num_slices) on device memory."""
+    _check(_lib.qubo_solve_slice_range_device(n, _ptr(d_Q), dtype, k_prefix, cache_bits, first_slice, num_slices,
+                                              _ptr(workspace), workspace_nbytes,
+                                              _ptr(stream) if stream is not None else 0, _ptr(d_result)))
+
+
+def enable_kernel_timing(enable: bool = True) -> None:
+    _lib.qubo_enable_kernel_timing(1 if enable else 0)
+
+
+def kernel_time_ms() -> float:
+    """Elapsed ms of the enumeration launches of the most recent call (events on its stream)."""
+    return float(_lib.qubo_kernel_time_ms())
 
 
 def solve_batched_device(batch: int, n: int, d_Q, workspace, workspace_nbytes: int, stream, d_results) -> None:

@@ -1,7 +1,7 @@
 """Build the CUDA library (libqubo_gb300.so) in-tree with nvcc for sm_103a.
 
 Every translation unit under csrc/ is compiled in parallel, then linked into one shared
-library next to this file. Run as `python -m exact_qubo_exhaustive_gb300.build`.
+library next to this file. Run as `python exact_qubo_exhaustive_gb300/build.py`.
 """
 from __future__ import annotations
 

@@ -19,6 +19,25 @@ std::mutex g_mu;
 std::string g_last_error;
 int g_last_launches = 0;
 volatile int g_abort = 0;
+bool g_timing_enabled = false;
+int g_timing_device = -1;
+KernelTiming g_timing;
+bool g_timing_recorded = false;
+
+// Events around the min-pass launches of the next calls, when kernel timing is enabled.
+const KernelTiming* timing_for_call(int dev) {
+  if (!g_timing_enabled) return nullptr;
+  if (g_timing_device != dev) {
+    if (g_timing.start) cudaEventDestroy(g_timing.start);
+    if (g_timing.stop) cudaEventDestroy(g_timing.stop);
+    g_timing = KernelTiming();
+    if (cudaEventCreate(&g_timing.start) != cudaSuccess || cudaEventCreate(&g_timing.stop) != cudaSuccess)
+      return nullptr;
+    g_timing_device = dev;
+  }
+  g_timing_recorded = true;
+  return &g_timing;
+}
 
 struct DeviceBuffers {
   int device = -1;
@@ -256,7 +275,7 @@ int host_search(const Plan& p, const void* Q, const uint64_t* gbase_host, std::v
   }
   int nl = 0;
   bool aborted = false;
-  e = run_search(p, g_buf.dq, w, w.results, s, &nl, &g_abort, &aborted);
+  e = run_search(p, g_buf.dq, w, w.results, s, &nl, &g_abort, &aborted, timing_for_call(g_buf.device));
   g_last_launches = nl;
   if (aborted) {
     cudaStreamSynchronize(s);
@@ -397,7 +416,8 @@ int qubo_solve_device(int n, const void* d_Q, int dtype, int k_prefix, int cache
   Work w = layout_workspace(p, static_cast<unsigned char*>(d_workspace));
   if (w.bytes > workspace_bytes) return QUBO_ERR_ARG;
   int nl = 0;
-  cudaError_t e = run_search(p, d_Q, w, d_result, static_cast<cudaStream_t>(cuda_stream), &nl, nullptr, nullptr);
+  cudaError_t e = run_search(p, d_Q, w, d_result, static_cast<cudaStream_t>(cuda_stream), &nl, nullptr, nullptr,
+                             timing_for_call(dev));
   g_last_launches = nl;
   if (e != cudaSuccess) return set_cuda_error(e, "kernel launch");
   return QUBO_OK;
@@ -485,6 +505,66 @@ int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void
   g_last_launches = nl;
   if (e != cudaSuccess) return set_cuda_error(e, "batched launch");
   return QUBO_OK;
+}
+
+size_t qubo_slice_range_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits, uint64_t num_slices) {
+  if (n < 1 || n > 62 || (dtype != QUBO_INT32 && dtype != QUBO_FP32) || k_prefix < 1 || k_prefix >= n ||
+      num_slices < 1)
+    return 0;
+  int dev;
+  if (current_device(&dev)) return 0;
+  Plan p;
+  if (make_plan(n, dtype, k_prefix, cache_bits, k_prefix, num_slices, false, &p)) return 0;
+  p.ngroups = 1;
+  p.upg = num_slices << (p.F - k_prefix);
+  p.total_units = p.upg;
+  return layout_workspace(p, nullptr).bytes;
+}
+
+int qubo_solve_slice_range_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits,
+                                  uint64_t first_slice, uint64_t num_slices, void* d_workspace,
+                                  size_t workspace_bytes, void* cuda_stream, qubo_result* d_result) {
+  int st = check_common(n, d_Q, dtype);
+  if (st) return st;
+  if (k_prefix < 1 || k_prefix >= n || num_slices < 1 || !d_workspace || !d_result ||
+      (reinterpret_cast<uintptr_t>(d_workspace) & 255))
+    return QUBO_ERR_ARG;
+  if (first_slice + num_slices > ((uint64_t)1 << k_prefix) || first_slice + num_slices < first_slice)
+    return QUBO_ERR_ARG;
+  if (g_abort) return QUBO_ERR_ABORTED;
+  int dev;
+  if ((st = current_device(&dev))) return st;
+  Plan p;
+  if ((st = make_plan(n, dtype, k_prefix, cache_bits, k_prefix, num_slices, false, &p))) return st;
+  const int s_bits = p.F - k_prefix;
+  p.ngroups = 1;
+  p.upg = num_slices << s_bits;
+  p.total_units = p.upg;
+  if (p.total_units >= ((uint64_t)1 << 32)) return QUBO_ERR_PLAN;
+  p.gbase0 = first_slice << s_bits;
+  Work w = layout_workspace(p, static_cast<unsigned char*>(d_workspace));
+  if (w.bytes > workspace_bytes) return QUBO_ERR_ARG;
+  int nl = 0;
+  cudaError_t e = run_search(p, d_Q, w, d_result, static_cast<cudaStream_t>(cuda_stream), &nl, nullptr, nullptr,
+                             timing_for_call(dev));
+  g_last_launches = nl;
+  if (e != cudaSuccess) return set_cuda_error(e, "kernel launch");
+  return QUBO_OK;
+}
+
+void qubo_enable_kernel_timing(int enable) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  g_timing_enabled = enable != 0;
+  g_timing_recorded = false;
+}
+
+double qubo_kernel_time_ms(void) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_timing_enabled || !g_timing_recorded || !g_timing.stop) return -1.0;
+  if (cudaEventSynchronize(g_timing.stop) != cudaSuccess) return -1.0;
+  float ms = 0.f;
+  if (cudaEventElapsedTime(&ms, g_timing.start, g_timing.stop) != cudaSuccess) return -1.0;
+  return (double)ms;
 }
 
 int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* out) {

@@ -51,7 +51,8 @@ struct Plan {
   uint64_t upg = 1;        // units per group
   uint64_t total_units = 1;
   size_t smem_bytes = 0;   // dynamic shared memory of the enumeration kernels
-  bool host_gbase = false; // group bases uploaded by the host (else one group at unit 0)
+  bool host_gbase = false; // group bases uploaded by the host (else one group, written on device)
+  uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
 };
 
 // Device pointers into one workspace.
@@ -78,9 +79,13 @@ Work layout_workspace(const Plan& p, unsigned char* base);
 
 // Kernel launch sequence for one plan on `stream`. d_Q is the device input, `res` receives
 // one qubo_result per group. Returns cudaSuccess or the first launch error; `launches` counts.
-// A set abort flag stops before the next min-pass launch and sets *aborted.
+// A set abort flag stops before the next min-pass launch and sets *aborted. When `timing` is
+// non-null, its two events are recorded around the min-pass launches.
+struct KernelTiming {
+  cudaEvent_t start = nullptr, stop = nullptr;
+};
 cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
-                       int* launches, const volatile int* abort_flag, bool* aborted);
+                       int* launches, const volatile int* abort_flag, bool* aborted, const KernelTiming* timing);
 
 // Batched mode (one block per instance).
 struct BatchPlan {

@@ -14,7 +14,8 @@ namespace qgb {
 //          minimiser lies within band = n(n+1)/2 image units of the image minimum.
 // ------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void* __restrict__ Qv, DevHeader* hdr,
-                                                   int32_t* U, double* U64, uint64_t* gbase0) {
+                                                   int32_t* U, double* U64, uint64_t* gbase0,
+                                                   uint64_t gbase0_value) {
   __shared__ unsigned long long s_sum;
   __shared__ int s_bad;
   __shared__ double s_part[256];
@@ -23,7 +24,7 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
   if (tid == 0) {
     s_sum = 0;
     s_bad = 0;
-    if (gbase0) *gbase0 = 0;
+    if (gbase0) *gbase0 = gbase0_value;
   }
   __syncthreads();
   if (dtype == QUBO_INT32) {
@@ -267,13 +268,14 @@ static cudaError_t launch_search(const Plan& p, int mode, const KParams& kp, int
 }
 
 cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
-                       int* launches, const volatile int* abort_flag, bool* aborted) {
+                       int* launches, const volatile int* abort_flag, bool* aborted, const KernelTiming* timing) {
   int nl = 0;
   if (aborted) *aborted = false;
   cudaError_t e;
   // gbase: uploaded by the host for slices and ranges; otherwise one group starting at unit 0,
   // written by the prep kernel.
-  prep_kernel<<<1, 256, 0, stream>>>(p.n, p.dtype, d_Q, w.hdr, w.U, w.U64, p.host_gbase ? nullptr : w.gbase);
+  prep_kernel<<<1, 256, 0, stream>>>(p.n, p.dtype, d_Q, w.hdr, w.U, w.U64, p.host_gbase ? nullptr : w.gbase,
+                                     p.gbase0);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -317,6 +319,7 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
     chunk = max_states_per_launch / states_per_unit;
     if (chunk < (uint64_t)p.blocks) chunk = p.blocks;
   }
+  if (timing && (e = cudaEventRecord(timing->start, stream)) != cudaSuccess) return e;
   for (uint64_t u0 = 0; u0 < p.total_units; u0 += chunk) {
     if (abort_flag && *abort_flag) {
       if (aborted) *aborted = true;
@@ -335,6 +338,7 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
     }
   }
 
+  if (timing && (e = cudaEventRecord(timing->stop, stream)) != cudaSuccess) return e;
   const int gblocks = p.ngroups < 1024 ? p.ngroups : 1024;
   group_min_kernel<<<gblocks, 256, 0, stream>>>(kp);
   ++nl;

@@ -120,12 +120,25 @@ QUBO_API size_t qubo_workspace_bytes(int n, int dtype, int k_prefix, int cache_b
 QUBO_API int qubo_solve_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits, void* d_workspace,
                       size_t workspace_bytes, void* cuda_stream, qubo_result* d_result);
 
+/* Device-resident form of qubo_solve_slice_range (one result over a contiguous slice range). */
+QUBO_API size_t qubo_slice_range_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits, uint64_t num_slices);
+QUBO_API int qubo_solve_slice_range_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits,
+                                           uint64_t first_slice, uint64_t num_slices, void* d_workspace,
+                                           size_t workspace_bytes, void* cuda_stream, qubo_result* d_result);
+
 QUBO_API size_t qubo_batched_workspace_bytes(int batch, int n, int dtype);
 QUBO_API int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void* d_workspace,
                               size_t workspace_bytes, void* cuda_stream, qubo_result* d_results);
 
 /* Planner decision for qubo_solve(n, ., dtype, k_prefix, cache_bits) on the current device. */
 QUBO_API int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* out);
+
+/* Kernel timing (measurement): while enabled, every search call records two CUDA events on its
+ * stream, around its enumeration (minimum-pass) launches. qubo_kernel_time_ms() waits for the
+ * second event and returns the elapsed milliseconds of the most recent call (-1 when disabled or
+ * nothing was recorded). Not thread-safe with concurrent device-resident calls. */
+QUBO_API void qubo_enable_kernel_timing(int enable);
+QUBO_API double qubo_kernel_time_ms(void);
 
 /* Number of kernel launches the last host or device call enqueued. */
 QUBO_API int qubo_last_launch_count(void);
