@@ -21,7 +21,7 @@ __all__ = [
     "QuboError", "INT32", "FP32", "solve", "solve_slices", "solve_slice_range", "solve_batched",
     "solve_device", "solve_batched_device", "workspace_bytes", "batched_workspace_bytes", "plan",
     "probe_alu", "last_launch_count", "slice_range_workspace_bytes", "solve_slice_range_device",
-    "enable_kernel_timing", "kernel_time_ms", "status_string", "last_error", "request_abort", "clear_abort",
+    "enable_kernel_timing", "kernel_time_ms", "solve_device_no_alloc", "NO_ALLOC_SCRATCH_BYTES", "status_string", "last_error", "request_abort", "clear_abort",
     "library_path", "RESULT_DTYPE",
 ]
 
@@ -77,6 +77,8 @@ _sig = {
     "qubo_solve_slice_range_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
                                                      ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64, ctypes.c_void_p,
                                                      ctypes.c_size_t, ctypes.c_void_p, ctypes.c_void_p]),
+    "qubo_solve_device_no_alloc": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                                  ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "qubo_enable_kernel_timing": (None, [ctypes.c_int]),
     "qubo_kernel_time_ms": (ctypes.c_double, []),
     "qubo_solve_batched_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
@@ -201,6 +203,18 @@ def solve_device(n: int, d_Q, dtype: int, workspace, workspace_nbytes: int, stre
     tensors with data_ptr()); stream is a cudaStream_t handle (int) or None. Asynchronous."""
     _check(_lib.qubo_solve_device(n, _ptr(d_Q), dtype, k_prefix, cache_bits, _ptr(workspace), workspace_nbytes,
                                   _ptr(stream) if stream is not None else 0, _ptr(d_result)))
+
+
+NO_ALLOC_SCRATCH_BYTES = 8 << 20
+
+
+def solve_device_no_alloc(n: int, d_Q, dtype: int, stream, d_result, k_prefix: int = 0, cache_bits: int = 0) -> None:
+    """Like solve_device, but with no workspace argument and no allocation: for callers that cannot
+    call cudaMalloc (a latency-critical loop, or a plug-in whose host owns all device memory).
+    Scratch is one fixed device array of NO_ALLOC_SCRATCH_BYTES shared by all calls; larger
+    problems raise QuboError(-1). Calls that overlap on the GPU race: keep them on one stream."""
+    _check(_lib.qubo_solve_device_no_alloc(n, _ptr(d_Q), dtype, k_prefix, cache_bits,
+                                           _ptr(stream) if stream is not None else 0, _ptr(d_result)))
 
 
 def slice_range_workspace_bytes(n: int, dtype: int, k_prefix: int, num_slices: int, cache_bits: int = 0) -> int:

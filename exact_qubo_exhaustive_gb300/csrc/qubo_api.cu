@@ -295,6 +295,23 @@ int host_search(const Plan& p, const void* Q, const uint64_t* gbase_host, std::v
 }
 
 }  // namespace
+
+// Plan of a whole-problem search, exactly as qubo_solve_device makes it.
+int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p) {
+  int st = make_plan(n, dtype, k_prefix, cache_bits, 0, 1, k_prefix > 0, p);
+  if (st) return st;
+  p->ngroups = 1;
+  p->upg = (uint64_t)1 << p->F;
+  p->total_units = p->upg;
+  return QUBO_OK;
+}
+
+int record_launch_count(int launches) {
+  g_last_launches = launches;
+  return launches;
+}
+
+int record_cuda_error(cudaError_t e, const char* where) { return set_cuda_error(e, where); }
 }  // namespace qgb
 
 using namespace qgb;

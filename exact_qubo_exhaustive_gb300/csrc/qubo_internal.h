@@ -97,6 +97,11 @@ size_t batched_workspace_bytes(const BatchPlan& bp);
 cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_result* res, cudaStream_t stream,
                         int* launches);
 
+// Whole-problem plan as qubo_solve_device makes it; launch-count bookkeeping of the C ABI.
+int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p);
+int record_launch_count(int launches);
+int record_cuda_error(cudaError_t e, const char* where);  // returns QUBO_ERR_CUDA
+
 // Measurement.
 cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz);
 

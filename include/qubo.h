@@ -120,6 +120,23 @@ QUBO_API size_t qubo_workspace_bytes(int n, int dtype, int k_prefix, int cache_b
 QUBO_API int qubo_solve_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits, void* d_workspace,
                       size_t workspace_bytes, void* cuda_stream, qubo_result* d_result);
 
+/* Search without any allocation, for callers that cannot call cudaMalloc when they need a result
+ * (a latency-critical loop that cannot afford cudaMalloc's device-wide synchronisation, or a
+ * plug-in inside a framework that owns all device memory and gives out no workspace). The paper
+ * has no counterpart: this is a deployment variant of qubo_solve_device with the same arguments
+ * minus the workspace. Scratch memory is one file-scope device array of
+ * QUBO_NO_ALLOC_SCRATCH_BYTES that every GPU loading the library keeps until exit; problems
+ * whose workspace (qubo_workspace_bytes) exceeds it return QUBO_ERR_ARG. The first call on a
+ * device looks the array's device address up (cudaGetSymbolAddress); make that first call before
+ * any stream capture. All calls share the array and it keeps the last call's contents; every
+ * call rewrites everything it reads, so nothing needs clearing. Calls that overlap on the GPU
+ * race on the array: order them on one stream. No cudaMalloc, cudaFree or allocating routine is
+ * called. d_Q, d_result: device pointers; cuda_stream: a cudaStream_t (NULL = legacy stream);
+ * asynchronous like qubo_solve_device. */
+#define QUBO_NO_ALLOC_SCRATCH_BYTES (8u << 20)
+QUBO_API int qubo_solve_device_no_alloc(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits,
+                                        void* cuda_stream, qubo_result* d_result);
+
 /* Device-resident form of qubo_solve_slice_range (one result over a contiguous slice range). */
 QUBO_API size_t qubo_slice_range_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits, uint64_t num_slices);
 QUBO_API int qubo_solve_slice_range_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits,
