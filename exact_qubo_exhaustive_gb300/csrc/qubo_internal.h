@@ -24,6 +24,12 @@ constexpr int kFastR = 4;
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 
+// Tensor-core minimum pass: 8 cached variables (256 MMA columns), 7 row variables (128 MMA rows).
+constexpr int kTcC = 8;
+constexpr int kTcRowBits = 7;
+constexpr int kTcThreads = 256;
+constexpr int64_t kTcMaxAbsSum = int64_t(1) << 21;  // every MMA operand piece and partial sum exact
+
 // Written by the device, read back by the host (lives at the start of the workspace).
 struct DevHeader {
   int32_t status;      // QUBO_OK or an error code found on the device
@@ -53,6 +59,9 @@ struct Plan {
   size_t smem_bytes = 0;   // dynamic shared memory of the enumeration kernels
   bool host_gbase = false; // group bases uploaded by the host (else one group, written on device)
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
+  bool tc = false;         // tensor-core minimum pass (int32, sum |U| <= kTcMaxAbsSum)
+  int w8 = 0;              // walked bits of the tensor-core split: n - F - kTcC
+  int tc_blocks = 0;       // grid of the tensor-core pass (one block per SM)
 };
 
 // Device pointers into one workspace.
@@ -71,6 +80,9 @@ struct Work {
   uint64_t* gties = nullptr;
   uint64_t* gkey = nullptr;
   qubo_result* results = nullptr;  // one per group
+  int32_t* M8 = nullptr;   // tensor-core split: (n - 8) x 256 interaction rows
+  int32_t* E8 = nullptr;   // 256 cached self energies
+  int32_t* T8 = nullptr;   // 2^w8 walked self energies, [Gray step][row]
   size_t bytes = 0;
 };
 

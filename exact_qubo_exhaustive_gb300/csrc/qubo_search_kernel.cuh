@@ -9,6 +9,7 @@ namespace qgb {
 struct KParams {
   int n, C, F, w;           // w = walked bits per unit
   int dtype;
+  int tc_active;            // a tensor-core minimum pass runs when sum |U| <= kTcMaxAbsSum
   int seg_bits;             // resolve: segments per tied unit = 2^seg_bits
   int ngroups;
   uint64_t upg;             // units per group
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   __shared__ int sL[64];
   __shared__ int s_red[32];
   if (p.hdr->status != QUBO_OK) return;
+  if (MODE == kModeMin && p.tc_active && p.hdr->abs_sum <= kTcMaxAbsSum) return;  // done on tensor cores
 
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
@@ -178,5 +180,10 @@ cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threa
 cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm);
+cudaError_t launch_tc_search(const KParams& p, int w8, const int32_t* M8, const int32_t* E8, const int32_t* T8,
+                             int blocks, cudaStream_t s);
+cudaError_t launch_tc_tables(int n, int w8, const DevHeader* hdr, const int32_t* U, int32_t* M8, int32_t* E8,
+                             int32_t* T8, cudaStream_t s);
+size_t tc_smem_bytes(int w8);
 
 }  // namespace qgb

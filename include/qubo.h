@@ -82,6 +82,8 @@ typedef struct qubo_plan_desc {
   uint64_t units;      /* work units (fixed prefixes) per call */
   size_t workspace_bytes;
   size_t smem_bytes;
+  int tensor_cores;    /* 1: the minimum pass runs on tcgen05 tensor cores when sum |U_ij| <= 2^21
+                          (opt-in: environment QUBO_TENSOR_CORES=1); 0: on the CUDA-core kernel */
 } qubo_plan_desc;
 
 /* Minimise one QUBO. Q is a HOST pointer to n*n int32 or fp32 values (row-major).
