@@ -247,6 +247,9 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   const int want_seg = ceil_log2_u64((uint64_t)p.blocks);
   while (seg < want_seg && (niter >> (seg + 1)) >= 1) ++seg;
   p.seg_bits = (niter > 0) ? seg : 0;
+  // Biased-binade minimum pass (int32 input; it needs at least one iteration of 2^(kBiasedR+1)
+  // Gray steps and stages fewer shared rows than the int32 pass, so the same launch shape fits).
+  p.biased = p.variant == kFast && dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
   // Tensor-core minimum pass for int32 input on sm_10x: the split needs >= 8 walked bits
   // (7 MMA row bits + at least one Gray-walked bit) and a Gray table of at most 2^24 entries.
   const int w8 = n - p.F - kTcC;

@@ -21,6 +21,7 @@ enum Variant : int {
 };
 constexpr int kFastCPT = 16;
 constexpr int kFastR = 4;
+constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 
@@ -29,6 +30,9 @@ constexpr int kTcC = 8;
 constexpr int kTcRowBits = 7;
 constexpr int kTcThreads = 256;
 constexpr int64_t kTcMaxAbsSum = int64_t(1) << 21;  // every MMA operand piece and partial sum exact
+// Biased fp32 minimum walk: every running column energy is a sum of distinct U entries, so
+// |V| <= sum |U| < 2^22 keeps 1.5 * 2^23 + V inside the binade [2^23, 2^24).
+constexpr int64_t kBiasedWalkMaxAbsSum = (int64_t(1) << 22) - 1;
 
 // Written by the device, read back by the host (lives at the start of the workspace).
 struct DevHeader {
@@ -60,6 +64,7 @@ struct Plan {
   bool host_gbase = false; // group bases uploaded by the host (else one group, written on device)
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
   bool tc = false;         // tensor-core minimum pass (int32, sum |U| <= kTcMaxAbsSum)
+  bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   int w8 = 0;              // walked bits of the tensor-core split: n - F - kTcC
   int tc_blocks = 0;       // grid of the tensor-core pass (one block per SM)
 };

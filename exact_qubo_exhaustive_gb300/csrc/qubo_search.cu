@@ -303,6 +303,7 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   kp.w = p.w;
   kp.dtype = p.dtype;
   kp.tc_active = p.tc ? 1 : 0;
+  kp.biased_active = p.biased ? 1 : 0;
   kp.seg_bits = p.seg_bits;
   kp.ngroups = p.ngroups;
   kp.upg = p.upg;
@@ -346,7 +347,12 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
       if ((e = launch_tc_search(kp, p.w8, w.M8, w.E8, w.T8, tcb, stream)) != cudaSuccess) return e;
       ++nl;
     }
-    // ... and the CUDA-core pass (exits at once when the tensor-core pass ran)
+    if (p.biased) {
+      // biased-binade CUDA-core pass (exits at once beyond its range or when the tensor-core pass ran) ...
+      if ((e = launch_search_biased(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
+      ++nl;
+    }
+    // ... and the int32 CUDA-core pass (exits at once when another pass ran)
     if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) return e;
     ++nl;
     if (kp.unit_end < p.total_units && abort_flag) {

@@ -1,5 +1,6 @@
-// Register-cached enumeration kernel: 16 columns per thread, the 4 lowest walked rows in
-// registers, the other walked rows in shared memory.
+// Register-cached enumeration kernel: 16 columns per thread, the lowest walked rows in
+// registers (4 for the int32 passes, 5 for the biased-binade minimum pass), the other walked
+// rows in shared memory.
 #include "qubo_search_kernel.cuh"
 
 namespace qgb {
@@ -21,6 +22,14 @@ cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threa
     case kModeTiesFp: return launch_one<kModeTiesFp>(p, blocks, threads, smem, s);
   }
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
+  auto k = search_kernel<kFastCPT, kBiasedR, kModeMin, true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<blocks, threads, smem, s>>>(p);
+  return cudaGetLastError();
 }
 
 cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm) {

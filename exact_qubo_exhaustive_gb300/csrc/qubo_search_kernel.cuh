@@ -2,6 +2,8 @@
 // resolve modes, segments of the units whose minimum reached their group's minimum.
 #pragma once
 
+#include <type_traits>
+
 #include "qubo_walk.cuh"
 
 namespace qgb {
@@ -10,6 +12,7 @@ struct KParams {
   int n, C, F, w;           // w = walked bits per unit
   int dtype;
   int tc_active;            // a tensor-core minimum pass runs when sum |U| <= kTcMaxAbsSum
+  int biased_active;        // a biased-binade minimum pass runs when sum |U| <= kBiasedWalkMaxAbsSum
   int seg_bits;             // resolve: segments per tied unit = 2^seg_bits
   int ngroups;
   uint64_t upg;             // units per group
@@ -48,19 +51,39 @@ __device__ __forceinline__ void unit_linear_terms(const int32_t* __restrict__ U,
   }
 }
 
-template <int CPT, int R, int MODE>
+// Minimum-pass walk of one unit in value type VT; returns this thread's best energy (int32).
+template <int CPT, int R, typename VT>
+__device__ __forceinline__ int min_walk(const WalkCtx& c, const KParams& p, int cP, int64_t niter) {
+  Walker<CPT, R, kModeMin, VT> W;
+  W.init(c, p.Ec, p.M, cP);
+  W.aux = kIntInf;
+  W.walk(c, 0, niter, niter, 0, nullptr, 0);
+  return W.aux - VOps<VT>::kBiasBits + W.s;
+}
+
+// BIASED: the minimum pass with column energies in the biased fp32 binade (VOps<float>); it runs
+// only when sum |U| <= kBiasedWalkMaxAbsSum, and the int32 minimum pass of the same launch
+// sequence then exits at once.
+template <int CPT, int R, int MODE, bool BIASED = false>
 __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const KParams p) {
+  static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
   __shared__ int s_red[32];
   if (p.hdr->status != QUBO_OK) return;
   if (MODE == kModeMin && p.tc_active && p.hdr->abs_sum <= kTcMaxAbsSum) return;  // done on tensor cores
+  if constexpr (BIASED) {
+    if (p.hdr->abs_sum > kBiasedWalkMaxAbsSum) return;  // beyond the binade: the int32 pass runs
+  } else if constexpr (MODE == kModeMin) {
+    if (p.biased_active && p.hdr->abs_sum <= kBiasedWalkMaxAbsSum) return;  // done by the biased pass
+  }
 
   const int tid = threadIdx.x;
   const int nthreads = blockDim.x;
   const int n = p.n, C = p.C, F = p.F, w = p.w;
   const int ncols = 1 << C;
   const int ndyn = w > R ? w - R : 0;
+  constexpr bool f32 = BIASED;  // staged rows in fp32 for the biased walk
 
   // Stage the walked rows of positions >= R (slice-independent) in shared memory.
   if constexpr (CPT >= 4) {
@@ -69,7 +92,9 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
     for (int idx = tid; idx < ndyn * nq; idx += nthreads) {
       const int rr = idx / nq, q = idx - rr * nq;
       const int v = n - C - 1 - (R + rr);
-      s_rows4[idx] = M4[(size_t)v * nq + q];
+      const int4 m = M4[(size_t)v * nq + q];
+      if (f32) reinterpret_cast<float4*>(s_rows4)[idx] = make_float4((float)m.x, (float)m.y, (float)m.z, (float)m.w);
+      else s_rows4[idx] = m;
     }
   } else {
     int* s_rows = reinterpret_cast<int*>(s_rows4);
@@ -122,26 +147,18 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
 
-    Walker<CPT, R, MODE> W;
-    W.init(c, p.Ec, p.M, cP);
-    W.seek(c, it0);
-    uint64_t gk = 0;
     if constexpr (MODE == kModeMin) {
-      W.aux = kIntInf;
-    } else {
-      W.aux = p.gmin[g] + p.hdr->band - W.s;
-      if constexpr (MODE == kModeTiesFp) gk = p.gkey[g];
-    }
-
-    if (niter == 0) {
-      // no walked variable (generic variant only): the single walked assignment is 0
-      W.step(c, prank, 0, p.T[0], p.U64, gk);
-    } else {
-      W.walk(c, it0, it1, it1, prank, p.U64, gk);
-    }
-
-    if constexpr (MODE == kModeMin) {
-      int best = W.aux + W.s;
+      int best;
+      if (niter == 0) {
+        // no walked variable (generic variant only): the single walked assignment is 0
+        Walker<CPT, R, MODE> W;
+        W.init(c, p.Ec, p.M, cP);
+        W.aux = kIntInf;
+        W.step(c, prank, 0, p.T[0], p.U64, 0);
+        best = W.aux + W.s;
+      } else {
+        best = min_walk<CPT, R, typename std::conditional<BIASED, float, int>::type>(c, p, cP, niter);
+      }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
       if (lane == 0) s_red[warp] = best;
@@ -152,6 +169,14 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
         p.unit_min[u] = b;
       }
     } else {
+      Walker<CPT, R, MODE> W;
+      W.init(c, p.Ec, p.M, cP);
+      W.seek(c, it0);
+      uint64_t gk = 0;
+      W.aux = p.gmin[g] + p.hdr->band - W.s;
+      if constexpr (MODE == kModeTiesFp) gk = p.gkey[g];
+      if (niter == 0) W.step(c, prank, 0, p.T[0], p.U64, gk);
+      else W.walk(c, it0, it1, it1, prank, p.U64, gk);
       uint64_t cnt = W.cnt, rmin = W.rmin, kmin = W.kmin;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -177,6 +202,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 
 // Launch helpers (one translation unit per variant).
 cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm);

@@ -87,6 +87,52 @@ __device__ __forceinline__ int min_all(const int* v) {
   }
 }
 
+// Representation of the running column energies V and walked rows in the walk.
+//
+// int: plain int32; every add and min runs on the integer ALU pipe (or the FMA pipe's
+// integer multiply-add, at the compiler's choice).
+//
+// float (biased binade): V[j] is held as the fp32 number kBias + V[j], kBias = 1.5 * 2^23. While
+// |V[j]| < 2^22 the number lies in [2^23, 2^24), where fp32 numbers are exactly the integers and
+// the bit pattern of x is x + (0x4B000000 - 2^23): an affine, increasing image of the value.
+// So the column update V += row is an exact FADD on the two FMA pipes, and the minimum over
+// columns, the fused add-min with the walked energy and the running best are integer
+// instructions on the bit patterns, exactly as in the int representation shifted by kBiasBits.
+template <typename VT>
+struct VOps;
+template <>
+struct VOps<int> {
+  static constexpr bool kInt = true;
+  static constexpr int kBiasBits = 0;
+  using V4 = int4;
+  static __device__ __forceinline__ int add(int a, int b) { return a + b; }
+  static __device__ __forceinline__ int sub(int a, int b) { return a - b; }
+  static __device__ __forceinline__ int energy(int x) { return x; }  // V representation of energy x
+  static __device__ __forceinline__ int row(int x) { return x; }     // row representation of x
+  static __device__ __forceinline__ int bits(int v) { return v; }    // order-preserving int image
+};
+template <>
+struct VOps<float> {
+  static constexpr bool kInt = false;
+  static constexpr int kBiasBits = 0x4B400000;  // bit pattern of 1.5 * 2^23
+  using V4 = float4;
+  static __device__ __forceinline__ float add(float a, float b) { return __fadd_rn(a, b); }
+  static __device__ __forceinline__ float sub(float a, float b) { return __fsub_rn(a, b); }
+  static __device__ __forceinline__ float energy(int x) { return __int_as_float(kBiasBits + x); }
+  static __device__ __forceinline__ float row(int x) { return static_cast<float>(x); }
+  static __device__ __forceinline__ int bits(float v) { return __float_as_int(v); }
+};
+
+// Minimum of the order images of N register values, with 3-input mins (one ALU instruction
+// per two values).
+template <typename VT, int N>
+__device__ __forceinline__ int vmin_bits(const VT* v) {
+  int b[N];
+#pragma unroll
+  for (int k = 0; k < N; ++k) b[k] = VOps<VT>::bits(v[k]);
+  return min_all<N>(b);
+}
+
 // Modes of one walk.
 enum WalkMode : int {
   kModeMin = 0,     // minimum energy of the walked states
@@ -101,7 +147,7 @@ struct WalkCtx {
   int nthreads;               // columns are distributed over this many threads
   int thread;                 // this thread's index among them
   const int* sL;              // linear terms L[v] of the unit (v >= F); L[v] for v < F: c(P) parts
-  const int4* rows4;          // walked rows a >= R (quad layout), or
+  const void* rows4;          // walked rows a >= R (quad layout, int4 or float4), or
   const int* rows1;           //   the same rows, one int per column (generic)
   const int* T;               // walked energies in Gray order
   bool t_global;              // T lives in global memory (use the read-only path)
@@ -115,13 +161,17 @@ __device__ __forceinline__ int column_of(int t, int nthreads, int jj) {
   else return ((((jj >> 2) * nthreads) + t) << 2) | (jj & 3);
 }
 
-template <int CPT, int R, int MODE>
+template <int CPT, int R, int MODE, typename VT = int>
 struct Walker {
+  static_assert(MODE == kModeMin || VOps<VT>::kInt, "resolve modes walk in int32");
+  static_assert(VOps<VT>::kInt || (CPT >= 4 && R >= 1), "the biased walk uses the fast layout");
+  using O = VOps<VT>;
+  using V4 = typename O::V4;
   static constexpr int kSteps = 1 << (R + 1);  // Gray steps per loop iteration
-  int V[CPT];
-  int Row[R > 0 ? R : 1][CPT];
+  VT V[CPT];
+  VT Row[R > 0 ? R : 1][CPT];
   int s;        // c(P) + sum of L over set walked positions >= R
-  int aux;      // kModeMin: running best minus s; resolve modes: threshold minus s
+  int aux;      // kModeMin: order image of (running best minus s); resolve modes: threshold minus s
   bool valid;   // this thread owns real columns (generic blocks may have idle lanes)
   int col0;     // generic: this thread's column
   // resolve accumulators
@@ -142,7 +192,7 @@ struct Walker {
       int lc = 0;
       for (int b = 0; b < C; ++b)
         if ((col0 >> b) & 1) lc += c.sL[n - 1 - b];
-      V[0] = Ec[col0] + lc;
+      V[0] = O::energy(Ec[col0] + lc);
     } else {
       valid = true;
       col0 = 0;
@@ -161,10 +211,10 @@ struct Walker {
         for (int b = 0; b < lk; ++b)
           if ((k >> b) & 1) Lk += c.sL[n - 1 - (2 + lt + b)];
         const int4 e = Ec4[k * T + t];
-        V[4 * k + 0] = e.x + Lk;
-        V[4 * k + 1] = e.y + Lk + Le1;
-        V[4 * k + 2] = e.z + Lk + Le2;
-        V[4 * k + 3] = e.w + Lk + Le1 + Le2;
+        V[4 * k + 0] = O::energy(e.x + Lk);
+        V[4 * k + 1] = O::energy(e.y + Lk + Le1);
+        V[4 * k + 2] = O::energy(e.z + Lk + Le2);
+        V[4 * k + 3] = O::energy(e.w + Lk + Le1 + Le2);
       }
       const int nq = (1 << C) >> 2;
       const int4* M4 = reinterpret_cast<const int4*>(M);
@@ -175,10 +225,10 @@ struct Walker {
 #pragma unroll
         for (int k = 0; k < kq; ++k) {
           const int4 m = M4[(size_t)v * nq + k * T + t];
-          Row[a][4 * k + 0] = m.x + Lv;
-          Row[a][4 * k + 1] = m.y + Lv;
-          Row[a][4 * k + 2] = m.z + Lv;
-          Row[a][4 * k + 3] = m.w + Lv;
+          Row[a][4 * k + 0] = O::row(m.x + Lv);
+          Row[a][4 * k + 1] = O::row(m.y + Lv);
+          Row[a][4 * k + 2] = O::row(m.z + Lv);
+          Row[a][4 * k + 3] = O::row(m.w + Lv);
         }
       }
     }
@@ -194,24 +244,24 @@ struct Walker {
     } else {
       constexpr int kq = CPT / 4;
       const int nq = (1 << c.C) >> 2;
-      const int4* rp = c.rows4 + (size_t)rr * nq + c.thread;
+      const V4* rp = reinterpret_cast<const V4*>(c.rows4) + (size_t)rr * nq + c.thread;
       if (d > 0) {
 #pragma unroll
         for (int k = 0; k < kq; ++k) {
-          const int4 m = rp[k * c.nthreads];
-          V[4 * k + 0] += m.x;
-          V[4 * k + 1] += m.y;
-          V[4 * k + 2] += m.z;
-          V[4 * k + 3] += m.w;
+          const V4 m = rp[k * c.nthreads];
+          V[4 * k + 0] = O::add(V[4 * k + 0], m.x);
+          V[4 * k + 1] = O::add(V[4 * k + 1], m.y);
+          V[4 * k + 2] = O::add(V[4 * k + 2], m.z);
+          V[4 * k + 3] = O::add(V[4 * k + 3], m.w);
         }
       } else {
 #pragma unroll
         for (int k = 0; k < kq; ++k) {
-          const int4 m = rp[k * c.nthreads];
-          V[4 * k + 0] -= m.x;
-          V[4 * k + 1] -= m.y;
-          V[4 * k + 2] -= m.z;
-          V[4 * k + 3] -= m.w;
+          const V4 m = rp[k * c.nthreads];
+          V[4 * k + 0] = O::sub(V[4 * k + 0], m.x);
+          V[4 * k + 1] = O::sub(V[4 * k + 1], m.y);
+          V[4 * k + 2] = O::sub(V[4 * k + 2], m.z);
+          V[4 * k + 3] = O::sub(V[4 * k + 3], m.w);
         }
       }
     }
@@ -221,8 +271,13 @@ struct Walker {
   __device__ __forceinline__ void dyn_flip(const WalkCtx& c, int a, int d) {
     add_dyn_row(c, a, d);
     const int Lv = c.sL[c.n - c.C - 1 - a];
-    if (d > 0) { s += Lv; aux -= Lv; }
-    else { s -= Lv; aux += Lv; }
+    if (d > 0) {
+      s += Lv;
+      aux -= Lv;
+    } else {
+      s -= Lv;
+      aux += Lv;
+    }
   }
 
   // Walk state at the start of iteration it0 (gray(i0) has only positions >= R set).
@@ -262,7 +317,7 @@ struct Walker {
 
   __device__ __forceinline__ void step(const WalkCtx& c, uint64_t prank, uint64_t i, int tv,
                                        const double* __restrict__ U64, uint64_t gkey) {
-    const int m = min_all<CPT>(V);
+    const int m = vmin_bits<VT, CPT>(V);
     if constexpr (MODE == kModeMin) {
       aux = __viaddmin_s32(m, tv, aux);
     } else {
@@ -273,32 +328,103 @@ struct Walker {
     }
   }
 
-  // Steps L.. of one iteration, unrolled by recursion so that every register row index and
-  // every flip sign is a compile-time constant.
+  // ----- fast layout (CPT >= 4): the loads of an iteration are issued ahead of their use.
+  // The walked energies of the next iteration replace those of this one quad by quad as they
+  // are consumed, and each shared-memory row is read a few steps before its flip, so neither
+  // the read-only cache nor shared memory latency stalls the adds.
+  static constexpr int kMid = 1 << R;                          // step after which position R flips
+  static constexpr int kAhead = kMid >= 16 ? 8 : (kMid >> 1);  // steps between a row read and its use
+  struct RowBuf {
+    V4 q[CPT >= 4 ? CPT / 4 : 1];
+  };
+
+  __device__ __forceinline__ void load_dyn_row(const WalkCtx& c, int a, RowBuf& b) const {
+    constexpr int kq = CPT / 4;
+    const int nq = (1 << c.C) >> 2;
+    const V4* rp = reinterpret_cast<const V4*>(c.rows4) + (size_t)(a - R) * nq + c.thread;
+#pragma unroll
+    for (int k = 0; k < kq; ++k) b.q[k] = rp[k * c.nthreads];
+  }
+
+  __device__ __forceinline__ void apply_dyn_row(const WalkCtx& c, int a, const RowBuf& b, bool up) {
+    constexpr int kq = CPT / 4;
+    const int Lv = c.sL[c.n - c.C - 1 - a];
+    if (up) {
+#pragma unroll
+      for (int k = 0; k < kq; ++k) {
+        V[4 * k + 0] = O::add(V[4 * k + 0], b.q[k].x);
+        V[4 * k + 1] = O::add(V[4 * k + 1], b.q[k].y);
+        V[4 * k + 2] = O::add(V[4 * k + 2], b.q[k].z);
+        V[4 * k + 3] = O::add(V[4 * k + 3], b.q[k].w);
+      }
+      s += Lv;
+      aux -= Lv;
+    } else {
+#pragma unroll
+      for (int k = 0; k < kq; ++k) {
+        V[4 * k + 0] = O::sub(V[4 * k + 0], b.q[k].x);
+        V[4 * k + 1] = O::sub(V[4 * k + 1], b.q[k].y);
+        V[4 * k + 2] = O::sub(V[4 * k + 2], b.q[k].z);
+        V[4 * k + 3] = O::sub(V[4 * k + 3], b.q[k].w);
+      }
+      s -= Lv;
+      aux += Lv;
+    }
+  }
+
+  template <int E>
+  static __device__ __forceinline__ int comp(const int4& x) {
+    if constexpr (E == 0) return x.x;
+    else if constexpr (E == 1) return x.y;
+    else if constexpr (E == 2) return x.z;
+    else return x.w;
+  }
+
+  static __device__ __forceinline__ int4 load_t4(const WalkCtx& c, const int4* p) {
+    return c.t_global ? __ldg(p) : *p;
+  }
+
+  // Steps L.. of one iteration, unrolled by recursion so that every register row index, every
+  // flip sign and every prefetch point is a compile-time constant. `tq` holds this iteration's
+  // walked energies; `tn` points at the next iteration's (or at this one's, on the last).
   template <int L>
-  __device__ __forceinline__ void steps_from(const WalkCtx& c, uint64_t prank, uint64_t base, int64_t iter,
-                                             const int* tv, const double* __restrict__ U64, uint64_t gkey) {
+  __device__ __forceinline__ void steps_fast(const WalkCtx& c, uint64_t prank, uint64_t base, int64_t iter,
+                                             int a_end, int4* tq, const int4* tn, RowBuf& rb,
+                                             const double* __restrict__ U64, uint64_t gkey) {
     if constexpr (L < kSteps) {
-      step(c, prank, base + L, tv[L], U64, gkey);
+      step(c, prank, base + L, comp<L & 3>(tq[L >> 2]), U64, gkey);
+      if constexpr ((L & 3) == 3) tq[L >> 2] = load_t4(c, tn + (L >> 2));
+      if constexpr (L == kMid - 1 - kAhead) load_dyn_row(c, R, rb);
+      if constexpr (L == kSteps - 1 - kAhead) load_dyn_row(c, a_end, rb);
       if constexpr (L + 1 < kSteps) {
-        if constexpr (L + 1 == (1 << R)) {
+        if constexpr (L + 1 == kMid) {
           // between the two halves: position R, rising on even iterations
-          dyn_flip(c, R, (iter & 1) ? -1 : +1);
+          apply_dyn_row(c, R, rb, (iter & 1) == 0);
         } else {
           // register position a < R; its direction depends on L only
           constexpr int a = ctz_c(L + 1);
           constexpr int bit = ((L >> a) ^ (L >> (a + 1))) & 1;
           if constexpr (bit) {
 #pragma unroll
-            for (int jj = 0; jj < CPT; ++jj) V[jj] -= Row[a][jj];
+            for (int jj = 0; jj < CPT; ++jj) V[jj] = O::sub(V[jj], Row[a][jj]);
           } else {
 #pragma unroll
-            for (int jj = 0; jj < CPT; ++jj) V[jj] += Row[a][jj];
+            for (int jj = 0; jj < CPT; ++jj) V[jj] = O::add(V[jj], Row[a][jj]);
           }
         }
       }
-      steps_from<L + 1>(c, prank, base, iter, tv, U64, gkey);
+      steps_fast<L + 1>(c, prank, base, iter, a_end, tq, tn, rb, U64, gkey);
     }
+  }
+
+  // ----- generic layout (one column per thread, R = 0): two steps per iteration.
+  __device__ __forceinline__ void steps_generic(const WalkCtx& c, uint64_t prank, uint64_t base, int64_t iter,
+                                                const double* __restrict__ U64, uint64_t gkey) {
+    const int2* T2 = reinterpret_cast<const int2*>(c.T) + (base >> 1);
+    const int2 x = c.t_global ? __ldg(T2) : T2[0];
+    step(c, prank, base, x.x, U64, gkey);
+    dyn_flip(c, R, (iter & 1) ? -1 : +1);
+    step(c, prank, base + 1, x.y, U64, gkey);
   }
 
   // Walk Gray iterations [it0, it1) of 2^(R+1) steps each. The flip that leaves an iteration is
@@ -306,30 +432,36 @@ struct Walker {
   // following call continues).
   __device__ __forceinline__ void walk(const WalkCtx& c, int64_t it0, int64_t it1, int64_t it_flip_end,
                                        uint64_t prank, const double* __restrict__ U64, uint64_t gkey) {
-    for (int64_t iter = it0; iter < it1; ++iter) {
-      const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
-      int tv[kSteps];
-      if constexpr (kSteps >= 4) {
-        const int4* T4 = reinterpret_cast<const int4*>(c.T) + (base >> 2);
+    if constexpr (CPT >= 4 && kSteps >= 4) {
+      const int4* T4 = reinterpret_cast<const int4*>(c.T);
+      int4 tq[kSteps / 4];
+      if (it0 < it1) {
 #pragma unroll
-        for (int q = 0; q < kSteps / 4; ++q) {
-          const int4 x = c.t_global ? __ldg(T4 + q) : T4[q];
-          tv[4 * q + 0] = x.x;
-          tv[4 * q + 1] = x.y;
-          tv[4 * q + 2] = x.z;
-          tv[4 * q + 3] = x.w;
-        }
-      } else {
-        const int2* T2 = reinterpret_cast<const int2*>(c.T) + (base >> 1);
-        const int2 x = c.t_global ? __ldg(T2) : T2[0];
-        tv[0] = x.x;
-        tv[1] = x.y;
+        for (int q = 0; q < kSteps / 4; ++q) tq[q] = load_t4(c, T4 + (static_cast<uint64_t>(it0) << (R - 1)) + q);
       }
-      steps_from<0>(c, prank, base, iter, tv, U64, gkey);
-      if (iter + 1 < it_flip_end) {
-        const int a = R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1;
-        const uint64_t ilast = base + kSteps - 1;
-        dyn_flip(c, a, ((gray_code(ilast) >> a) & 1u) ? -1 : +1);
+      RowBuf rb;
+      for (int64_t iter = it0; iter < it1; ++iter) {
+        const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
+        const bool flip_end = iter + 1 < it_flip_end;
+        // a_end is only read when flip_end; otherwise a valid row (R) is read and left unused
+        const int a_end = flip_end ? R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1 : R;
+        const int4* tn = T4 + (((iter + 1 < it1) ? base + kSteps : base) >> 2);
+        steps_fast<0>(c, prank, base, iter, a_end, tq, tn, rb, U64, gkey);
+        if (flip_end) {
+          const uint64_t ilast = base + kSteps - 1;
+          apply_dyn_row(c, a_end, rb, ((gray_code(ilast) >> a_end) & 1u) == 0);
+        }
+      }
+    } else {
+      for (int64_t iter = it0; iter < it1; ++iter) {
+        const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
+        static_assert(CPT == 1 && R == 0, "generic layout");
+        steps_generic(c, prank, base, iter, U64, gkey);
+        if (iter + 1 < it_flip_end) {
+          const int a = R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1;
+          const uint64_t ilast = base + kSteps - 1;
+          dyn_flip(c, a, ((gray_code(ilast) >> a) & 1u) ? -1 : +1);
+        }
       }
     }
   }

@@ -114,6 +114,45 @@ def test_tensor_range_limit_falls_back_exactly(q, monkeypatch):
         check_int(q, Q)
 
 
+def _with_abs_sum(Q, total):
+    """Q with Q[0, 0] changed so that sum |Q_ij| (upper triangle) is exactly `total`."""
+    Q = Q.copy()
+    Q[0, 0] = 0
+    rest = int(np.abs(Q.astype(np.int64)).sum())
+    assert 0 <= total - rest < (1 << 31)
+    Q[0, 0] = -(total - rest)
+    assert int(np.abs(Q.astype(np.int64)).sum()) == total
+    return Q
+
+
+@pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
+def test_biased_walk_range_limit_is_exact(q, sign):
+    # The CUDA-core minimum walk keeps column energies in the fp32 binade [2^23, 2^24) for
+    # sum |U| <= 2^22 - 1 and in int32 above. Both sides of the limit, with running values pushed
+    # to the extremes: all-negative entries reach E = -sum |U| at x = 1, all-positive ones +sum |U|.
+    n = 26
+    lo, hi = {"mixed": (-20000, 20000), "negative": (-20000, -1), "positive": (1, 20000)}[sign]
+    for total in ((1 << 22) - 1, 1 << 22):
+        Q = np.triu(qi.random_upper_int(n, lo, hi, 2300 + total % 7))
+        if sign == "positive":
+            Q = np.abs(Q)
+            Q[0, 0] = 0
+            Q[0, 0] = total - int(np.abs(Q.astype(np.int64)).sum())
+        else:
+            Q = _with_abs_sum(Q, total)
+        assert int(np.abs(Q.astype(np.int64)).sum()) == total
+        e, x, t = check_int(q, Q)
+        if sign == "negative":
+            assert e == -total and x.all()
+
+
+def test_int32_walk_large_values(q):
+    # sum |U| near 2^29: the minimum walk stays in int32 on the fast kernel
+    Q = qi.random_upper_int(28, -(1 << 21), 1 << 21, 2301)
+    assert int(np.abs(Q.astype(np.int64)).sum()) > (1 << 22)
+    check_int(q, Q)
+
+
 # ---------------------------------------------------------------- configs
 
 def test_n20_config(q):
