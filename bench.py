@@ -46,7 +46,7 @@ SMS = 152
 LANES_PER_CLK = 128          # issue-limited int32 lanes per SM per clock (ALU + FMA-heavy pipes)
 MAX_SM_MHZ = 2070.0
 PROFILE = os.path.join(ROOT, "profiles", "search_kernel_n40.md")
-KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_fast.cu"]
+KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_fast.cu", "qubo_internal.h"]
 
 
 def log(*a):
@@ -79,7 +79,7 @@ def profiled_traffic():
     if kv.get("kernel_source_sha256") != kernel_source_hash():
         return None, "kernel changed since the ncu capture"
     try:
-        return float(kv["traffic_bytes_per_launch_n40"]), "ncu capture (scaled to a full n=40 launch)"
+        return float(kv["traffic_bytes_per_launch_n40"]), "ncu capture of a full n=40 launch (one-pass DRAM metrics)"
     except (KeyError, ValueError):
         return None, "ncu summary without traffic"
 
@@ -287,9 +287,9 @@ def run_gb300(args):
                        "tie_count": int(r["tie_count"])},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                          "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "search_kernel<16,4,min> (enumeration)", "kernel_ms": kern,
-                         "peak_basis": "152 SMs x 128 int32 lanes/clk (issue limit; ALU + FMA-heavy pipes, "
-                                       "measured by the add probe) x 2.07 GHz max SM clock",
+                         "kernel": "search_kernel<16,5,min,biased> (enumeration, biased fp32-binade minimum pass)", "kernel_ms": kern,
+                         "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
+                                       "add per state) x 2.07 GHz max SM clock",
                          "traffic_source": traffic_src,
                          "frac_at_measured_clock": (achieved / (SMS * LANES_PER_CLK * clocks["sm_mhz"] * 1e-6)
                                                     if clocks.get("sm_mhz") else None)},
