@@ -188,6 +188,15 @@ def run_reference(args):
     return 0
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank floats over the default process group (the slowest rank
+    sets the whole job's step time)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
 def run_gb300(args):
     import torch
     rank, world, local = dist_env()
@@ -260,9 +269,7 @@ def run_gb300(args):
     e2e = sum(e2e_ms) / len(e2e_ms)
 
     if world > 1:
-        t = torch.tensor([ms, e2e, kern], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, e2e, kern = (float(v) for v in t.tolist())
+        ms, e2e, kern = max_over_ranks([ms, e2e, kern], dev)
 
     value = world * STATES / (ms * 1e-3)
     e2e_value = world * STATES / (e2e * 1e-3)
