@@ -27,6 +27,7 @@ __all__ = [
 
 INT32 = 0
 FP32 = 1
+FP64 = 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "libqubo_gb300.so")
@@ -91,6 +92,10 @@ _sig = {
     "qubo_request_abort": (None, []),
     "qubo_clear_abort": (None, []),
     "qubo_probe_alu": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64p, _f64p]),
+    "qubo_ising_to_qubo": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
+                                          ctypes.c_void_p, _f64p]),
+    "qubo_solve_ising": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                        ctypes.c_int, _f64p, ctypes.c_void_p, _u64p]),
 }
 for _name, (_res, _args) in _sig.items():
     _f = getattr(_lib, _name)
@@ -118,13 +123,15 @@ def _matrix(Q):
         raise ValueError("Q must be a square matrix")
     if Q.dtype == np.float32:
         return np.ascontiguousarray(Q), FP32
+    if Q.dtype == np.float64:
+        return np.ascontiguousarray(Q), FP64
     if Q.dtype.kind in "iu" and Q.dtype.itemsize <= 4:
         return np.ascontiguousarray(Q, dtype=np.int32), INT32
     if Q.dtype.kind in "iu":
         if Q.size and (Q.min() < -(1 << 31) or Q.max() >= (1 << 31)):
             raise ValueError("integer Q must fit int32")
         return np.ascontiguousarray(Q, dtype=np.int32), INT32
-    raise TypeError("Q must be int32 or float32")
+    raise TypeError("Q must be int32, float32 or float64")
 
 
 def solve(Q, k_prefix: int = 0, cache_bits: int = 0):
@@ -165,6 +172,45 @@ def solve_slice_range(Q, k_prefix: int, first_slice: int, num_slices: int, cache
     _check(_lib.qubo_solve_slice_range(n, Q.ctypes.data, dt, k_prefix, cache_bits, first_slice, num_slices,
                                        ctypes.byref(e), x.ctypes.data_as(_u8p), ctypes.byref(t)))
     return (int(e.value) if dt == INT32 else float(e.value)), x, int(t.value)
+
+
+def _ising_inputs(J, h):
+    J = np.asarray(J)
+    if J.ndim != 2 or J.shape[0] != J.shape[1]:
+        raise ValueError("J must be a square matrix")
+    n = J.shape[0]
+    if J.dtype in (np.float32, np.float64):
+        dt = FP32 if J.dtype == np.float32 else FP64
+        J = np.ascontiguousarray(J)
+        h = None if h is None else np.ascontiguousarray(h, dtype=J.dtype)
+    else:
+        dt = INT32
+        J, _ = _matrix(J)
+        h = None if h is None else np.ascontiguousarray(h, dtype=np.int32)
+    if h is not None and h.shape != (n,):
+        raise ValueError("h must have n entries")
+    return J, h, dt, n
+
+
+def ising_to_qubo(J, h=None):
+    """Exact QUBO of H(s) = sum_ij J_ij s_i s_j + sum_i h_i s_i: (Q, offset), H = E_Q(x) + offset."""
+    J, h, dt, n = _ising_inputs(J, h)
+    Q = np.zeros((n, n), np.int32 if dt == INT32 else np.float64)
+    off = ctypes.c_double()
+    _check(_lib.qubo_ising_to_qubo(n, J.ctypes.data, None if h is None else h.ctypes.data, dt, Q.ctypes.data,
+                                   ctypes.byref(off)))
+    return Q, (int(off.value) if dt == INT32 else float(off.value))
+
+
+def solve_ising(J, h=None, k_prefix: int = 0, cache_bits: int = 0):
+    """Exhaustive Ising ground state: (H_min, spins s in {-1,+1} as int8, number of ground states)."""
+    J, h, dt, n = _ising_inputs(J, h)
+    e = ctypes.c_double()
+    s = np.zeros(n, np.int8)
+    t = ctypes.c_uint64()
+    _check(_lib.qubo_solve_ising(n, J.ctypes.data, None if h is None else h.ctypes.data, dt, k_prefix, cache_bits,
+                                 ctypes.byref(e), s.ctypes.data, ctypes.byref(t)))
+    return (int(e.value) if dt == INT32 else float(e.value)), s, int(t.value)
 
 
 def solve_batched(Qs):

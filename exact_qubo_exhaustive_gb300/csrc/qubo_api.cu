@@ -264,7 +264,7 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
 }
 
 int check_common(int n, const void* Q, int dtype) {
-  if (n < 1 || n > 62 || Q == nullptr || (dtype != QUBO_INT32 && dtype != QUBO_FP32)) return QUBO_ERR_ARG;
+  if (n < 1 || n > 62 || Q == nullptr || !valid_dtype(dtype)) return QUBO_ERR_ARG;
   return QUBO_OK;
 }
 
@@ -278,7 +278,7 @@ int host_search(const Plan& p, const void* Q, const uint64_t* gbase_host, std::v
   if (st) return st;
   Work lay = layout_workspace(p, nullptr);
   if ((st = ensure(&g_buf.ws, &g_buf.ws_bytes, lay.bytes, false, "cudaMalloc(workspace)"))) return st;
-  const size_t qbytes = (size_t)p.n * p.n * 4;
+  const size_t qbytes = (size_t)p.n * p.n * dtype_bytes(p.dtype);
   if ((st = ensure(&g_buf.dq, &g_buf.dq_bytes, qbytes, false, "cudaMalloc(Q)"))) return st;
   const size_t rbytes = (size_t)p.ngroups * sizeof(qubo_result);
   if ((st = ensure(&g_buf.hres, &g_buf.hres_bytes, rbytes, true, "cudaMallocHost(results)"))) return st;
@@ -333,6 +333,10 @@ int record_launch_count(int launches) {
 }
 
 int record_cuda_error(cudaError_t e, const char* where) { return set_cuda_error(e, where); }
+bool valid_dtype(int dtype) { return dtype == QUBO_INT32 || dtype == QUBO_FP32 || dtype == QUBO_FP64; }
+
+size_t dtype_bytes(int dtype) { return dtype == QUBO_FP64 ? 8 : 4; }
+
 }  // namespace qgb
 
 using namespace qgb;
@@ -426,7 +430,7 @@ int qubo_solve_slice_range(int n, const void* Q, int dtype, int k_prefix, int ca
 }
 
 size_t qubo_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits) {
-  if (n < 1 || n > 62 || (dtype != QUBO_INT32 && dtype != QUBO_FP32)) return 0;
+  if (n < 1 || n > 62 || !valid_dtype(dtype)) return 0;
   int dev;
   if (current_device(&dev)) return 0;
   Plan p;
@@ -546,7 +550,7 @@ int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void
 }
 
 size_t qubo_slice_range_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits, uint64_t num_slices) {
-  if (n < 1 || n > 62 || (dtype != QUBO_INT32 && dtype != QUBO_FP32) || k_prefix < 1 || k_prefix >= n ||
+  if (n < 1 || n > 62 || !valid_dtype(dtype) || k_prefix < 1 || k_prefix >= n ||
       num_slices < 1)
     return 0;
   int dev;
@@ -606,7 +610,7 @@ double qubo_kernel_time_ms(void) {
 }
 
 int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* out) {
-  if (n < 1 || n > 62 || (dtype != QUBO_INT32 && dtype != QUBO_FP32) || !out) return QUBO_ERR_ARG;
+  if (n < 1 || n > 62 || !valid_dtype(dtype) || !out) return QUBO_ERR_ARG;
   if (k_prefix > n || cache_bits > n) return QUBO_ERR_PLAN;
   int dev, st;
   if ((st = current_device(&dev))) return st;

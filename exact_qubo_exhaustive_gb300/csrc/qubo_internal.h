@@ -115,6 +115,8 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
                         int* launches);
 
 // Whole-problem plan as qubo_solve_device makes it; launch-count bookkeeping of the C ABI.
+bool valid_dtype(int dtype);
+size_t dtype_bytes(int dtype);
 int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p);
 int record_launch_count(int launches);
 int record_cuda_error(cudaError_t e, const char* where);  // returns QUBO_ERR_CUDA

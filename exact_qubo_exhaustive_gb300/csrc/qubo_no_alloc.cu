@@ -48,7 +48,7 @@ using namespace qgb;
 
 extern "C" int qubo_solve_device_no_alloc(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits,
                                           void* cuda_stream, qubo_result* d_result) {
-  if (n < 1 || n > 62 || d_Q == nullptr || d_result == nullptr || (dtype != QUBO_INT32 && dtype != QUBO_FP32))
+  if (n < 1 || n > 62 || d_Q == nullptr || d_result == nullptr || !valid_dtype(dtype))
     return QUBO_ERR_ARG;
   if (k_prefix > n || cache_bits > n) return QUBO_ERR_PLAN;
   int count = 0, dev = 0;

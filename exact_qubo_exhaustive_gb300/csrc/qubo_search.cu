@@ -8,7 +8,7 @@ namespace qgb {
 // ------------------------------------------------------------------------------------------------
 // A1: fold Q to the upper triangle and validate (one block).
 //   int32: U_ii = Q_ii, U_ij = Q_ij + Q_ji (i < j) in int64; S = sum |U_ij| must be <= 2^30 - 1.
-//   fp32:  every entry finite; U64 folded in fp64; the int32 image is round(U64 * 2^s) with the
+//   fp32/fp64: every entry finite; U64 folded in fp64; the int32 image is round(U64 * 2^s) with the
 //          largest s keeping sum |image| <= 2^30 - 1. A state's image energy then differs from
 //          2^s times its energy by at most (#selected terms)/2 <= n(n+1)/4, so every fp64
 //          minimiser lies within band = n(n+1)/2 image units of the image minimum.
@@ -50,17 +50,19 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
     }
     return;
   }
-  // fp32
-  const float* Q = static_cast<const float*>(Qv);
+  // fp32 / fp64
+  const float* Qf = static_cast<const float*>(Qv);
+  const double* Qd = static_cast<const double*>(Qv);
+  auto load = [&](int idx) -> double { return dtype == QUBO_FP64 ? Qd[idx] : (double)Qf[idx]; };
   double local = 0.0;
   int bad = 0;
   for (int idx = tid; idx < nn; idx += nt) {
     const int i = idx / n, j = idx - (idx / n) * n;
-    const float a = Q[idx];
+    const double a = load(idx);
     if (!isfinite(a)) bad = 1;
     double u = 0.0;
-    if (j == i) u = (double)a;
-    else if (j > i) u = __dadd_rn((double)a, (double)Q[j * n + i]);
+    if (j == i) u = a;
+    else if (j > i) u = __dadd_rn(a, load(j * n + i));
     U64[idx] = u;
     local += fabs(u);
   }
@@ -243,7 +245,7 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   const size_t nT = ((size_t)1 << p.w) < 4 ? 4 : ((size_t)1 << p.w);
   w.hdr = reinterpret_cast<DevHeader*>(take(sizeof(DevHeader)));
   w.U = reinterpret_cast<int32_t*>(take(nn * 4));
-  w.U64 = reinterpret_cast<double*>(take(p.dtype == QUBO_FP32 ? nn * 8 : 8));
+  w.U64 = reinterpret_cast<double*>(take(p.dtype != QUBO_INT32 ? nn * 8 : 8));
   w.M = reinterpret_cast<int32_t*>(take((size_t)(p.n - p.C > 0 ? p.n - p.C : 1) * ncols * 4));
   w.Ec = reinterpret_cast<int32_t*>(take(ncols * 4 < 16 ? 16 : ncols * 4));
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));

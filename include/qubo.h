@@ -22,6 +22,8 @@
  *    of U with a proven error band, and every state inside the band is re-evaluated in fp64, so
  *    the returned minimiser is the exact fp64 minimiser (lowest rank among equal fp64 values).
  *    Non-finite entries fail with QUBO_ERR_NONFINITE.
+ *  - dtype QUBO_FP64: as QUBO_FP32 with fp64 entries (8 bytes each); the fold and every energy
+ *    are the same fp64 operations. The batched entry points take int32 only.
  *  - out_min_energy receives E_min (exact for int32), out_argmin_x[n] receives x in {0,1}
  *    (x_0 first), out_tie_count the number of minimisers (for fp32: states with fp64 energy
  *    equal to E_min). On error no output is written.
@@ -48,12 +50,13 @@ extern "C" {
 /* dtype codes */
 #define QUBO_INT32 0
 #define QUBO_FP32 1
+#define QUBO_FP64 2 /* fp64 input: the same fp64 semantics as QUBO_FP32, without the input rounding */
 
 /* status codes (0 or negative) */
 #define QUBO_OK 0
 #define QUBO_ERR_ARG (-1)       /* n out of range, null pointer, bad dtype, bad slice id */
 #define QUBO_ERR_RANGE (-2)     /* int32: S > 2^30 - 1 */
-#define QUBO_ERR_NONFINITE (-3) /* fp32: NaN or Inf in Q */
+#define QUBO_ERR_NONFINITE (-3) /* fp32/fp64: NaN or Inf in Q */
 #define QUBO_ERR_PLAN (-4)      /* explicit k_prefix / cache_bits the kernels cannot run */
 #define QUBO_ERR_CUDA (-5)      /* a CUDA call failed (message via qubo_last_error) */
 #define QUBO_ERR_NODEV (-6)     /* no CUDA device */
@@ -86,7 +89,7 @@ typedef struct qubo_plan_desc {
                           (opt-in: environment QUBO_TENSOR_CORES=1); 0: on the CUDA-core kernel */
 } qubo_plan_desc;
 
-/* Minimise one QUBO. Q is a HOST pointer to n*n int32 or fp32 values (row-major).
+/* Minimise one QUBO. Q is a HOST pointer to n*n int32, fp32 or fp64 values (row-major).
  * (Algorithm 2 of §III-B with the §III-C1 split; inputs Q, A/B sizes; outputs x_opt, E_min.) */
 QUBO_API int qubo_solve(int n, const void* Q, int dtype, int k_prefix, int cache_bits, double* out_min_energy,
                uint8_t* out_argmin_x, uint64_t* out_tie_count);
@@ -148,6 +151,29 @@ QUBO_API int qubo_solve_slice_range_device(int n, const void* d_Q, int dtype, in
 QUBO_API size_t qubo_batched_workspace_bytes(int batch, int n, int dtype);
 QUBO_API int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void* d_workspace,
                               size_t workspace_bytes, void* cuda_stream, qubo_result* d_results);
+
+/* ---- Ising input ----
+ * §I: the Ising form with spins s in {-1,+1} and the QUBO form are the same problem under
+ * s = 2x - 1. Convention: H(s) = sum_{i,j} J_ij s_i s_j + sum_i h_i s_i over all i, j (only
+ * J_ij + J_ji matters off the diagonal; J_ii adds the constant J_ii). J is n*n row-major, h has n
+ * entries or is NULL (zero field); both have the element type of dtype.
+ *
+ * qubo_ising_to_qubo: the exact equivalent QUBO, upper triangular, and the offset C with
+ * H(s) = E_Q(x) + C for x = (s + 1) / 2:
+ *   Q_ij = 4 (J_ij + J_ji) (i < j),  Q_ii = 2 h_i - 2 sum_{j != i} (J_ij + J_ji),
+ *   C = sum_{i<j} (J_ij + J_ji) - sum_i h_i + sum_i J_ii.
+ * dtype QUBO_INT32: out_Q receives n*n int32 (computed in int64; QUBO_ERR_RANGE if an entry
+ * leaves int32); C is exact. QUBO_FP32 / QUBO_FP64: out_Q receives n*n fp64 computed in fp64
+ * (fixed order); non-finite input or output gives QUBO_ERR_NONFINITE. */
+QUBO_API int qubo_ising_to_qubo(int n, const void* J, const void* h, int dtype, void* out_Q, double* out_offset);
+
+/* Minimise H(s) over all 2^n spin states: converts as above and runs qubo_solve (int32 input
+ * stays int32; fp32/fp64 input is searched as the fp64 QUBO). out_min_H = E_min + C (exact for
+ * int32), out_argmin_s[n] in {-1,+1} is the ground state whose bit vector x = (s + 1) / 2 has the
+ * lowest rank, out_tie_count the number of ground states. Errors as qubo_solve; outputs are
+ * untouched on error. */
+QUBO_API int qubo_solve_ising(int n, const void* J, const void* h, int dtype, int k_prefix, int cache_bits,
+                              double* out_min_H, int8_t* out_argmin_s, uint64_t* out_tie_count);
 
 /* Planner decision for qubo_solve(n, ., dtype, k_prefix, cache_bits) on the current device. */
 QUBO_API int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* out);

@@ -62,6 +62,11 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
         lib.oracle_num_threads.restype = ctypes.c_int
         lib.oracle_fold_i32.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_fold_f32.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_fold_f64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_ising_direct_i64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64,
+                                                ctypes.c_uint64, _i64p, _u64p, _u64p]
+        lib.oracle_ising_direct_f64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64,
+                                                ctypes.c_uint64, _f64p, _u64p, _u64p]
         lib.oracle_energy_i64.restype = ctypes.c_int64
         lib.oracle_energy_i64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_eval64.restype = ctypes.c_double
@@ -121,6 +126,13 @@ class Oracle:
         self.lib.oracle_fold_f32(n, _ptr(Q), _ptr(U))
         return U
 
+    def fold_f64(self, Q) -> np.ndarray:
+        Q = np.ascontiguousarray(Q, dtype=np.float64)
+        n = Q.shape[0]
+        U = np.zeros((n, n), dtype=np.float64)
+        self.lib.oracle_fold_f64(n, _ptr(Q), _ptr(U))
+        return U
+
     def energy_i64(self, U, x) -> int:
         U = np.ascontiguousarray(U, dtype=np.int64)
         x = np.ascontiguousarray(x, dtype=np.uint8)
@@ -144,6 +156,28 @@ class Oracle:
         e, r, t = ctypes.c_int64(), ctypes.c_uint64(), ctypes.c_uint64()
         self.lib.oracle_direct_i64(n, _ptr(U), lo, hi, ctypes.byref(e), ctypes.byref(r), ctypes.byref(t))
         return int(e.value), int(r.value), int(t.value)
+
+    def ising_direct(self, J, h=None):
+        """Ising ground state by direct evaluation of H(s) = sum_ij J_ij s_i s_j + sum_i h_i s_i over
+        all 2^n spin states: (H_min, spins of the lowest-rank ground state as int8, ground states)."""
+        J = np.asarray(J)
+        n = J.shape[0]
+        if J.dtype.kind == "f":
+            Jd = np.ascontiguousarray(J, dtype=np.float64)
+            hd = None if h is None else np.ascontiguousarray(h, dtype=np.float64)
+            e, r, t = ctypes.c_double(), ctypes.c_uint64(), ctypes.c_uint64()
+            self.lib.oracle_ising_direct_f64(n, _ptr(Jd), None if hd is None else _ptr(hd), 0, 1 << n,
+                                             ctypes.byref(e), ctypes.byref(r), ctypes.byref(t))
+            H = float(e.value)
+        else:
+            Jd = np.ascontiguousarray(J, dtype=np.int64)
+            hd = None if h is None else np.ascontiguousarray(h, dtype=np.int64)
+            e, r, t = ctypes.c_int64(), ctypes.c_uint64(), ctypes.c_uint64()
+            self.lib.oracle_ising_direct_i64(n, _ptr(Jd), None if hd is None else _ptr(hd), 0, 1 << n,
+                                             ctypes.byref(e), ctypes.byref(r), ctypes.byref(t))
+            H = int(e.value)
+        s = 2 * bits_of_rank(n, int(r.value)).astype(np.int8) - 1
+        return H, s, int(t.value)
 
     def gray_i64(self, U, k: int = 0, prefix: int = 0):
         U = np.ascontiguousarray(U, dtype=np.int64)
@@ -187,15 +221,15 @@ class Oracle:
 
     # -- whole-problem entry points on the raw Q
     def solve(self, Q, method: str = "gray"):
-        """(E_min, argmin bits, ties) of the raw matrix Q (int32 or fp32), whole state space."""
+        """(E_min, argmin bits, ties) of the raw matrix Q (int32, fp32 or fp64), whole state space."""
         return self.solve_slice(Q, 0, 0, method)
 
     def solve_slice(self, Q, k: int, prefix: int, method: str = "gray"):
         """Same, restricted to the states whose first k variables equal `prefix` (MSB first)."""
         Q = np.asarray(Q)
         n = Q.shape[0]
-        if Q.dtype == np.float32:
-            U = self.fold_f32(Q)
+        if Q.dtype in (np.float32, np.float64):
+            U = self.fold_f32(Q) if Q.dtype == np.float32 else self.fold_f64(Q)
             if method == "direct":
                 e, r, t = self.direct_f64(U, prefix << (n - k), (prefix + 1) << (n - k))
             else:

@@ -26,6 +26,8 @@
  *                       flipping x_k changes E by d*(U_kk + h_k), h_v = sum_{u != v} U_uv x_u,
  *                       then every other field moves by d*U_kv.
  * Both take a fixed prefix (the first k variables), which is the subproblem split of §III-C1.
+ *   oracle_ising_direct_* -- the Ising energy H(s) of §I from its definition, per spin state
+ *                       (no conversion to the QUBO form), for the Ising entry points.
  *
  * Parity pins for every function live in tests/test_oracle.py.
  */
@@ -87,6 +89,17 @@ ORACLE_API void oracle_fold_f32(int n, const float* Q, double* U) {
       double v = 0.0;
       if (j == i) v = (double)Q[i * n + i];
       else if (j > i) v = (double)Q[i * n + j] + (double)Q[j * n + i];
+      U[i * n + j] = v;
+    }
+}
+
+/* The same fold for fp64 input (one fp64 add per off-diagonal pair). */
+ORACLE_API void oracle_fold_f64(int n, const double* Q, double* U) {
+  for (int i = 0; i < n; ++i)
+    for (int j = 0; j < n; ++j) {
+      double v = 0.0;
+      if (j == i) v = Q[i * n + i];
+      else if (j > i) v = Q[i * n + j] + Q[j * n + i];
       U[i * n + j] = v;
     }
 }
@@ -463,4 +476,77 @@ ORACLE_API int64_t oracle_subproblem_i64(int n, const int64_t* U, int k, uint64_
       Qr[a * m + b] = v;
     }
   return c;
+}
+
+/* ---------------------------------------------------------------- Ising form (§I) */
+
+/* H(s) = sum_{i,j} J_ij s_i s_j + sum_i h_i s_i with s_i = 2 x_i - 1, evaluated from its
+ * definition for every state with rank(x) in [lo, hi) (no conversion to the QUBO form): the
+ * minimum, the lowest rank reaching it and the number of states reaching it. h may be NULL. */
+ORACLE_API void oracle_ising_direct_i64(int n, const int64_t* J, const int64_t* h, uint64_t lo, uint64_t hi,
+                                        int64_t* hmin, uint64_t* argmin, uint64_t* ties) {
+  res_i64 total = {0, 0, 0, 0};
+  int nt = thread_count();
+  res_i64* part = (res_i64*)calloc((size_t)nt, sizeof(res_i64));
+#pragma omp parallel
+  {
+    int t = 0;
+#ifdef _OPENMP
+    t = omp_get_thread_num();
+#endif
+    uint8_t x[64];
+    res_i64 r = {0, 0, 0, 0};
+#pragma omp for schedule(static)
+    for (int64_t st = (int64_t)lo; st < (int64_t)hi; ++st) {
+      bits_of_rank(n, (uint64_t)st, x);
+      int64_t H = 0;
+      for (int i = 0; i < n; ++i) {
+        const int64_t si = x[i] ? 1 : -1;
+        for (int j = 0; j < n; ++j) H += J[i * n + j] * si * (x[j] ? 1 : -1);
+        if (h) H += h[i] * si;
+      }
+      see_i64(&r, H, (uint64_t)st);
+    }
+    part[t] = r;
+  }
+  for (int t = 0; t < nt; ++t) merge_i64(&total, &part[t]);
+  free(part);
+  *hmin = total.e;
+  *argmin = total.rank;
+  *ties = total.ties;
+}
+
+/* The same in fp64 (sum in the order written: i ascending, j ascending, then the field). */
+ORACLE_API void oracle_ising_direct_f64(int n, const double* J, const double* h, uint64_t lo, uint64_t hi,
+                                        double* hmin, uint64_t* argmin, uint64_t* ties) {
+  res_f64 total = {0, 0, 0, 0};
+  int nt = thread_count();
+  res_f64* part = (res_f64*)calloc((size_t)nt, sizeof(res_f64));
+#pragma omp parallel
+  {
+    int t = 0;
+#ifdef _OPENMP
+    t = omp_get_thread_num();
+#endif
+    uint8_t x[64];
+    res_f64 r = {0, 0, 0, 0};
+#pragma omp for schedule(static)
+    for (int64_t st = (int64_t)lo; st < (int64_t)hi; ++st) {
+      bits_of_rank(n, (uint64_t)st, x);
+      double H = 0.0;
+      for (int i = 0; i < n; ++i) {
+        const double si = x[i] ? 1.0 : -1.0;
+        for (int j = 0; j < n; ++j) H += J[i * n + j] * si * (x[j] ? 1.0 : -1.0);
+        if (h) H += h[i] * si;
+      }
+      if (!r.have || H < r.e) { r.e = H; r.rank = (uint64_t)st; r.ties = 1; r.have = 1; }
+      else if (H == r.e) { r.ties += 1; if ((uint64_t)st < r.rank) r.rank = (uint64_t)st; }
+    }
+    part[t] = r;
+  }
+  for (int t = 0; t < nt; ++t) merge_f64(&total, &part[t]);
+  free(part);
+  *hmin = total.e;
+  *argmin = total.rank;
+  *ties = total.ties;
 }

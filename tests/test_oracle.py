@@ -272,3 +272,67 @@ def test_generator_stream_definition():
     assert v.min() >= -1000 and v.max() <= 1000
     z = qi.Stream(6).normals(20000)
     assert abs(z.mean()) < 0.05 and abs(z.std() - 1) < 0.05
+
+
+# ---------------------------------------------------------------- Ising form (§I)
+
+def brute_ising(J, h):
+    """Pure-Python H(s) = sum_{i,j} J_ij s_i s_j + sum_i h_i s_i over all s (tiny n only)."""
+    n = len(J)
+    best, arg, ties = None, None, 0
+    for r, x in enumerate(itertools.product((0, 1), repeat=n)):
+        s = [2 * b - 1 for b in x]
+        H = sum(int(J[i][j]) * s[i] * s[j] for i in range(n) for j in range(n)) + sum(int(h[i]) * s[i] for i in range(n))
+        if best is None or H < best:
+            best, arg, ties = H, r, 1
+        elif H == best:
+            ties += 1
+    return best, arg, ties
+
+
+def test_ising_two_spin_example():
+    # H = s0 s1: the two anti-aligned states are the ground states, H = -1; x = (0, 1) has rank 1
+    H, s, t = O.ising_direct(np.array([[0, 1], [0, 0]], np.int64))
+    assert (H, t) == (-1, 2) and list(s) == [-1, 1]
+
+
+def test_ising_field_only_closed_form():
+    h = np.array([3, -2, 0, 5, -1], np.int64)
+    H, s, t = O.ising_direct(np.zeros((5, 5), np.int64), h)
+    assert H == -int(np.abs(h).sum()) and t == 2  # one free spin (h = 0)
+    assert list(s) == [-1, 1, -1, -1, 1]          # s_i = -sign(h_i); the free spin takes -1 (rank)
+
+
+@pytest.mark.parametrize("seed", [1, 2, 3])
+def test_ising_direct_matches_brute_force(seed):
+    st = qi.Stream(700 + seed)
+    n = 7
+    J = st.integers(-9, 9, n * n).reshape(n, n)
+    h = st.integers(-9, 9, n)
+    H, s, t = O.ising_direct(J, h)
+    bh, br, bt = brute_ising(J, h)
+    assert (H, t) == (bh, bt)
+    assert list(s) == [2 * ((br >> (n - 1 - i)) & 1) - 1 for i in range(n)]
+    Hf, sf, tf = O.ising_direct(J.astype(np.float64), h.astype(np.float64))  # fp64 twin
+    assert (Hf, tf) == (float(bh), bt) and (sf == s).all()
+
+
+def test_ising_direct_invariances():
+    st = qi.Stream(711)
+    n = 9
+    J = st.integers(-20, 20, n * n).reshape(n, n)
+    h = st.integers(-20, 20, n)
+    H, s, t = O.ising_direct(J, h)
+    assert O.ising_direct(J.T, h)[0] == H                        # only J_ij + J_ji matters
+    Jd = J + np.diag(st.integers(-5, 5, n))
+    assert O.ising_direct(Jd, h)[0] == H + int(np.diag(Jd - J).sum())  # J_ii s_i^2 is a constant
+    assert O.ising_direct(J, -h)[0] == O.ising_direct(J, h)[0]   # s -> -s symmetry of the pair terms
+
+
+@pytest.mark.parametrize("n,seed", [(10, 4), (14, 5), (18, 6)])
+def test_ising_direct_mattis_closed_form(n, seed):
+    s_star, w, J = qi.mattis_couplings(n, 1, 100, seed)
+    H, s, t = O.ising_direct(J)
+    assert H == -int(np.triu(w, 1).sum()) and t == 2
+    want = s_star if s_star[0] == -1 else -s_star
+    assert (s == want).all()
