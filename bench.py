@@ -328,14 +328,20 @@ def other_configs(q, torch, dev, stream):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) / reps
 
-    for name, n, Q, dt in (("n36_fp32", 36, qi.workload_n36_f32(), q.FP32), ("n32_int32", 32, qi.workload_n32(), q.INT32),
+    for name, n, Q, dt in (("n40_narrow_int32", 40, qi.workload_n40_narrow(), q.INT32),
+                           ("n36_fp32", 36, qi.workload_n36_f32(), q.FP32), ("n32_int32", 32, qi.workload_n32(), q.INT32),
                            ("n20_int32", 20, qi.workload_n20(), q.INT32)):
         dq = torch.from_numpy(Q).to(dev)
         nb = q.workspace_bytes(n, dt)
         ws = torch.empty(nb, dtype=torch.uint8, device=dev)
         res = torch.zeros(32, dtype=torch.uint8, device=dev)
         ms = timed(lambda: q.solve_device(n, dq, dt, ws, nb, stream.cuda_stream, res))
-        out[name] = {"ms": ms, "states_per_s": (1 << n) / (ms * 1e-3)}
+        kern = q.kernel_time_ms()
+        out[name] = {"ms": ms, "states_per_s": (1 << n) / (ms * 1e-3), "min_pass_ms": kern,
+                     "min_pass_states_per_s": (1 << n) / (kern * 1e-3) if kern > 0 else None}
+        if name == "n40_narrow_int32":
+            out[name]["workload"] = ("n=40 dense QUBO, int32 upper-triangular, entries uniform in [-4,4] "
+                                     "(sum |U| = 1822: the packed 16x2 minimum pass)")
     Qs = qi.workload_batched()
     dq = torch.from_numpy(Qs).to(dev)
     nb = max(q.batched_workspace_bytes(4096, 24), 256)
@@ -352,6 +358,8 @@ def profile_case(n: int, dtype_name: str):
     import exact_qubo_exhaustive_gb300 as q
     if dtype_name == "fp32":
         Q, dt = qi.random_symmetric_normal_f32(n, qi.MASTER_SEED + 3), q.FP32
+    elif dtype_name == "int32_narrow":
+        Q, dt = qi.random_upper_int(n, -4, 4, qi.MASTER_SEED + 5), q.INT32
     else:
         Q, dt = qi.random_upper_int(n, -1000, 1000, qi.MASTER_SEED + 2), q.INT32
     dq = torch.from_numpy(Q).cuda()
@@ -378,7 +386,7 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="only run two searches of an N-variable instance (for ncu), print no JSON")
-    ap.add_argument("--profile-dtype", choices=["int32", "fp32"], default="int32")
+    ap.add_argument("--profile-dtype", choices=["int32", "fp32", "int32_narrow"], default="int32")
     args = ap.parse_args(argv)
     if args.profile_case:
         return profile_case(args.profile_case, args.profile_dtype)

@@ -32,6 +32,8 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
       if (KIND == 3) a[k] = __viaddmin_s32(a[k], x, y);
       if (KIND == 4) f[k] = __fadd_rn(f[k], f[(k + 1) % kChains]);
       if (KIND == 5) f[k] = fminf(f[k], f[(k + 1) % kChains]);
+      if (KIND == 6) a[k] = (int)__vimin3_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
+      if (KIND == 7) a[k] = (int)__viaddmin_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
     }
   }
   const unsigned long long c1 = clock64();
@@ -73,7 +75,9 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       case 2: return launch<2>(blocks, it, out, clk);
       case 3: return launch<3>(blocks, it, out, clk);
       case 4: return launch<4>(blocks, it, out, clk);
-      default: return launch<5>(blocks, it, out, clk);
+      case 5: return launch<5>(blocks, it, out, clk);
+      case 6: return launch<6>(blocks, it, out, clk);
+      default: return launch<7>(blocks, it, out, clk);
     }
   };
   cudaEvent_t e0 = nullptr, e1 = nullptr;

@@ -250,6 +250,18 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   // Biased-binade minimum pass (int32 input; it needs at least one iteration of 2^(kBiasedR+1)
   // Gray steps and stages fewer shared rows than the int32 pass, so the same launch shape fits).
   p.biased = p.variant == kFast && dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
+  // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
+  // shared rows are 2 bytes per column.
+  if (p.variant == kFast && dtype == QUBO_INT32 && p.C >= 10 && p.w >= kPackedR + 1) {
+    p.packed_threads = (1 << p.C) / 32;
+    p.packed_smem = packed_smem_bytes(p.C, p.w);
+    int pocc = 0;
+    if (p.packed_smem + kStaticSmemReserve <= di.smem_optin &&
+        occupancy_packed(p.packed_threads, p.packed_smem, &pocc) == cudaSuccess && pocc >= 1) {
+      p.packed = true;
+      p.packed_blocks = std::max(1, di.sms) * pocc;
+    }
+  }
   // Tensor-core minimum pass for int32 input on sm_10x: the split needs >= 8 walked bits
   // (7 MMA row bits + at least one Gray-walked bit) and a Gray table of at most 2^24 entries.
   const int w8 = n - p.F - kTcC;
@@ -633,6 +645,8 @@ int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* ou
   out->workspace_bytes = layout_workspace(p, nullptr).bytes;
   out->smem_bytes = p.smem_bytes;
   out->tensor_cores = p.tc ? 1 : 0;
+  out->packed = p.packed ? 1 : 0;
+  out->biased = p.biased ? 1 : 0;
   return QUBO_OK;
 }
 
@@ -658,7 +672,7 @@ void qubo_request_abort(void) { g_abort = 1; }
 void qubo_clear_abort(void) { g_abort = 0; }
 
 int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz) {
-  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 5) return QUBO_ERR_ARG;
+  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 7) return QUBO_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   int dev, st;
   if ((st = current_device(&dev))) return st;

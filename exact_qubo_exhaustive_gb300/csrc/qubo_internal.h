@@ -22,6 +22,7 @@ enum Variant : int {
 constexpr int kFastCPT = 16;
 constexpr int kFastR = 4;
 constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
+constexpr int kPackedR = 5;  // register rows of the packed 16x2 minimum pass
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 
@@ -33,6 +34,9 @@ constexpr int64_t kTcMaxAbsSum = int64_t(1) << 21;  // every MMA operand piece a
 // Biased fp32 minimum walk: every running column energy is a sum of distinct U entries, so
 // |V| <= sum |U| < 2^22 keeps 1.5 * 2^23 + V inside the binade [2^23, 2^24).
 constexpr int64_t kBiasedWalkMaxAbsSum = (int64_t(1) << 22) - 1;
+// Packed 16x2 minimum walk: column energies within sum |U| and (best - offset) within 2 sum |U|
+// stay inside (-2^15, 2^15) when sum |U| < 2^14.
+constexpr int64_t kPackedMaxAbsSum = (int64_t(1) << 14) - 1;
 
 // Written by the device, read back by the host (lives at the start of the workspace).
 struct DevHeader {
@@ -65,6 +69,10 @@ struct Plan {
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
   bool tc = false;         // tensor-core minimum pass (int32, sum |U| <= kTcMaxAbsSum)
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
+  bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
+  int packed_threads = 0;  // 2^C / 32
+  int packed_blocks = 0;
+  size_t packed_smem = 0;
   int w8 = 0;              // walked bits of the tensor-core split: n - F - kTcC
   int tc_blocks = 0;       // grid of the tensor-core pass (one block per SM)
 };
@@ -77,6 +85,7 @@ struct Work {
   int32_t* M = nullptr;     // (n - C) x 2^C: interaction of each non-cached variable with each column
   int32_t* Ec = nullptr;    // 2^C: energy of the cached variables alone
   int32_t* T = nullptr;     // 2^w (padded): walked-variable energy, in Gray order
+  uint32_t* T2 = nullptr;   // packed pass: T's low 16 bits in both halves
   int32_t* unit_min = nullptr;
   uint32_t* tied = nullptr;
   uint64_t* gbase = nullptr;  // first unit prefix of each group

@@ -122,9 +122,11 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
 //   M[v][j]  = sum_{cached b} U[v][b] x_b(j)        interaction rows M_int, v < n - C
 //   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
 //   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
+//   T2[i]    = (T[i] mod 2^16) in both 16-bit halves (packed pass; optional)
 // ------------------------------------------------------------------------------------------------
 __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __restrict__ hdr,
-                              const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint64_t nTpad) {
+                              const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint32_t* T2,
+                              uint64_t nTpad) {
   if (hdr->status != QUBO_OK) return;
   const int ncols = 1 << C;
   const uint64_t nM = (uint64_t)(n - C) << C;
@@ -153,6 +155,7 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
       const uint64_t i = idx - nM - nE;
       if (i >= ((uint64_t)1 << w)) {
         T[i] = 0;
+        if (T2) T2[i] = 0;
         continue;
       }
       const uint64_t g = i ^ (i >> 1);
@@ -165,6 +168,7 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
           if ((g >> b) & 1u) acc += U[(n - C - 1 - b) * n + va];  // n-C-1-b <= va
       }
       T[i] = acc;
+      if (T2) T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
     }
   }
 }
@@ -249,6 +253,7 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.M = reinterpret_cast<int32_t*>(take((size_t)(p.n - p.C > 0 ? p.n - p.C : 1) * ncols * 4));
   w.Ec = reinterpret_cast<int32_t*>(take(ncols * 4 < 16 ? 16 : ncols * 4));
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));
+  if (p.packed) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
   w.unit_min = reinterpret_cast<int32_t*>(take(p.total_units * 4));
   w.tied = reinterpret_cast<uint32_t*>(take(p.total_units * 4));
   w.gbase = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
@@ -289,7 +294,7 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   const uint64_t nTpad = ((uint64_t)1 << p.w) < 4 ? 4 : ((uint64_t)1 << p.w);
   const uint64_t tab_work = ((uint64_t)(p.n - p.C) << p.C) + ((uint64_t)1 << p.C) + nTpad;
   const int tab_blocks = (int)((tab_work + 255) / 256 < 4096 ? (tab_work + 255) / 256 : 4096);
-  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, nTpad);
+  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, nTpad);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.tc) {
@@ -306,6 +311,7 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   kp.dtype = p.dtype;
   kp.tc_active = p.tc ? 1 : 0;
   kp.biased_active = p.biased ? 1 : 0;
+  kp.packed_active = p.packed ? 1 : 0;
   kp.seg_bits = p.seg_bits;
   kp.ngroups = p.ngroups;
   kp.upg = p.upg;
@@ -315,6 +321,7 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   kp.M = w.M;
   kp.Ec = w.Ec;
   kp.T = w.T;
+  kp.T2 = w.T2;
   kp.gbase = w.gbase;
   kp.unit_min = w.unit_min;
   kp.tied = w.tied;
@@ -349,8 +356,14 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
       if ((e = launch_tc_search(kp, p.w8, w.M8, w.E8, w.T8, tcb, stream)) != cudaSuccess) return e;
       ++nl;
     }
+    if (p.packed) {
+      // packed 16x2 CUDA-core pass (exits at once unless it owns the minimum pass) ...
+      const int pb = (int)(nunits < (uint64_t)p.packed_blocks ? nunits : (uint64_t)p.packed_blocks);
+      if ((e = launch_search_packed(kp, pb, p.packed_threads, p.packed_smem, stream)) != cudaSuccess) return e;
+      ++nl;
+    }
     if (p.biased) {
-      // biased-binade CUDA-core pass (exits at once beyond its range or when the tensor-core pass ran) ...
+      // biased-binade CUDA-core pass (exits at once unless it owns the minimum pass) ...
       if ((e = launch_search_biased(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
       ++nl;
     }

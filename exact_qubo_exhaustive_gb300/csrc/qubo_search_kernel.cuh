@@ -13,6 +13,7 @@ struct KParams {
   int dtype;
   int tc_active;            // a tensor-core minimum pass runs when sum |U| <= kTcMaxAbsSum
   int biased_active;        // a biased-binade minimum pass runs when sum |U| <= kBiasedWalkMaxAbsSum
+  int packed_active;        // a packed 16x2 minimum pass runs when sum |U| <= kPackedMaxAbsSum
   int seg_bits;             // resolve: segments per tied unit = 2^seg_bits
   int ngroups;
   uint64_t upg;             // units per group
@@ -23,6 +24,7 @@ struct KParams {
   const int32_t* M;
   const int32_t* Ec;
   const int32_t* T;
+  const uint32_t* T2;       // packed pass: T's low 16 bits in both halves
   const uint64_t* gbase;
   int32_t* unit_min;
   uint32_t* tied;
@@ -33,21 +35,33 @@ struct KParams {
   qubo_result* results;
 };
 
+// Which of the minimum passes of one launch sequence does the work; the others exit at once.
+// The tensor-core pass (opt-in) first, then the narrowest CUDA-core representation that the
+// proven range admits.
+enum MinPassOwner : int { kOwnerTc = 0, kOwnerPacked = 1, kOwnerBiased = 2, kOwnerInt = 3 };
+__device__ __forceinline__ int min_pass_owner(const KParams& p) {
+  const int64_t S = p.hdr->abs_sum;
+  if (p.tc_active && S <= kTcMaxAbsSum) return kOwnerTc;
+  if (p.packed_active && S <= kPackedMaxAbsSum) return kOwnerPacked;
+  if (p.biased_active && S <= kBiasedWalkMaxAbsSum) return kOwnerBiased;
+  return kOwnerInt;
+}
+
 // Linear terms of a unit with prefix P (F bits, bit F-1-f is x_f):
 //   sL[v] = sum_{f<F, x_f=1} U[f][v]                 for free v >= F (diag(x_f U_fr) of §III-C1),
 //   sL[f] = x_f * sum_{f<=f2<F, x_f2=1} U[f][f2]      for fixed f < F (their sum is c(P)).
 __device__ __forceinline__ void unit_linear_terms(const int32_t* __restrict__ U, int n, int F, uint64_t P, int* sL,
-                                                  int tid) {
-  if (tid < n) {
+                                                  int tid, int nthreads) {
+  for (int v = tid; v < n; v += nthreads) {
     int acc = 0;
-    if (tid >= F) {
+    if (v >= F) {
       for (int f = 0; f < F; ++f)
-        if ((P >> (F - 1 - f)) & 1u) acc += U[f * n + tid];
-    } else if ((P >> (F - 1 - tid)) & 1u) {
-      for (int f2 = tid; f2 < F; ++f2)
-        if ((P >> (F - 1 - f2)) & 1u) acc += U[tid * n + f2];
+        if ((P >> (F - 1 - f)) & 1u) acc += U[f * n + v];
+    } else if ((P >> (F - 1 - v)) & 1u) {
+      for (int f2 = v; f2 < F; ++f2)
+        if ((P >> (F - 1 - f2)) & 1u) acc += U[v * n + f2];
     }
-    sL[tid] = acc;
+    sL[v] = acc;
   }
 }
 
@@ -61,9 +75,8 @@ __device__ __forceinline__ int min_walk(const WalkCtx& c, const KParams& p, int 
   return W.aux - VOps<VT>::kBiasBits + W.s;
 }
 
-// BIASED: the minimum pass with column energies in the biased fp32 binade (VOps<float>); it runs
-// only when sum |U| <= kBiasedWalkMaxAbsSum, and the int32 minimum pass of the same launch
-// sequence then exits at once.
+// BIASED: the minimum pass with column energies in the biased fp32 binade (VOps<float>). Which
+// minimum pass of a launch sequence runs is decided on the device by min_pass_owner.
 template <int CPT, int R, int MODE, bool BIASED = false>
 __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const KParams p) {
   static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
@@ -71,11 +84,8 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   __shared__ int sL[64];
   __shared__ int s_red[32];
   if (p.hdr->status != QUBO_OK) return;
-  if (MODE == kModeMin && p.tc_active && p.hdr->abs_sum <= kTcMaxAbsSum) return;  // done on tensor cores
-  if constexpr (BIASED) {
-    if (p.hdr->abs_sum > kBiasedWalkMaxAbsSum) return;  // beyond the binade: the int32 pass runs
-  } else if constexpr (MODE == kModeMin) {
-    if (p.biased_active && p.hdr->abs_sum <= kBiasedWalkMaxAbsSum) return;  // done by the biased pass
+  if constexpr (MODE == kModeMin) {
+    if (min_pass_owner(p) != (BIASED ? kOwnerBiased : kOwnerInt)) return;  // another pass does it
   }
 
   const int tid = threadIdx.x;
@@ -142,7 +152,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
     const uint64_t prank = (F > 0) ? (P << (n - F)) : 0;
 
     __syncthreads();  // previous item is done with sL; staged rows are visible
-    unit_linear_terms(p.U, n, F, P, sL, tid);
+    unit_linear_terms(p.U, n, F, P, sL, tid, nthreads);
     __syncthreads();
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
@@ -203,6 +213,9 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 // Launch helpers (one translation unit per variant).
 cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t occupancy_packed(int threads, size_t smem, int* blocks_per_sm);
+size_t packed_smem_bytes(int C, int w);
 cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm);

@@ -194,7 +194,7 @@ __global__ void __launch_bounds__(kBlock, 1) tc_min_kernel(const KParams p, int 
     const uint64_t g = u / p.upg;
     const uint64_t P = p.gbase[g] + (u - g * p.upg);
     __syncthreads();  // the previous unit is finished by every warp
-    unit_linear_terms(p.U, n, F, P, sL, tid);
+    unit_linear_terms(p.U, n, F, P, sL, tid, (int)blockDim.x);
     __syncthreads();
     int s = 0;
     for (int f = 0; f < F; ++f) s += sL[f];

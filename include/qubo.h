@@ -87,6 +87,10 @@ typedef struct qubo_plan_desc {
   size_t smem_bytes;
   int tensor_cores;    /* 1: the minimum pass runs on tcgen05 tensor cores when sum |U_ij| <= 2^21
                           (opt-in: environment QUBO_TENSOR_CORES=1); 0: on the CUDA-core kernel */
+  int packed;          /* 1: int32 input whose sum |U_ij| <= 2^14 - 1 runs the minimum pass with two
+                          16-bit energies per 32-bit word (§IV-B.5's narrow path); 0: not available */
+  int biased;          /* 1: int32 input whose sum |U_ij| <= 2^22 - 1 (and not narrower) runs the
+                          minimum pass with fp32 column adds in the exact binade [2^23, 2^24) */
 } qubo_plan_desc;
 
 /* Minimise one QUBO. Q is a HOST pointer to n*n int32, fp32 or fp64 values (row-major).
@@ -202,7 +206,7 @@ QUBO_API void qubo_clear_abort(void);
  * independent chains of one operation per thread on every SM and reports warp-lane
  * operations per second and the SM clock seen by the kernel (clock64 / globaltimer).
  * kind: 0 int32 add, 1 int32 min, 2 int32 3-input min, 3 int32 add-then-min (fused),
- *       4 fp32 add, 5 fp32 min. */
+ *       4 fp32 add, 5 fp32 min, 6 packed 16x2 3-input min, 7 packed 16x2 add-then-min. */
 QUBO_API int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz);
 
 #ifdef __cplusplus

@@ -185,6 +185,11 @@ def workload_n40():
     return random_upper_int(40, -1000, 1000, MASTER_SEED + 2)
 
 
+def workload_n40_narrow():
+    """n=40 dense, entries uniform in [-4, 4]: sum |U| ~ 1.8e3, inside the 16-bit packed range."""
+    return random_upper_int(40, -4, 4, MASTER_SEED + 5)
+
+
 def workload_n36_f32():
     return random_symmetric_normal_f32(36, MASTER_SEED + 3)
 

@@ -58,9 +58,10 @@ def test_ising_fp_against_oracle(q, dt):
     x = ((s + 1) // 2).astype(np.uint8)
     r = int("".join(str(int(b)) for b in x), 2)
     import ctypes
+    Jd = np.ascontiguousarray(J, np.float64)  # kept alive across the call
+    hd = np.ascontiguousarray(h, np.float64)
     e, a, c = ctypes.c_double(), ctypes.c_uint64(), ctypes.c_uint64()
-    O.lib.oracle_ising_direct_f64(n, np.ascontiguousarray(J, np.float64).ctypes.data,
-                                  np.ascontiguousarray(h, np.float64).ctypes.data, r, r + 1,
+    O.lib.oracle_ising_direct_f64(n, Jd.ctypes.data, hd.ctypes.data, r, r + 1,
                                   ctypes.byref(e), ctypes.byref(a), ctypes.byref(c))
     assert abs(e.value - H) <= tol  # the returned spins reach the returned energy
 

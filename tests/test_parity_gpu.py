@@ -153,6 +153,53 @@ def test_int32_walk_large_values(q):
     check_int(q, Q)
 
 
+# ---------------------------------------------------------------- packed 16x2 minimum pass
+
+@pytest.mark.parametrize("n,lo,hi,seed", [(19, -30, 30, 1), (22, -20, 20, 2), (26, -9, 9, 3), (30, -3, 3, 4),
+                                          (31, 0, 2, 5)])
+def test_packed_pass_small_range(q, n, lo, hi, seed):
+    Q = qi.random_upper_int(n, lo, hi, 2400 + seed)
+    assert int(np.abs(Q.astype(np.int64)).sum()) <= (1 << 14) - 1
+    assert q.plan(n)["packed"] == 1
+    check_int(q, Q)
+
+
+@pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
+def test_packed_range_limit_is_exact(q, sign):
+    # sum |U| = 2^14 - 1 runs the packed pass (values pushed to +-sum |U|), 2^14 the biased one
+    n = 24
+    lo, hi = {"mixed": (-80, 80), "negative": (-80, -1), "positive": (1, 80)}[sign]
+    for total in ((1 << 14) - 1, 1 << 14):
+        Q = np.triu(qi.random_upper_int(n, lo, hi, 2450 + total % 5))
+        if sign == "positive":
+            Q = np.abs(Q)
+            Q[0, 0] = 0
+            Q[0, 0] = total - int(np.abs(Q.astype(np.int64)).sum())
+        else:
+            Q = _with_abs_sum(Q, total)
+        assert int(np.abs(Q.astype(np.int64)).sum()) == total
+        e, x, t = check_int(q, Q)
+        if sign == "negative":
+            assert e == -total and x.all()
+
+
+def test_packed_pass_all_ties(q):
+    # Q = 0: every state ties; the packed minimum is 0 and the resolve pass counts 2^n
+    e, x, t = q.solve(np.zeros((27, 27), np.int32))
+    assert (e, t) == (0, 1 << 27) and not x.any()
+
+
+def test_n40_narrow_slices_against_oracle(q):
+    Q = qi.workload_n40_narrow()
+    assert q.plan(40)["packed"] == 1
+    k = 16
+    ids = qi.Stream(4041).integers(0, (1 << k) - 1, 4).astype(np.uint64)
+    e, x, t = q.solve_slices(Q, k, ids)
+    for i, sid in enumerate(ids):
+        want = O.solve_slice(Q, k, int(sid))
+        assert (int(e[i]), int(t[i])) == (want[0], want[2]) and (x[i] == want[1]).all()
+
+
 # ---------------------------------------------------------------- configs
 
 def test_n20_config(q):
