@@ -342,6 +342,17 @@ def other_configs(q, torch, dev, stream):
         if name == "n40_narrow_int32":
             out[name]["workload"] = ("n=40 dense QUBO, int32 upper-triangular, entries uniform in [-4,4] "
                                      "(sum |U| = 1822: the packed 16x2 minimum pass)")
+    # k lowest energies of the n=40 workload through the host entry point (wall clock)
+    Q40 = qi.workload_n40()
+    q.solve_lowest(Q40, 1024)
+    t0 = time.perf_counter()
+    reps = 2
+    for _ in range(reps):
+        e40, _ = q.solve_lowest(Q40, 1024)
+    wall = (time.perf_counter() - t0) * 1e3 / reps
+    out["n40_lowest_k1024_int32"] = {"ms": wall, "states_per_s": (1 << 40) / (wall * 1e-3),
+                                     "e_first": int(e40[0]), "e_last": int(e40[-1]),
+                                     "timing": "host call, wall clock (includes H2D, passes, D2H, host sort)"}
     Qs = qi.workload_batched()
     dq = torch.from_numpy(Qs).to(dev)
     nb = max(q.batched_workspace_bytes(4096, 24), 256)

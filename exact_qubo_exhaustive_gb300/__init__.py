@@ -93,6 +93,8 @@ _sig = {
     "qubo_request_abort": (None, []),
     "qubo_clear_abort": (None, []),
     "qubo_probe_alu": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64p, _f64p]),
+    "qubo_solve_lowest": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                         ctypes.c_int, _f64p, _u8p, ctypes.POINTER(ctypes.c_int)]),
     "qubo_ising_to_qubo": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                           ctypes.c_void_p, _f64p]),
     "qubo_solve_ising": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
@@ -173,6 +175,22 @@ def solve_slice_range(Q, k_prefix: int, first_slice: int, num_slices: int, cache
     _check(_lib.qubo_solve_slice_range(n, Q.ctypes.data, dt, k_prefix, cache_bits, first_slice, num_slices,
                                        ctypes.byref(e), x.ctypes.data_as(_u8p), ctypes.byref(t)))
     return (int(e.value) if dt == INT32 else float(e.value)), x, int(t.value)
+
+
+LOWEST_MAX_K = 1 << 20
+
+
+def solve_lowest(Q, k: int, k_prefix: int = 0, cache_bits: int = 0):
+    """The min(k, 2^n) lowest states of x^T Q x (int32 Q): (energies int64[m], states uint8[m, n]),
+    ordered by energy, then by rank."""
+    Q, dt = _matrix(Q)
+    n = Q.shape[0]
+    e = np.zeros(k, np.float64)
+    x = np.zeros((k, n), np.uint8)
+    m = ctypes.c_int()
+    _check(_lib.qubo_solve_lowest(n, Q.ctypes.data, dt, k_prefix, cache_bits, k, e.ctypes.data_as(_f64p),
+                                  x.ctypes.data_as(_u8p), ctypes.byref(m)))
+    return e[:m.value].astype(np.int64), x[:m.value]
 
 
 def _ising_inputs(J, h):

@@ -345,6 +345,17 @@ int record_launch_count(int launches) {
 }
 
 int record_cuda_error(cudaError_t e, const char* where) { return set_cuda_error(e, where); }
+
+std::mutex& api_mutex() { return g_mu; }
+
+bool abort_requested() { return g_abort != 0; }
+
+int api_stream(cudaStream_t* s) {
+  const int st = prepare_device_buffers();
+  if (st) return st;
+  *s = g_buf.stream;
+  return QUBO_OK;
+}
 bool valid_dtype(int dtype) { return dtype == QUBO_INT32 || dtype == QUBO_FP32 || dtype == QUBO_FP64; }
 
 size_t dtype_bytes(int dtype) { return dtype == QUBO_FP64 ? 8 : 4; }

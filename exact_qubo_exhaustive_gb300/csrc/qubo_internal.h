@@ -3,6 +3,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -47,6 +49,13 @@ struct DevHeader {
   int64_t abs_sum;     // sum |U_ij| of the int32 image
   double abs_sum64;    // fp32 path: sum |U_ij| in fp64
   int32_t pad[8];
+};
+
+// One state found by the k-lowest passes: its energy and rank.
+struct KeyCand {
+  int32_t e;
+  int32_t pad;
+  uint64_t rank;
 };
 
 // Host-side plan (one call).
@@ -129,6 +138,9 @@ size_t dtype_bytes(int dtype);
 int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p);
 int record_launch_count(int launches);
 int record_cuda_error(cudaError_t e, const char* where);  // returns QUBO_ERR_CUDA
+std::mutex& api_mutex();      // serialises the host entry points
+bool abort_requested();       // qubo_request_abort() was called and not cleared
+int api_stream(cudaStream_t* s);  // the library's stream on the current device (QUBO_OK or an error)
 
 // Measurement.
 cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz);

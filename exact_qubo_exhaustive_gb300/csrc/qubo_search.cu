@@ -279,10 +279,11 @@ static cudaError_t launch_search(const Plan& p, int mode, const KParams& kp, int
   return launch_search_generic(mode, kp, blocks, p.threads, p.smem_bytes, s);
 }
 
-cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
-                       int* launches, const volatile int* abort_flag, bool* aborted, const KernelTiming* timing) {
-  int nl = 0;
-  if (aborted) *aborted = false;
+// Fold, tables and the minimum pass (unit minima in w.unit_min); fills kp for later passes.
+// Returns with *aborted set (and nothing further enqueued) when a cancellation is seen.
+static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
+                             int& nl, const volatile int* abort_flag, bool* aborted, const KernelTiming* timing,
+                             KParams& kp) {
   cudaError_t e;
   // gbase: uploaded by the host for slices and ranges; otherwise one group starting at unit 0,
   // written by the prep kernel.
@@ -302,7 +303,6 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
     ++nl;
   }
 
-  KParams kp;
   memset(&kp, 0, sizeof(kp));
   kp.n = p.n;
   kp.C = p.C;
@@ -343,7 +343,6 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   for (uint64_t u0 = 0; u0 < p.total_units; u0 += chunk) {
     if (abort_flag && *abort_flag) {
       if (aborted) *aborted = true;
-      if (launches) *launches = nl;
       return cudaSuccess;
     }
     kp.unit_begin = u0;
@@ -377,6 +376,20 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   }
 
   if (timing && (e = cudaEventRecord(timing->stop, stream)) != cudaSuccess) return e;
+  return cudaSuccess;
+}
+
+cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_result* res, cudaStream_t stream,
+                       int* launches, const volatile int* abort_flag, bool* aborted, const KernelTiming* timing) {
+  int nl = 0;
+  bool stop = false;
+  KParams kp;
+  cudaError_t e = run_front(p, d_Q, w, res, stream, nl, abort_flag, &stop, timing, kp);
+  if (aborted) *aborted = stop;
+  if (e != cudaSuccess || stop) {
+    if (launches) *launches = nl;
+    return e;
+  }
   const int gblocks = p.ngroups < 1024 ? p.ngroups : 1024;
   group_min_kernel<<<gblocks, 256, 0, stream>>>(kp);
   ++nl;
@@ -401,6 +414,29 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (launches) *launches = nl;
   return cudaSuccess;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Stages for drivers that decide between passes on the host (the k lowest energies).
+// ------------------------------------------------------------------------------------------------
+cudaError_t run_min_stage(const Plan& p, const void* d_Q, const Work& w, cudaStream_t stream, int* launches,
+                          KParams* kp_out) {
+  int nl = 0;
+  bool stop = false;
+  cudaError_t e = run_front(p, d_Q, w, nullptr, stream, nl, nullptr, &stop, nullptr, *kp_out);
+  if (launches) *launches = nl;
+  return e;
+}
+
+cudaError_t run_key_pass(const Plan& p, const KParams& base, int mode, int theta, uint64_t rho, KeyCand* cand,
+                         uint32_t cap, unsigned long long* counter, cudaStream_t stream) {
+  KParams kp = base;
+  kp.theta = theta;
+  kp.rho = rho;
+  kp.cand = cand;
+  kp.cand_cap = cap;
+  kp.cand_count = counter;
+  return launch_search(p, mode, kp, p.blocks, stream);
 }
 
 }  // namespace qgb

@@ -19,6 +19,8 @@ cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int th
     case kModeTiesInt: return launch_one<kModeTiesInt>(p, blocks, threads, smem, s);
     case kModeKeyFp: return launch_one<kModeKeyFp>(p, blocks, threads, smem, s);
     case kModeTiesFp: return launch_one<kModeTiesFp>(p, blocks, threads, smem, s);
+    case kModeCountKey: return launch_one<kModeCountKey>(p, blocks, threads, smem, s);
+    case kModeCollectKey: return launch_one<kModeCollectKey>(p, blocks, threads, smem, s);
   }
   return cudaErrorInvalidValue;
 }

@@ -33,6 +33,12 @@ struct KParams {
   uint64_t* gties;
   uint64_t* gkey;
   qubo_result* results;
+  // key modes (k lowest energies)
+  int theta;
+  uint64_t rho;
+  KeyCand* cand;
+  unsigned long long* cand_count;  // kModeCountKey: the count; kModeCollectKey: the append index
+  uint32_t cand_cap;
 };
 
 // Which of the minimum passes of one launch sequence does the work; the others exit at once.
@@ -127,6 +133,11 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   c.rows1 = reinterpret_cast<const int*>(s_rows4);
   c.T = p.T;
   c.t_global = true;
+  c.theta = p.theta;
+  c.rho = p.rho;
+  c.cand = p.cand;
+  c.cand_count = p.cand_count;
+  c.cand_cap = p.cand_cap;
 
   const int64_t niter = walk_iterations<R>(w);
   const int lane = tid & 31, warp = tid >> 5;
@@ -183,7 +194,11 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
       W.init(c, p.Ec, p.M, cP);
       W.seek(c, it0);
       uint64_t gk = 0;
-      W.aux = p.gmin[g] + p.hdr->band - W.s;
+      if constexpr (MODE == kModeCountKey || MODE == kModeCollectKey) {
+        W.aux = p.theta - W.s;
+      } else {
+        W.aux = p.gmin[g] + p.hdr->band - W.s;
+      }
       if constexpr (MODE == kModeTiesFp) gk = p.gkey[g];
       if (niter == 0) W.step(c, prank, 0, p.T[0], p.U64, gk);
       else W.walk(c, it0, it1, it1, prank, p.U64, gk);
@@ -199,6 +214,10 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
       if (lane == 0) {
         if constexpr (MODE == kModeKeyFp) {
           if (kmin != ~0ull) atomicMin(reinterpret_cast<unsigned long long*>(&p.gkey[g]), kmin);
+        } else if constexpr (MODE == kModeCountKey) {
+          if (cnt) atomicAdd(p.cand_count, (unsigned long long)cnt);
+        } else if constexpr (MODE == kModeCollectKey) {
+          // appended one by one during the walk
         } else {
           if (cnt) {
             atomicAdd(reinterpret_cast<unsigned long long*>(&p.gties[g]), cnt);
@@ -216,6 +235,16 @@ cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size
 cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_packed(int threads, size_t smem, int* blocks_per_sm);
 size_t packed_smem_bytes(int C, int w);
+
+// Fold, tables and minimum pass only (w.unit_min holds every unit's minimum afterwards); kp_out
+// receives the parameters for run_key_pass.
+cudaError_t run_min_stage(const Plan& p, const void* d_Q, const Work& w, cudaStream_t stream, int* launches,
+                          KParams* kp_out);
+// One pass over the units listed in w.tied (hdr->tied_count of them, 2^seg_bits segments each)
+// in mode kModeCountKey (adds to *counter the states with key (E, rank) < (theta, rho)) or
+// kModeCollectKey (appends them to cand[0, cap) at index atomicAdd(counter, 1)).
+cudaError_t run_key_pass(const Plan& p, const KParams& base, int mode, int theta, uint64_t rho, KeyCand* cand,
+                         uint32_t cap, unsigned long long* counter, cudaStream_t stream);
 cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm);

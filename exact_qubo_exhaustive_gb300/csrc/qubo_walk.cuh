@@ -139,6 +139,8 @@ enum WalkMode : int {
   kModeTiesInt = 1, // count states with energy <= threshold and keep the lowest rank
   kModeKeyFp = 2,   // lowest fp64 energy (order key) among states within the band
   kModeTiesFp = 3,  // count states whose fp64 energy equals the group's key, lowest rank
+  kModeCountKey = 4,    // count states whose key (E, rank) is below (theta, rho)
+  kModeCollectKey = 5,  // append every such state (E, rank) to a candidate buffer
 };
 
 // Everything one walk needs; pointers may be global or shared memory.
@@ -151,6 +153,12 @@ struct WalkCtx {
   const int* rows1;           //   the same rows, one int per column (generic)
   const int* T;               // walked energies in Gray order
   bool t_global;              // T lives in global memory (use the read-only path)
+  // key modes: states with E < theta, or E == theta and rank < rho
+  int theta;
+  uint64_t rho;
+  KeyCand* cand;              // kModeCollectKey: candidate buffer of cand_cap entries
+  unsigned long long* cand_count;
+  uint32_t cand_cap;
 };
 
 // Column of (thread t, slot jj). Fast layout: quads of 4 consecutive columns, quad k of thread t
@@ -309,6 +317,19 @@ struct Walker {
           if (order_key(eval64_rank(U64, c.n, rank)) == gkey) {
             ++cnt;
             rmin = rank < rmin ? rank : rmin;
+          }
+        } else if constexpr (MODE == kModeCountKey || MODE == kModeCollectKey) {
+          const int E = V[jj] + tv + s;  // <= theta by the filter above
+          if (E < c.theta || rank < c.rho) {
+            if constexpr (MODE == kModeCountKey) {
+              ++cnt;
+            } else {
+              const unsigned long long idx = atomicAdd(c.cand_count, 1ull);
+              if (idx < c.cand_cap) {
+                c.cand[idx].e = E;
+                c.cand[idx].rank = rank;
+              }
+            }
           }
         }
       }

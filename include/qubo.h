@@ -156,6 +156,19 @@ QUBO_API size_t qubo_batched_workspace_bytes(int batch, int n, int dtype);
 QUBO_API int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void* d_workspace,
                               size_t workspace_bytes, void* cuda_stream, qubo_result* d_results);
 
+/* ---- low-energy spectrum ----
+ * The k lowest energies (§I: the search sees every state, so it can return the low-energy
+ * spectrum, not only the minimum). Result: the min(k, 2^n) states with the smallest keys
+ * (E(x), rank(x)), in ascending order -- energies ascending, equal energies by rank -- so it is
+ * unique whatever the decomposition. out_energies[k] receives the energies (exact), out_x[k * n]
+ * the states (x_0 first), *out_count the number written. int32 input only (QUBO_ERR_ARG for other
+ * dtypes); 1 <= k <= QUBO_LOWEST_MAX_K. Q is a host pointer as for qubo_solve. The call runs the
+ * minimum pass, then re-walks only the units that can hold one of the k states (more passes
+ * only for very degenerate spectra). It allocates its device memory per call. */
+#define QUBO_LOWEST_MAX_K (1 << 20)
+QUBO_API int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, int cache_bits, int k,
+                               double* out_energies, uint8_t* out_x, int* out_count);
+
 /* ---- Ising input ----
  * §I: the Ising form with spins s in {-1,+1} and the QUBO form are the same problem under
  * s = 2x - 1. Convention: H(s) = sum_{i,j} J_ij s_i s_j + sum_i h_i s_i over all i, j (only

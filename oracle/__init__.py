@@ -63,6 +63,9 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
         lib.oracle_fold_i32.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_fold_f32.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_fold_f64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_lowest_i64.restype = ctypes.c_int
+        lib.oracle_lowest_i64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
+                                          ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_ising_direct_i64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64,
                                                 ctypes.c_uint64, _i64p, _u64p, _u64p]
         lib.oracle_ising_direct_f64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64,
@@ -156,6 +159,17 @@ class Oracle:
         e, r, t = ctypes.c_int64(), ctypes.c_uint64(), ctypes.c_uint64()
         self.lib.oracle_direct_i64(n, _ptr(U), lo, hi, ctypes.byref(e), ctypes.byref(r), ctypes.byref(t))
         return int(e.value), int(r.value), int(t.value)
+
+    def lowest(self, Q, k: int, lo: int = 0, hi: int | None = None):
+        """The k smallest keys (E, rank) of the int32 matrix Q among ranks [lo, hi), ascending:
+        (energies int64[m], states uint8[m, n])."""
+        U = self.fold_i32(Q)
+        n = U.shape[0]
+        hi = (1 << n) if hi is None else hi
+        e = np.zeros(k, np.int64)
+        r = np.zeros(k, np.uint64)
+        m = self.lib.oracle_lowest_i64(n, _ptr(U), k, lo, hi, _ptr(e), _ptr(r))
+        return e[:m], np.array([bits_of_rank(n, int(v)) for v in r[:m]], dtype=np.uint8).reshape(m, n)
 
     def ising_direct(self, J, h=None):
         """Ising ground state by direct evaluation of H(s) = sum_ij J_ij s_i s_j + sum_i h_i s_i over

@@ -26,6 +26,7 @@
  *                       flipping x_k changes E by d*(U_kk + h_k), h_v = sum_{u != v} U_uv x_u,
  *                       then every other field moves by d*U_kv.
  * Both take a fixed prefix (the first k variables), which is the subproblem split of §III-C1.
+ *   oracle_lowest_i64 -- the k smallest keys (E, rank), every state evaluated from scratch.
  *   oracle_ising_direct_* -- the Ising energy H(s) of §I from its definition, per spin state
  *                       (no conversion to the QUBO form), for the Ising entry points.
  *
@@ -549,4 +550,64 @@ ORACLE_API void oracle_ising_direct_f64(int n, const double* J, const double* h,
   *hmin = total.e;
   *argmin = total.rank;
   *ties = total.ties;
+}
+
+/* ---------------------------------------------------------------- lowest part of the spectrum */
+
+/* The k states with the smallest keys (E(x), rank(x)) among ranks [lo, hi), in ascending key
+ * order, each state evaluated from scratch (O(n^2)). Writes min(k, hi - lo) entries and returns
+ * that number. Each thread keeps a sorted array of its k best keys; the arrays are merged at the
+ * end. */
+typedef struct {
+  int64_t e;
+  uint64_t rank;
+} key_i64;
+
+static int key_less(key_i64 a, key_i64 b) { return a.e < b.e || (a.e == b.e && a.rank < b.rank); }
+
+static void keep_lowest(key_i64* top, int* m, int k, key_i64 x) {
+  if (*m == k && !key_less(x, top[k - 1])) return;
+  int i = (*m < k) ? (*m)++ : k - 1;
+  while (i > 0 && key_less(x, top[i - 1])) {
+    top[i] = top[i - 1];
+    --i;
+  }
+  top[i] = x;
+}
+
+ORACLE_API int oracle_lowest_i64(int n, const int64_t* U, int k, uint64_t lo, uint64_t hi, int64_t* out_e,
+                                 uint64_t* out_rank) {
+  if (k < 1) return 0;
+  int nt = thread_count();
+  key_i64* all = (key_i64*)calloc((size_t)nt * (size_t)k, sizeof(key_i64));
+  int* cnt = (int*)calloc((size_t)nt, sizeof(int));
+#pragma omp parallel
+  {
+    int t = 0;
+#ifdef _OPENMP
+    t = omp_get_thread_num();
+#endif
+    uint8_t x[64];
+    key_i64* top = all + (size_t)t * (size_t)k;
+    int m = 0;
+#pragma omp for schedule(static)
+    for (int64_t st = (int64_t)lo; st < (int64_t)hi; ++st) {
+      bits_of_rank(n, (uint64_t)st, x);
+      key_i64 v = {oracle_energy_i64(n, U, x), (uint64_t)st};
+      keep_lowest(top, &m, k, v);
+    }
+    cnt[t] = m;
+  }
+  key_i64* best = (key_i64*)calloc((size_t)k, sizeof(key_i64));
+  int m = 0;
+  for (int t = 0; t < nt; ++t)
+    for (int i = 0; i < cnt[t]; ++i) keep_lowest(best, &m, k, all[(size_t)t * (size_t)k + i]);
+  for (int i = 0; i < m; ++i) {
+    out_e[i] = best[i].e;
+    out_rank[i] = best[i].rank;
+  }
+  free(best);
+  free(cnt);
+  free(all);
+  return m;
 }

@@ -336,3 +336,47 @@ def test_ising_direct_mattis_closed_form(n, seed):
     assert H == -int(np.triu(w, 1).sum()) and t == 2
     want = s_star if s_star[0] == -1 else -s_star
     assert (s == want).all()
+
+
+# ---------------------------------------------------------------- lowest part of the spectrum
+
+def brute_spectrum(Q):
+    """All (E, rank) pairs of x^T Q x sorted by energy then rank (pure Python, tiny n)."""
+    n = len(Q)
+    keys = []
+    for r, x in enumerate(itertools.product((0, 1), repeat=n)):
+        keys.append((sum(int(Q[i][j]) for i in range(n) for j in range(n) if x[i] and x[j]), r))
+    return sorted(keys)
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_lowest_matches_sorted_brute_force(seed):
+    n = 8
+    Q = qi.random_full_int(n, -20, 20, 730 + seed)
+    want = brute_spectrum(Q)
+    for k in (1, 5, 37, 1 << n, (1 << n) + 10):
+        e, x = O.lowest(Q, k)
+        got = [(int(a), oracle.rank_of_bits(b)) for a, b in zip(e, x)]
+        assert got == want[:k]
+
+
+def test_lowest_k1_is_the_minimum_and_ranges_merge():
+    Q = qi.random_upper_int(14, -50, 50, 733)
+    e, x = O.lowest(Q, 1)
+    m = O.solve(Q)
+    assert e[0] == m[0] and (x[0] == m[1]).all()
+    k, n = 40, 14
+    whole = O.lowest(Q, k)
+    a, b = O.lowest(Q, k, 0, 5000), O.lowest(Q, k, 5000, 1 << n)
+    merged = sorted([(int(v), oracle.rank_of_bits(s)) for v, s in zip(*a)] +
+                    [(int(v), oracle.rank_of_bits(s)) for v, s in zip(*b)])[:k]
+    assert merged == [(int(v), oracle.rank_of_bits(s)) for v, s in zip(*whole)]
+
+
+def test_lowest_degenerate_and_diagonal_closed_forms():
+    e, x = O.lowest(np.zeros((10, 10), np.int32), 7)  # every state ties: ranks 0..6
+    assert (e == 0).all() and [oracle.rank_of_bits(s) for s in x] == list(range(7))
+    d = np.array([-5, 3, -2, 0], np.int32)  # E = sum of the chosen diagonal entries
+    e, x = O.lowest(np.diag(d), 16)
+    sub = sorted((int(sum(d[i] for i in range(4) if (r >> (3 - i)) & 1)), r) for r in range(16))
+    assert [(int(a), oracle.rank_of_bits(b)) for a, b in zip(e, x)] == sub

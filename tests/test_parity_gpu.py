@@ -153,6 +153,19 @@ def test_int32_walk_large_values(q):
     check_int(q, Q)
 
 
+def test_fewer_threads_than_variables(q):
+    # cache_bits = 9 gives 32-thread blocks (16 columns each) while n = 44 > 32: every variable's
+    # per-unit linear term must still be formed
+    n, k = 44, 22
+    Q = qi.random_upper_int(n, -200, 200, 2470)
+    assert q.plan(n, q.INT32, 0, 9)["threads_per_block"] < n
+    ids = qi.Stream(2471).integers(0, (1 << k) - 1, 3).astype(np.uint64)
+    e, x, t = q.solve_slices(Q, k, ids, cache_bits=9)
+    for i, sid in enumerate(ids):
+        want = O.solve_slice(Q, k, int(sid))
+        assert (int(e[i]), int(t[i])) == (want[0], want[2]) and (x[i] == want[1]).all()
+
+
 # ---------------------------------------------------------------- packed 16x2 minimum pass
 
 @pytest.mark.parametrize("n,lo,hi,seed", [(19, -30, 30, 1), (22, -20, 20, 2), (26, -9, 9, 3), (30, -3, 3, 4),
