@@ -353,6 +353,20 @@ def other_configs(q, torch, dev, stream):
     out["n40_lowest_k1024_int32"] = {"ms": wall, "states_per_s": (1 << 40) / (wall * 1e-3),
                                      "e_first": int(e40[0]), "e_last": int(e40[-1]),
                                      "timing": "host call, wall clock (includes H2D, passes, D2H, host sort)"}
+    # long-run driver: n=42 in 8 checkpointed chunks of 32 slices against one uninterrupted call
+    import tempfile
+    Q42 = qi.random_upper_int(42, -1000, 1000, qi.MASTER_SEED + 6)
+    q.solve(Q42)
+    t0 = time.perf_counter()
+    one = q.solve(Q42)
+    t_one = (time.perf_counter() - t0) * 1e3
+    with tempfile.TemporaryDirectory() as td:
+        t0 = time.perf_counter()
+        ck = q.solve_checkpointed(Q42, 8, os.path.join(td, "n42.ckpt"), slices_per_chunk=32)
+        t_ck = (time.perf_counter() - t0) * 1e3
+    out["n42_checkpointed_8_chunks_int32"] = {"ms": t_ck, "states_per_s": (1 << 42) / (t_ck * 1e-3),
+                                              "uninterrupted_ms": t_one, "same_result": ck[1] == one[0] and ck[3] == one[2],
+                                              "timing": "host calls, wall clock"}
     Qs = qi.workload_batched()
     dq = torch.from_numpy(Qs).to(dev)
     nb = max(q.batched_workspace_bytes(4096, 24), 256)

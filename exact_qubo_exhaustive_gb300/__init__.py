@@ -95,6 +95,13 @@ _sig = {
     "qubo_probe_alu": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, _f64p, _f64p]),
     "qubo_solve_lowest": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                          ctypes.c_int, _f64p, _u8p, ctypes.POINTER(ctypes.c_int)]),
+    "qubo_solve_checkpointed": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
+                                               ctypes.c_int, ctypes.c_uint64, ctypes.c_char_p, ctypes.c_double,
+                                               _f64p, _u8p, _u64p, _u64p]),
+    "qubo_checkpoint_read": (ctypes.c_int, [ctypes.c_char_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                            ctypes.POINTER(ctypes.c_int), _u64p, _u64p, _u64p,
+                                            ctypes.POINTER(ctypes.c_int), _f64p, _u64p, _u64p]),
+    "qubo_fnv1a64": (ctypes.c_uint64, [ctypes.c_void_p, ctypes.c_size_t]),
     "qubo_ising_to_qubo": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
                                           ctypes.c_void_p, _f64p]),
     "qubo_solve_ising": (ctypes.c_int, [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int, ctypes.c_int,
@@ -191,6 +198,50 @@ def solve_lowest(Q, k: int, k_prefix: int = 0, cache_bits: int = 0):
     _check(_lib.qubo_solve_lowest(n, Q.ctypes.data, dt, k_prefix, cache_bits, k, e.ctypes.data_as(_f64p),
                                   x.ctypes.data_as(_u8p), ctypes.byref(m)))
     return e[:m.value].astype(np.int64), x[:m.value]
+
+
+INCOMPLETE = 1
+
+
+def solve_checkpointed(Q, k_prefix: int, checkpoint_path: str, slices_per_chunk: int = 0,
+                       time_budget_s: float = 0.0, cache_bits: int = 0):
+    """Slice-chunked search that saves its progress after every chunk and resumes from the file.
+
+    Returns (complete, E, x, ties, slices_done): complete is False when the time budget ended the
+    call (E, x, ties then cover the slices done so far)."""
+    Q, dt = _matrix(Q)
+    n = Q.shape[0]
+    e = ctypes.c_double()
+    x = np.zeros(n, np.uint8)
+    t = ctypes.c_uint64()
+    done = ctypes.c_uint64()
+    st = _lib.qubo_solve_checkpointed(n, Q.ctypes.data, dt, k_prefix, cache_bits, slices_per_chunk,
+                                      os.fsencode(checkpoint_path), time_budget_s, ctypes.byref(e),
+                                      x.ctypes.data_as(_u8p), ctypes.byref(t), ctypes.byref(done))
+    if st not in (0, INCOMPLETE):
+        raise QuboError(st)
+    return st == 0, (int(e.value) if dt == INT32 else float(e.value)), x, int(t.value), int(done.value)
+
+
+def checkpoint_read(checkpoint_path: str) -> dict:
+    """Contents of a checkpoint file written by solve_checkpointed."""
+    ints = [ctypes.c_int() for _ in range(4)]
+    u64 = [ctypes.c_uint64() for _ in range(5)]
+    e = ctypes.c_double()
+    _check(_lib.qubo_checkpoint_read(os.fsencode(checkpoint_path), ctypes.byref(ints[0]), ctypes.byref(ints[1]),
+                                     ctypes.byref(ints[2]), ctypes.byref(u64[0]), ctypes.byref(u64[1]),
+                                     ctypes.byref(u64[2]), ctypes.byref(ints[3]), ctypes.byref(e),
+                                     ctypes.byref(u64[3]), ctypes.byref(u64[4])))
+    return {"n": ints[0].value, "dtype": ints[1].value, "k_prefix": ints[2].value, "q_hash": u64[0].value,
+            "next_slice": u64[1].value, "total_slices": u64[2].value, "have": ints[3].value,
+            "min_energy": e.value, "argmin_rank": u64[3].value, "tie_count": u64[4].value}
+
+
+def fnv1a64(data) -> int:
+    """The 64-bit FNV-1a hash the checkpoint files use to identify a problem."""
+    b = bytes(data)
+    buf = ctypes.create_string_buffer(b, len(b))
+    return int(_lib.qubo_fnv1a64(buf, len(b)))
 
 
 def _ising_inputs(J, h):

@@ -668,11 +668,13 @@ const char* qubo_status_string(int status) {
     case QUBO_OK: return "ok";
     case QUBO_ERR_ARG: return "invalid argument";
     case QUBO_ERR_RANGE: return "int32 range: sum of |U_ij| exceeds 2^30 - 1";
-    case QUBO_ERR_NONFINITE: return "non-finite entry in fp32 Q";
+    case QUBO_ERR_NONFINITE: return "non-finite entry in floating-point input";
     case QUBO_ERR_PLAN: return "no kernel plan for the requested k_prefix / cache_bits";
     case QUBO_ERR_CUDA: return "CUDA error";
     case QUBO_ERR_NODEV: return "no CUDA device";
     case QUBO_ERR_ABORTED: return "aborted";
+    case QUBO_ERR_CHECKPOINT: return "checkpoint file unreadable, corrupt, or of another problem";
+    case QUBO_INCOMPLETE: return "incomplete: time budget reached, progress saved";
   }
   return "unknown status";
 }

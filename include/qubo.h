@@ -61,6 +61,8 @@ extern "C" {
 #define QUBO_ERR_CUDA (-5)      /* a CUDA call failed (message via qubo_last_error) */
 #define QUBO_ERR_NODEV (-6)     /* no CUDA device */
 #define QUBO_ERR_ABORTED (-7)   /* the call was cancelled by qubo_request_abort() */
+#define QUBO_ERR_CHECKPOINT (-8) /* checkpoint file unreadable, corrupt, or of another problem */
+#define QUBO_INCOMPLETE 1        /* not an error: a time budget ended the call, progress is saved */
 
 /* Device-side result record: one per solved problem (or slice). */
 typedef struct qubo_result {
@@ -155,6 +157,38 @@ QUBO_API int qubo_solve_slice_range_device(int n, const void* d_Q, int dtype, in
 QUBO_API size_t qubo_batched_workspace_bytes(int batch, int n, int dtype);
 QUBO_API int qubo_solve_batched_device(int batch, int n, const void* d_Q, int dtype, void* d_workspace,
                               size_t workspace_bytes, void* cuda_stream, qubo_result* d_results);
+
+/* ---- long runs: checkpoint / resume ----
+ * §III-C1 / §IV-C: the 2^k_prefix slices (fixed first k_prefix variables) are independent, so a
+ * long search can stop between slices and continue later. qubo_solve_checkpointed processes the
+ * slices in ascending order, `slices_per_chunk` at a time (0: about 2^44 states per chunk), each
+ * chunk as one qubo_solve_slice_range call, and after every chunk rewrites the checkpoint file
+ * at `checkpoint_path` (written to "<path>.tmp", then renamed over it). The file holds the
+ * problem's identity (n, dtype, k_prefix, a 64-bit FNV-1a hash of Q's bytes), the next slice and
+ * the combined record so far (lowest energy; among equal energies the lowest rank and the summed
+ * tie count). If the file exists when the call starts, the call resumes from it; a file of
+ * another problem, or a corrupt one, gives QUBO_ERR_CHECKPOINT and is left untouched.
+ * time_budget_s > 0: no new chunk starts once that many seconds have passed since the call
+ * began (at least one chunk runs per call). Returns QUBO_OK when every slice is done
+ * (out_* hold the final result, exactly as qubo_solve would give), or QUBO_INCOMPLETE with the
+ * record over the slices done so far in out_* and their number in *out_slices_done. A
+ * qubo_request_abort() stops between chunks with QUBO_ERR_ABORTED (progress up to the last
+ * chunk is saved). 1 <= k_prefix < n. Other arguments and errors as qubo_solve_slice_range. */
+QUBO_API int qubo_solve_checkpointed(int n, const void* Q, int dtype, int k_prefix, int cache_bits,
+                                     uint64_t slices_per_chunk, const char* checkpoint_path, double time_budget_s,
+                                     double* out_min_energy, uint8_t* out_argmin_x, uint64_t* out_tie_count,
+                                     uint64_t* out_slices_done);
+
+/* Reads a checkpoint file (progress monitoring): problem identity, progress and the record so far
+ * (*out_have = 0 before the first chunk finished). QUBO_ERR_CHECKPOINT if unreadable or corrupt;
+ * QUBO_ERR_ARG for a null pointer. */
+QUBO_API int qubo_checkpoint_read(const char* checkpoint_path, int* out_n, int* out_dtype, int* out_k_prefix,
+                                  uint64_t* out_q_hash, uint64_t* out_next_slice, uint64_t* out_total_slices,
+                                  int* out_have, double* out_min_energy, uint64_t* out_argmin_rank,
+                                  uint64_t* out_tie_count);
+
+/* 64-bit FNV-1a hash of `bytes` bytes (the problem identity stored in checkpoint files). */
+QUBO_API uint64_t qubo_fnv1a64(const void* data, size_t bytes);
 
 /* ---- low-energy spectrum ----
  * The k lowest energies (§I: the search sees every state, so it can return the low-energy
