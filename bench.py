@@ -275,6 +275,12 @@ def run_gb300(args):
     e2e_value = world * STATES / (e2e * 1e-3)
     achieved = STATES / (kern * 1e-3) / 1e12  # int32 adds (one per state) per second, in T/s
     peak = SMS * LANES_PER_CLK * MAX_SM_MHZ * 1e6 / 1e12
+    # the measured INT32-add roofline: the best int32 add throughput of the add microbenchmark
+    # (kind 0: the compiler's own split of the adds; kind 8: half of them forced onto the FMA
+    # pipe's multiply-add) times the SM count, at the clock the probe saw
+    probes = [q.probe_alu(kind, 20000) for kind in (0, 8)]
+    best_ops, probe_mhz = max(probes, key=lambda t: t[0])
+    r_int = best_ops / 1e12
     traffic, traffic_src = profiled_traffic()
 
     extra = {}
@@ -298,6 +304,10 @@ def run_gb300(args):
                          "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
                                        "add per state) x 2.07 GHz max SM clock",
                          "traffic_source": traffic_src,
+                         "measured_int32_add_peak": r_int,
+                         "frac_of_measured_int32_add": achieved / r_int,
+                         "measured_int32_add_basis": (f"qubo_probe_alu int32 add chains: {best_ops / (SMS * probe_mhz * 1e6):.1f} "
+                                                      f"lanes/clk/SM at {probe_mhz:.0f} MHz x {SMS} SMs"),
                          "frac_at_measured_clock": (achieved / (SMS * LANES_PER_CLK * clocks["sm_mhz"] * 1e-6)
                                                     if clocks.get("sm_mhz") else None)},
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": N * N * 4,

@@ -11,6 +11,7 @@ constexpr int kChains = 16;
 
 template <int KIND>
 __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int* out, unsigned long long* clk) {
+  const unsigned one = (unsigned)(seed > 0 ? 1 : 2);  // 1 at run time (seed is 1), unknown to the compiler
   int a[kChains];
   float f[kChains];
 #pragma unroll
@@ -34,6 +35,15 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
       if (KIND == 5) f[k] = fminf(f[k], f[(k + 1) % kChains]);
       if (KIND == 6) a[k] = (int)__vimin3_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 7) a[k] = (int)__viaddmin_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
+      if (KIND == 8) {
+        // int32 adds, half of them as multiply-adds by a run-time one, so that the ALU and the
+        // FMA pipe's integer multiply-add unit share them
+        if (k & 1) {
+          asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(a[k]) : "r"(x), "r"(one));
+        } else {
+          a[k] = a[k] + x;
+        }
+      }
     }
   }
   const unsigned long long c1 = clock64();
@@ -77,7 +87,8 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       case 4: return launch<4>(blocks, it, out, clk);
       case 5: return launch<5>(blocks, it, out, clk);
       case 6: return launch<6>(blocks, it, out, clk);
-      default: return launch<7>(blocks, it, out, clk);
+      case 7: return launch<7>(blocks, it, out, clk);
+      default: return launch<8>(blocks, it, out, clk);
     }
   };
   cudaEvent_t e0 = nullptr, e1 = nullptr;

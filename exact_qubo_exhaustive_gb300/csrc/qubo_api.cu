@@ -503,16 +503,18 @@ int qubo_solve_batched(int batch, int n, const void* Q, int dtype, double* out_m
     const size_t qbytes = per * 4 * (size_t)batch;
     if ((st = ensure(&g_buf.dq, &g_buf.dq_bytes, qbytes, false, "cudaMalloc(Q)"))) return st;
     const size_t rbytes = (size_t)batch * sizeof(qubo_result);
-    if ((st = ensure(&g_buf.ws, &g_buf.ws_bytes, rbytes, false, "cudaMalloc(results)"))) return st;
+    const size_t wsb = (batched_workspace_bytes(bp) + 255) & ~(size_t)255;  // then the results
+    if ((st = ensure(&g_buf.ws, &g_buf.ws_bytes, wsb + rbytes, false, "cudaMalloc(workspace)"))) return st;
     if ((st = ensure(&g_buf.hres, &g_buf.hres_bytes, rbytes, true, "cudaMallocHost(results)"))) return st;
     cudaStream_t s = g_buf.stream;
     cudaError_t e = cudaMemcpyAsync(g_buf.dq, Q, qbytes, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return set_cuda_error(e, "cudaMemcpyAsync(Q)");
     int nl = 0;
-    e = run_batched(bp, g_buf.dq, nullptr, static_cast<qubo_result*>(g_buf.ws), s, &nl);
+    qubo_result* d_res = reinterpret_cast<qubo_result*>(static_cast<unsigned char*>(g_buf.ws) + wsb);
+    e = run_batched(bp, g_buf.dq, g_buf.ws, d_res, s, &nl);
     g_last_launches = nl;
     if (e != cudaSuccess) return set_cuda_error(e, "batched launch");
-    e = cudaMemcpyAsync(g_buf.hres, g_buf.ws, rbytes, cudaMemcpyDeviceToHost, s);
+    e = cudaMemcpyAsync(g_buf.hres, d_res, rbytes, cudaMemcpyDeviceToHost, s);
     if (e != cudaSuccess) return set_cuda_error(e, "cudaMemcpyAsync(results)");
     if ((e = cudaStreamSynchronize(s)) != cudaSuccess) return set_cuda_error(e, "cudaStreamSynchronize");
     const qubo_result* r = static_cast<const qubo_result*>(g_buf.hres);
@@ -685,7 +687,7 @@ void qubo_request_abort(void) { g_abort = 1; }
 void qubo_clear_abort(void) { g_abort = 0; }
 
 int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz) {
-  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 7) return QUBO_ERR_ARG;
+  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 8) return QUBO_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   int dev, st;
   if ((st = current_device(&dev))) return st;

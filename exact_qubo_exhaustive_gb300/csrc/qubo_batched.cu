@@ -4,8 +4,11 @@
 // register walker as the single-problem kernel, records per-(warp, segment) minima, and then
 // re-walks only the segments whose minimum equals the instance minimum to find the lowest
 // rank and the tie count.
+#include <algorithm>
 #include <cstring>
+#include <type_traits>
 
+#include "qubo_packed_walk.cuh"
 #include "qubo_walk.cuh"
 
 namespace qgb {
@@ -136,7 +139,7 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
   }
   __syncthreads();
 
-  WalkCtx c;
+  WalkCtx c{};
   c.n = n;
   c.C = C;
   c.F = 0;
@@ -213,10 +216,458 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
     out[blockIdx.x] = r;
   }
 }
+
+// ------------------------------------------------------------------------------------------------
+// Table-based pipeline (18 <= n <= kBatchTabMaxN). Every instance gets the energy-component cache
+// of the single-problem search in the workspace (M_int rows, E(U_B), the Gray-ordered walked
+// energies), built for all instances by one grid-stride kernel. Each instance is split into 2^F
+// work units (§III-C1), and persistent minimum passes walk the units of every instance with the
+// same walkers as the single-problem kernels: the packed 16x2 pass, the biased fp32-binade pass
+// or the int32 pass, chosen per instance by its sum |U| (a pass skips the units of instances it
+// does not own). A last pass re-walks only the units that reach their instance's minimum, for the
+// lowest rank and the tie count.
+// ------------------------------------------------------------------------------------------------
+constexpr int kBatchTabMaxN = 32;
+constexpr int kBatchTabC = 12;
+
+struct BatchTables {
+  int batch, n, C, F, w;
+  const int32_t* Q;
+  int32_t* U;  // batch x n*n        folded triangle
+  int32_t* M;  // batch x (n-C)*2^C  interaction rows
+  int32_t* Ec; // batch x 2^C        cached self energies
+  int32_t* T;  // batch x 2^w        walked energies in Gray order
+  uint32_t* T2;  // batch x 2^w      T's low 16 bits in both halves (packed pass)
+  int64_t* S;    // batch            sum |U|
+  int32_t* status;
+  int32_t* unit_min;  // batch x 2^F
+  int32_t* gmin;
+  unsigned long long* grank;
+  unsigned long long* gties;
+  size_t su, sm, se, st;  // per-instance strides of U, M, Ec, T / T2
+};
+
+enum BatchClass : int { kBatchPacked = 0, kBatchBiased = 1, kBatchInt = 2 };
+
+__device__ __forceinline__ int batch_class(int64_t S) {
+  if (S <= kPackedMaxAbsSum) return kBatchPacked;
+  if (S <= kBiasedWalkMaxAbsSum) return kBatchBiased;
+  return kBatchInt;
+}
+
+__global__ void __launch_bounds__(256) bprep_kernel(BatchTables b) {
+  __shared__ unsigned long long s_sum;
+  const int g = blockIdx.x, n = b.n;
+  const int32_t* Q = b.Q + (size_t)g * n * n;
+  int32_t* U = b.U + (size_t)g * b.su;
+  if (threadIdx.x == 0) s_sum = 0;
+  __syncthreads();
+  unsigned long long local = 0;
+  for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
+    long long u;
+    fold_entry(Q, n, idx / n, idx % n, &u);
+    local += (unsigned long long)(u < 0 ? -u : u);
+    U[idx] = (int32_t)u;  // only used when the range check passes
+  }
+  atomicAdd(&s_sum, local);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    b.S[g] = (int64_t)s_sum;
+    b.status[g] = s_sum > (unsigned long long)kMaxAbsSum ? QUBO_ERR_RANGE : QUBO_OK;
+    b.gmin[g] = kIntInf;
+    b.grank[g] = ~0ull;
+    b.gties[g] = 0;
+  }
+}
+
+// The caches of every instance (the single-problem tables, §II-C Table I), one block per instance.
+// The C cached bits split into a low half (lo bits) and a high half; with the partial sums of the
+// halves in shared memory every table entry is a few adds:
+//   M[v][j] = A_v[j_lo] + B_v[j_hi]                         (A, B: subset sums of U[v][cached])
+//   E(U_B)[j] = El[j_lo] + Eh[j_hi] + sum_{b in j_lo} Y[j_hi][b]   (Y: coupling of a high subset
+//                                                                   to low bit b)
+constexpr int kBatchMaxHalf = 64;  // 2^(C/2) for C = kBatchTabC
+
+__global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
+  __shared__ int sU[kBatchTabMaxN * kBatchTabMaxN];
+  __shared__ int sA[kBatchTabMaxN][kBatchMaxHalf];
+  __shared__ int sB[kBatchTabMaxN][kBatchMaxHalf];
+  __shared__ int sEl[kBatchMaxHalf], sEh[kBatchMaxHalf];
+  __shared__ int sY[kBatchMaxHalf][kBatchTabC / 2];
+  const int g = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
+  if (b.status[g] != QUBO_OK) return;
+  const int n = b.n, C = b.C, w = b.w;
+  const int lo = C / 2, hi = C - lo;
+  const int nlo = 1 << lo, nhi = 1 << hi;
+  const int32_t* U = b.U + (size_t)g * b.su;
+  for (int i = tid; i < n * n; i += nt) sU[i] = U[i];
+  __syncthreads();
+  const int nv = n - C;
+  // cached bit k (0 = fastest) is variable n - 1 - k; low half k < lo, high half k >= lo
+  for (int idx = tid; idx < nv * (nlo + nhi); idx += nt) {
+    const int v = idx / (nlo + nhi), r = idx - v * (nlo + nhi);
+    int acc = 0;
+    if (r < nlo) {
+      for (int k = 0; k < lo; ++k)
+        if ((r >> k) & 1) acc += sU[v * n + (n - 1 - k)];
+      sA[v][r] = acc;
+    } else {
+      const int h = r - nlo;
+      for (int k = 0; k < hi; ++k)
+        if ((h >> k) & 1) acc += sU[v * n + (n - 1 - (lo + k))];
+      sB[v][h] = acc;
+    }
+  }
+  for (int idx = tid; idx < nlo + nhi + nhi * lo; idx += nt) {
+    if (idx < nlo) {  // energy of a low subset alone
+      int acc = 0;
+      for (int k1 = 0; k1 < lo; ++k1) {
+        if (!((idx >> k1) & 1)) continue;
+        const int a = n - 1 - k1;
+        for (int k2 = k1; k2 < lo; ++k2)
+          if ((idx >> k2) & 1) acc += sU[(n - 1 - k2) * n + a];  // n-1-k2 <= a
+      }
+      sEl[idx] = acc;
+    } else if (idx < nlo + nhi) {  // energy of a high subset alone
+      const int h = idx - nlo;
+      int acc = 0;
+      for (int k1 = 0; k1 < hi; ++k1) {
+        if (!((h >> k1) & 1)) continue;
+        const int a = n - 1 - (lo + k1);
+        for (int k2 = k1; k2 < hi; ++k2)
+          if ((h >> k2) & 1) acc += sU[(n - 1 - (lo + k2)) * n + a];
+      }
+      sEh[h] = acc;
+    } else {  // coupling of high subset h to low bit k: sum_{k' in h} U[var(lo + k')][var(k)]
+      const int r = idx - nlo - nhi, h = r / lo, k = r - h * lo;
+      int acc = 0;
+      for (int k2 = 0; k2 < hi; ++k2)
+        if ((h >> k2) & 1) acc += sU[(n - 1 - (lo + k2)) * n + (n - 1 - k)];
+      sY[h][k] = acc;
+    }
+  }
+  __syncthreads();
+  const int ncols = 1 << C;
+  int32_t* M = b.M + (size_t)g * b.sm;
+  for (int idx = tid; idx < nv * ncols; idx += nt) {
+    const int v = idx >> C, j = idx & (ncols - 1);
+    M[idx] = sA[v][j & (nlo - 1)] + sB[v][j >> lo];
+  }
+  int32_t* Ec = b.Ec + (size_t)g * b.se;
+  for (int j = tid; j < ncols; j += nt) {
+    const int l = j & (nlo - 1), h = j >> lo;
+    int acc = sEl[l] + sEh[h];
+    for (int k = 0; k < lo; ++k)
+      if ((l >> k) & 1) acc += sY[h][k];
+    Ec[j] = acc;
+  }
+  int32_t* T = b.T + (size_t)g * b.st;
+  uint32_t* T2 = b.T2 + (size_t)g * b.st;
+  for (int i = tid; i < (1 << w); i += nt) {
+    const unsigned gc = (unsigned)(i ^ (i >> 1));
+    int acc = 0;
+    for (int a = 0; a < w; ++a) {
+      if (!((gc >> a) & 1u)) continue;
+      const int va = n - C - 1 - a;
+      for (int c2 = a; c2 < w; ++c2)
+        if ((gc >> c2) & 1u) acc += sU[(n - C - 1 - c2) * n + va];
+    }
+    T[i] = acc;
+    T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
+  }
+}
+
+// Per-unit linear terms of instance g (F fixed bits), as unit_linear_terms of the main kernel.
+__device__ __forceinline__ void bunit_terms(const int32_t* __restrict__ U, int n, int F, uint64_t P, int* sL) {
+  for (int v = threadIdx.x; v < n; v += blockDim.x) {
+    int acc = 0;
+    if (v >= F) {
+      for (int f = 0; f < F; ++f)
+        if ((P >> (F - 1 - f)) & 1u) acc += U[f * n + v];
+    } else if ((P >> (F - 1 - v)) & 1u) {
+      for (int f2 = v; f2 < F; ++f2)
+        if ((P >> (F - 1 - f2)) & 1u) acc += U[v * n + f2];
+    }
+    sL[v] = acc;
+  }
+}
+
+// Minimum passes of the 16-column layout: VT = float (biased binade) or int; MODE kModeMin, or
+// kModeTiesInt for the re-walk of the units at their instance's minimum.
+template <int R, typename VT, int MODE>
+__global__ void __launch_bounds__(256, 1) bwalk_kernel(BatchTables b) {
+  extern __shared__ __align__(16) int4 s_rows4[];
+  __shared__ int sL[64];
+  __shared__ int s_red[32];
+  constexpr int kClass = std::is_same<VT, float>::value ? kBatchBiased : kBatchInt;
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int n = b.n, C = b.C, F = b.F, w = b.w;
+  const int nq = (1 << C) >> 2;
+  const int ndyn = w - R;
+  const uint64_t units = (uint64_t)b.batch << F;
+  const int64_t niter = walk_iterations<R>(w);
+  const int lane = tid & 31, warp = tid >> 5;
+  int staged = -1;
+  WalkCtx c{};
+  c.n = n;
+  c.C = C;
+  c.F = F;
+  c.w = w;
+  c.nthreads = nthreads;
+  c.thread = tid;
+  c.sL = sL;
+  c.rows4 = s_rows4;
+  c.rows1 = nullptr;
+  c.t_global = true;
+  // a contiguous range of units per block, so that a block stages each instance's rows once
+  const uint64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
+  for (uint64_t u = u_begin; u < u_end; ++u) {
+    const int g = (int)(u >> F);
+    const uint64_t P = u & (((uint64_t)1 << F) - 1);
+    if (b.status[g] != QUBO_OK) continue;
+    if constexpr (MODE == kModeMin) {
+      if (batch_class(b.S[g]) != kClass) continue;
+    } else {
+      if (batch_class(b.S[g]) == kBatchPacked || b.unit_min[u] != b.gmin[g]) continue;  // packed: own re-walk
+    }
+    __syncthreads();  // the previous unit is done with sL and the staged rows
+    if (g != staged) {
+      const int4* M4 = reinterpret_cast<const int4*>(b.M + (size_t)g * b.sm);
+#pragma unroll 4
+      for (int idx = tid; idx < ndyn * nq; idx += nthreads) {
+        const int rr = idx / nq, q = idx - rr * nq;
+        const int v = n - C - 1 - (R + rr);
+        const int4 m = M4[(size_t)v * nq + q];
+        if constexpr (kClass == kBatchBiased)
+          reinterpret_cast<float4*>(s_rows4)[idx] = make_float4((float)m.x, (float)m.y, (float)m.z, (float)m.w);
+        else
+          s_rows4[idx] = m;
+      }
+      staged = g;
+    }
+    const int32_t* U = b.U + (size_t)g * b.su;
+    bunit_terms(U, n, F, P, sL);
+    __syncthreads();
+    int cP = 0;
+    for (int f = 0; f < F; ++f) cP += sL[f];
+    c.T = b.T + (size_t)g * b.st;
+    const int32_t* Ec = b.Ec + (size_t)g * b.se;
+    const int32_t* M = b.M + (size_t)g * b.sm;
+    Walker<kFastCPT, R, MODE, VT> W;
+    W.init(c, Ec, M, cP);
+    if constexpr (MODE == kModeMin) {
+      W.aux = kIntInf;
+      W.walk(c, 0, niter, niter, 0, nullptr, 0);
+      int best = W.aux - VOps<VT>::kBiasBits + W.s;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+      if (lane == 0) s_red[warp] = best;
+      __syncthreads();
+      if (tid == 0) {
+        int m = s_red[0];
+        for (int k = 1; k < (nthreads >> 5); ++k) m = min(m, s_red[k]);
+        b.unit_min[u] = m;
+      }
+    } else {
+      W.aux = b.gmin[g] - W.s;
+      const uint64_t prank = (F > 0) ? (P << (n - F)) : 0;
+      W.walk(c, 0, niter, niter, prank, nullptr, 0);
+      uint64_t cnt = W.cnt, rmin = W.rmin;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        const uint64_t r2 = __shfl_xor_sync(0xffffffffu, rmin, off);
+        rmin = r2 < rmin ? r2 : rmin;
+      }
+      if (lane == 0 && cnt) {
+        atomicAdd(&b.gties[g], (unsigned long long)cnt);
+        atomicMin(&b.grank[g], (unsigned long long)rmin);
+      }
+    }
+  }
+}
+
+// Packed 16x2 passes over the units of the instances with sum |U| <= kPackedMaxAbsSum: the
+// minimum (kModeMin) or the re-walk of the units at the instance minimum (kModeTiesInt).
+template <int MODE>
+__global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
+  extern __shared__ __align__(16) int4 s_rows4[];
+  __shared__ int sL[64];
+  __shared__ int s_red[32];
+  __shared__ __align__(16) uint32_t s_scan[MODE == kModeTiesInt ? 128 * 16 : 4];
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int n = b.n, C = b.C, F = b.F, w = b.w;
+  const int ncols = 1 << C, nwords = ncols >> 1;
+  const int ndyn = w - kPackedR;
+  const uint64_t units = (uint64_t)b.batch << F;
+  const int64_t niter = walk_iterations<kPackedR>(w);
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* s_words = reinterpret_cast<uint32_t*>(s_rows4);
+  int staged = -1;
+  WalkCtx c{};
+  c.n = n;
+  c.C = C;
+  c.F = F;
+  c.w = w;
+  c.nthreads = nthreads;
+  c.thread = tid;
+  c.sL = sL;
+  c.rows4 = s_rows4;
+  c.rows1 = nullptr;
+  c.t_global = true;
+  c.scratch = s_scan;
+  // a contiguous range of units per block, so that a block stages each instance's rows once
+  const uint64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
+  for (uint64_t u = u_begin; u < u_end; ++u) {
+    const int g = (int)(u >> F);
+    const uint64_t P = u & (((uint64_t)1 << F) - 1);
+    if (b.status[g] != QUBO_OK || batch_class(b.S[g]) != kBatchPacked) continue;
+    if (MODE == kModeTiesInt && b.unit_min[u] != b.gmin[g]) continue;
+    __syncthreads();
+    if (g != staged) {
+      const int32_t* M = b.M + (size_t)g * b.sm;
+      const int nq4 = nwords >> 1;  // two words per 16-byte load
+#pragma unroll 4
+      for (int idx = tid; idx < ndyn * nq4; idx += nthreads) {
+        const int rr = idx / nq4, q = idx - rr * nq4;
+        const int v = n - C - 1 - (kPackedR + rr);
+        const int4 m = reinterpret_cast<const int4*>(M + (size_t)v * ncols)[q];
+        reinterpret_cast<uint2*>(s_words)[idx] = make_uint2(packed::combine(m.x, m.y), packed::combine(m.z, m.w));
+      }
+      staged = g;
+    }
+    bunit_terms(b.U + (size_t)g * b.su, n, F, P, sL);
+    __syncthreads();
+    int cP = 0;
+    for (int f = 0; f < F; ++f) cP += sL[f];
+    c.T = reinterpret_cast<const int*>(b.T2 + (size_t)g * b.st);
+    packed::PackedWalker<kPackedR, MODE> W;
+    W.init(c, b.Ec + (size_t)g * b.se, b.M + (size_t)g * b.sm, cP);
+    if constexpr (MODE == kModeMin) {
+      int best = W.walk(c, niter);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+      if (lane == 0) s_red[warp] = best;
+      __syncthreads();
+      if (tid == 0) {
+        int m = s_red[0];
+        for (int k = 1; k < (nthreads >> 5); ++k) m = min(m, s_red[k]);
+        b.unit_min[u] = m;
+      }
+    } else {
+      W.aux = ((uint32_t)((int)packed::kHalfBias + b.gmin[g] - W.s) & 0xffffu) * 0x10001u;
+      W.walk(c, niter, (F > 0) ? (P << (n - F)) : 0);
+      uint64_t cnt = W.cnt, rmin = W.rmin;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        const uint64_t r2 = __shfl_xor_sync(0xffffffffu, rmin, off);
+        rmin = r2 < rmin ? r2 : rmin;
+      }
+      if (lane == 0 && cnt) {
+        atomicAdd(&b.gties[g], (unsigned long long)cnt);
+        atomicMin(&b.grank[g], (unsigned long long)rmin);
+      }
+    }
+  }
+}
+
+// Instance minima over their units.
+__global__ void bgroup_kernel(BatchTables b) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= b.batch || b.status[g] != QUBO_OK) return;
+  int m = kIntInf;
+  for (uint64_t k = 0; k < ((uint64_t)1 << b.F); ++k) m = min(m, b.unit_min[((uint64_t)g << b.F) + k]);
+  b.gmin[g] = m;
+}
+
+__global__ void bfinal_kernel(BatchTables b, qubo_result* out) {
+  const int g = blockIdx.x * blockDim.x + threadIdx.x;
+  if (g >= b.batch) return;
+  qubo_result r;
+  r.status = b.status[g];
+  r.reserved = 0;
+  r.min_energy = r.status == QUBO_OK ? (double)b.gmin[g] : 0.0;
+  r.argmin_rank = r.status == QUBO_OK ? b.grank[g] : 0;
+  r.tie_count = r.status == QUBO_OK ? b.gties[g] : 0;
+  out[g] = r;
+}
+
+size_t al256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// Workspace of the table-based pipeline; base may be null (sizes only).
+BatchTables batch_tables(const BatchPlan& bp, unsigned char* base, size_t* bytes) {
+  BatchTables t;
+  std::memset(&t, 0, sizeof(t));
+  t.batch = bp.batch;
+  t.n = bp.n;
+  t.C = bp.C;
+  t.F = bp.F;
+  t.w = bp.w;
+  t.su = (size_t)bp.n * bp.n;
+  t.sm = (size_t)(bp.n - bp.C) << bp.C;
+  t.se = (size_t)1 << bp.C;
+  t.st = (size_t)1 << bp.w;
+  size_t off = 0;
+  auto take = [&](size_t nbytes) {
+    unsigned char* p = base ? base + off : nullptr;
+    off += al256(nbytes);
+    return p;
+  };
+  const size_t B = (size_t)bp.batch;
+  t.U = reinterpret_cast<int32_t*>(take(B * t.su * 4));
+  t.M = reinterpret_cast<int32_t*>(take(B * t.sm * 4));
+  t.Ec = reinterpret_cast<int32_t*>(take(B * t.se * 4));
+  t.T = reinterpret_cast<int32_t*>(take(B * t.st * 4));
+  t.T2 = reinterpret_cast<uint32_t*>(take(B * t.st * 4));
+  t.S = reinterpret_cast<int64_t*>(take(B * 8));
+  t.status = reinterpret_cast<int32_t*>(take(B * 4));
+  t.unit_min = reinterpret_cast<int32_t*>(take((B << bp.F) * 4));
+  t.gmin = reinterpret_cast<int32_t*>(take(B * 4));
+  t.grank = reinterpret_cast<unsigned long long*>(take(B * 8));
+  t.gties = reinterpret_cast<unsigned long long*>(take(B * 8));
+  if (bytes) *bytes = off;
+  return t;
+}
+
+template <typename K>
+cudaError_t set_smem(K k, size_t smem) {
+  return cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+}
+
 }  // namespace
 
 bool plan_batched(int batch, int n, BatchPlan* bp) {
-  if (batch < 1 || n < 14 || n > kBatchMaxN) return false;
+  if (batch < 1 || n < 14) return false;
+  const DevInfo& di = device_info();
+  if (n >= 18 && n <= kBatchTabMaxN) {
+    BatchPlan p;
+    p.batch = batch;
+    p.n = n;
+    p.C = kBatchTabC;
+    p.F = n - p.C - 9 > 0 ? n - p.C - 9 : 0;  // units of 2^(n - F) states, 9 walked bits at most
+    p.w = n - p.C - p.F;
+    p.threads = (1 << p.C) / kFastCPT;
+    p.tabled = true;
+    p.smem_int = (size_t)(p.w - kFastR) << (p.C + 2);
+    p.smem_biased = (size_t)(p.w - kBiasedR) << (p.C + 2);
+    p.smem_packed = (size_t)(p.w - kPackedR) << (p.C + 1);
+    if (p.w < kPackedR + 1 || p.smem_int + 4096 > di.smem_optin) return false;
+    int occ = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bwalk_kernel<kFastR, int, kModeMin>, p.threads,
+                                                      p.smem_int) != cudaSuccess || occ < 1)
+      occ = 1;
+    p.blocks = std::max(1, di.sms) * occ;
+    if (set_smem(bpacked_kernel<kModeMin>, p.smem_packed) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bpacked_kernel<kModeMin>, (1 << p.C) / 32,
+                                                      p.smem_packed) != cudaSuccess ||
+        occ < 1)
+      occ = 1;
+    p.packed_blocks = std::max(1, di.sms) * occ;
+    *bp = p;
+    return true;
+  }
+  if (n > kBatchMaxN) return false;
   // cache bits: 2^C columns = threads * 16; walked w = n - C needs w >= R + 1 + log2(segments)
   int C = n >= 24 ? 11 : n - (kFastR + 1 + 5);
   if (C > 12) C = 12;
@@ -229,20 +680,60 @@ bool plan_batched(int batch, int n, BatchPlan* bp) {
   bp->w = w;
   bp->threads = (1 << C) / kFastCPT;
   bp->smem_bytes = ((size_t)(w - kFastR) << (C + 2)) + ((size_t)1 << (w + 2)) + (size_t)n * n * 4;
-  const DevInfo& di = device_info();
+  bp->tabled = false;
   if (bp->smem_bytes + 4096 > di.smem_optin) return false;
   return true;
 }
 
-size_t batched_workspace_bytes(const BatchPlan& bp) { return 256; }
+size_t batched_workspace_bytes(const BatchPlan& bp) {
+  if (!bp.tabled) return 256;
+  size_t bytes = 0;
+  batch_tables(bp, nullptr, &bytes);
+  return bytes;
+}
 
 cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_result* res, cudaStream_t stream,
                         int* launches) {
-  (void)d_ws;
-  cudaError_t e = cudaFuncSetAttribute(batched_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bp.smem_bytes);
-  if (e != cudaSuccess) return e;
-  batched_kernel<<<bp.batch, bp.threads, bp.smem_bytes, stream>>>(bp.n, bp.C, static_cast<const int32_t*>(d_Q), res);
-  if (launches) *launches = 1;
+  cudaError_t e;
+  if (!bp.tabled) {
+    (void)d_ws;
+    if ((e = set_smem(batched_kernel, bp.smem_bytes)) != cudaSuccess) return e;
+    batched_kernel<<<bp.batch, bp.threads, bp.smem_bytes, stream>>>(bp.n, bp.C, static_cast<const int32_t*>(d_Q),
+                                                                       res);
+    if (launches) *launches = 1;
+    return cudaGetLastError();
+  }
+  BatchTables t = batch_tables(bp, static_cast<unsigned char*>(d_ws), nullptr);
+  t.Q = static_cast<const int32_t*>(d_Q);
+  int nl = 0;
+  bprep_kernel<<<bp.batch, 256, 0, stream>>>(t);
+  ++nl;
+  btables_kernel<<<bp.batch, 256, 0, stream>>>(t);
+  ++nl;
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = set_smem(bpacked_kernel<kModeMin>, bp.smem_packed)) != cudaSuccess) return e;
+  bpacked_kernel<kModeMin><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
+  ++nl;
+  auto kb = bwalk_kernel<kBiasedR, float, kModeMin>;
+  if ((e = set_smem(kb, bp.smem_biased)) != cudaSuccess) return e;
+  kb<<<bp.blocks, bp.threads, bp.smem_biased, stream>>>(t);
+  ++nl;
+  auto ki = bwalk_kernel<kFastR, int, kModeMin>;
+  if ((e = set_smem(ki, bp.smem_int)) != cudaSuccess) return e;
+  ki<<<bp.blocks, bp.threads, bp.smem_int, stream>>>(t);
+  ++nl;
+  bgroup_kernel<<<(bp.batch + 127) / 128, 128, 0, stream>>>(t);
+  ++nl;
+  if ((e = set_smem(bpacked_kernel<kModeTiesInt>, bp.smem_packed)) != cudaSuccess) return e;
+  bpacked_kernel<kModeTiesInt><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
+  ++nl;
+  auto kr = bwalk_kernel<kFastR, int, kModeTiesInt>;
+  if ((e = set_smem(kr, bp.smem_int)) != cudaSuccess) return e;
+  kr<<<bp.blocks, bp.threads, bp.smem_int, stream>>>(t);
+  ++nl;
+  bfinal_kernel<<<(bp.batch + 127) / 128, 128, 0, stream>>>(t, res);
+  ++nl;
+  if (launches) *launches = nl;
   return cudaGetLastError();
 }
 

@@ -126,6 +126,14 @@ cudaError_t run_search(const Plan& p, const void* d_Q, const Work& w, qubo_resul
 struct BatchPlan {
   int batch = 0, n = 0, C = 0, w = 0, threads = 0;
   size_t smem_bytes = 0;
+  // table-based pipeline (tabled = true): per-instance caches in the workspace, work units of
+  // 2^(n - F) states shared by persistent minimum passes (packed / biased / int32), re-walk of
+  // the units at each instance's minimum
+  bool tabled = false;
+  int F = 0;
+  int blocks = 0;          // persistent grid of the 256-thread passes
+  int packed_blocks = 0;   // persistent grid of the 128-thread packed pass
+  size_t smem_int = 0, smem_biased = 0, smem_packed = 0;
 };
 bool plan_batched(int batch, int n, BatchPlan* bp);
 size_t batched_workspace_bytes(const BatchPlan& bp);

@@ -121,7 +121,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
     }
   }
 
-  WalkCtx c;
+  WalkCtx c{};
   c.n = n;
   c.C = C;
   c.F = F;

@@ -159,6 +159,7 @@ struct WalkCtx {
   KeyCand* cand;              // kModeCollectKey: candidate buffer of cand_cap entries
   unsigned long long* cand_count;
   uint32_t cand_cap;
+  uint32_t* scratch;          // packed ties scan: 16 words per thread (shared memory)
 };
 
 // Column of (thread t, slot jj). Fast layout: quads of 4 consecutive columns, quad k of thread t

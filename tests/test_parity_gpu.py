@@ -383,6 +383,54 @@ def test_batched_ties_and_other_sizes(q):
         assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all()
 
 
+def test_batched_mixed_passes_against_oracle(q):
+    # one batch whose instances take the packed, biased and int32 minimum passes, plus all-ties
+    # and many-ties instances
+    n = 24
+    Qs = np.stack([qi.random_upper_int(n, -20, 20, 510), qi.random_upper_int(n, -1000, 1000, 511),
+                   qi.random_upper_int(n, -(1 << 20), 1 << 20, 512), np.zeros((n, n), np.int32),
+                   qi.random_upper_int(n, -1, 1, 513), qi.random_upper_int(n, -30, 30, 514),
+                   qi.random_upper_int(n, -5000, 5000, 515)])
+    sums = np.abs(Qs.astype(np.int64)).sum(axis=(1, 2))
+    assert sums[0] <= (1 << 14) - 1 < sums[1] <= (1 << 22) - 1 < sums[2]
+    e, x, t = q.solve_batched(Qs)
+    for b in range(Qs.shape[0]):
+        want = O.solve(Qs[b])
+        assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), b
+
+
+@pytest.mark.parametrize("n,batch", [(18, 40), (21, 12), (28, 2)])
+def test_batched_sizes_and_unit_splits(q, n, batch):
+    # n = 18, 21: one unit per instance; n = 28: 2^7 units per instance
+    Qs = qi.batched_upper_int(batch, n, -60, 60, 520 + n)
+    e, x, t = q.solve_batched(Qs)
+    for b in range(batch):
+        want = O.solve(Qs[b])
+        assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all()
+
+
+def test_batched_device_reports_per_instance_status(q):
+    import torch
+    n, batch = 20, 3
+    Qs = qi.batched_upper_int(batch, n, -50, 50, 530)
+    Qs[1, 0, 0] = (1 << 30)  # beyond the int32 range: only this instance fails
+    dq = torch.from_numpy(Qs).cuda()
+    nb = q.batched_workspace_bytes(batch, n)
+    ws = torch.empty(max(nb, 256), dtype=torch.uint8, device="cuda")
+    res = torch.zeros(batch * 32, dtype=torch.uint8, device="cuda")
+    q.solve_batched_device(batch, n, dq, ws, nb, torch.cuda.current_stream().cuda_stream, res)
+    torch.cuda.synchronize()
+    r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)
+    assert list(r["status"]) == [0, -2, 0]
+    for b in (0, 2):
+        want = O.solve(Qs[b])
+        assert (int(r["min_energy"][b]), int(r["tie_count"][b]), int(r["argmin_rank"][b])) == \
+            (want[0], want[2], oracle.rank_of_bits(want[1]))
+    with pytest.raises(q.QuboError) as ei:
+        q.solve_batched(Qs)
+    assert ei.value.status == -2
+
+
 # ---------------------------------------------------------------- device-resident entry point
 
 def test_device_entry_point(q):
