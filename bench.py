@@ -387,6 +387,24 @@ def other_configs(q, torch, dev, stream):
     return out
 
 
+def profile_batched(batch: int):
+    """Two batched searches of the 4096 x n=24 workload's shape (first `batch` instances), for ncu."""
+    import torch
+    import exact_qubo_exhaustive_gb300 as q
+    Qs = qi.workload_batched()[:batch]
+    dq = torch.from_numpy(np.ascontiguousarray(Qs)).cuda()
+    nb = max(q.batched_workspace_bytes(batch, 24), 256)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    res = torch.zeros(batch * 32, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    for _ in range(2):
+        q.solve_batched_device(batch, 24, dq, ws, nb, s.cuda_stream, res)
+    torch.cuda.synchronize()
+    r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)
+    log(f"profile batched {batch} x n=24: statuses ok={int((r['status'] == 0).sum())} E0={r['min_energy'][0]}")
+    return 0 if (r["status"] == 0).all() else 1
+
+
 def profile_case(n: int, dtype_name: str):
     """Two searches of an n-variable instance shaped like the workload (for ncu captures)."""
     import torch
@@ -422,9 +440,13 @@ def main(argv=None):
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="only run two searches of an N-variable instance (for ncu), print no JSON")
     ap.add_argument("--profile-dtype", choices=["int32", "fp32", "int32_narrow"], default="int32")
+    ap.add_argument("--profile-batched", type=int, default=0, metavar="B",
+                    help="run two batched searches of the first B instances of the batched workload (for ncu)")
     args = ap.parse_args(argv)
     if args.profile_case:
         return profile_case(args.profile_case, args.profile_dtype)
+    if args.profile_batched:
+        return profile_batched(args.profile_batched)
     if args.warmup < 3:
         log("warmup raised to 3 (timing rule)")
         args.warmup = 3
