@@ -87,6 +87,9 @@ struct PackedWalker {
   static constexpr int kSteps = 1 << (R + 1);
   static constexpr int kMid = 1 << R;
   static constexpr int kAhead = kMid >= 16 ? 8 : (kMid >> 1);
+  static constexpr int kQuads = kSteps / 4;                 // walked-energy quads per iteration
+  static constexpr int kRing = kQuads < 4 ? kQuads : 4;     // quads held ahead; divides kQuads
+  static_assert(kQuads % kRing == 0, "the ring must divide an iteration's quads");
   uint32_t V[kPW];
   uint32_t Row[R][kPW];
   int s;          // c(P) + sum of L over set walked positions >= R
@@ -183,13 +186,13 @@ struct PackedWalker {
 
   template <int L>
   __device__ __forceinline__ void steps(const WalkCtx& c, uint64_t prank, uint64_t base, int64_t iter, int a_end,
-                                        uint4* tq, const uint4* tn, RowBuf& rb) {
+                                        uint4* tq, const uint4* tc, const uint4* tn, RowBuf& rb) {
     if constexpr (L < kSteps) {
       if constexpr (MODE == kModeMin) {
-        aux = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[L >> 2]), aux);
+        aux = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[(L >> 2) % kRing]), aux);
       } else {
         // per half m + T (no state lies below the target, so a hit is an equal half)
-        const uint32_t q = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[L >> 2]), 0xffffffffu);
+        const uint32_t q = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[(L >> 2) % kRing]), 0xffffffffu);
         const uint32_t t = aux & 0xffffu;
         const bool hit = (q & 0xffffu) <= t || (q >> 16) <= t;
         if (__any_sync(0xffffffffu, hit) && hit) {
@@ -198,12 +201,16 @@ struct PackedWalker {
 #pragma unroll
           for (int k = 0; k < kPW / 4; ++k) slot[k] = make_uint4(V[4 * k], V[4 * k + 1], V[4 * k + 2], V[4 * k + 3]);
           const TieScan r = scan_ties(slot, c.thread, c.nthreads, c.C, prank, base + L,
-                                      comp<L & 3>(tq[L >> 2]) & 0xffffu, t);
+                                      comp<L & 3>(tq[(L >> 2) % kRing]) & 0xffffu, t);
           cnt += r.cnt;
           rmin = r.rmin < rmin ? r.rmin : rmin;
         }
       }
-      if constexpr ((L & 3) == 3) tq[L >> 2] = __ldg(tn + (L >> 2));
+      if constexpr ((L & 3) == 3) {
+        constexpr int q = L >> 2;
+        if constexpr (q + kRing < kQuads) tq[q % kRing] = __ldg(tc + q + kRing);
+        else tq[q % kRing] = __ldg(tn + (q + kRing - kQuads));
+      }
       if constexpr (L == kMid - 1 - kAhead) load_dyn_row(c, R, rb);
       if constexpr (L == kSteps - 1 - kAhead) load_dyn_row(c, a_end, rb);
       if constexpr (L + 1 < kSteps) {
@@ -221,7 +228,7 @@ struct PackedWalker {
           }
         }
       }
-      steps<L + 1>(c, prank, base, iter, a_end, tq, tn, rb);
+      steps<L + 1>(c, prank, base, iter, a_end, tq, tc, tn, rb);
     }
   }
 
@@ -229,16 +236,17 @@ struct PackedWalker {
   // (kModeMin). prank: the unit's prefix bits in rank position (kModeTiesInt).
   __device__ __forceinline__ int walk(const WalkCtx& c, int64_t niter, uint64_t prank = 0) {
     const uint4* T4 = reinterpret_cast<const uint4*>(c.T);
-    uint4 tq[kSteps / 4];
+    uint4 tq[kRing];
 #pragma unroll
-    for (int q = 0; q < kSteps / 4; ++q) tq[q] = __ldg(T4 + q);
+    for (int q = 0; q < kRing; ++q) tq[q] = __ldg(T4 + q);
     RowBuf rb;
     for (int64_t iter = 0; iter < niter; ++iter) {
       const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
       const bool flip_end = iter + 1 < niter;
       const int a_end = flip_end ? R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1 : R;
+      const uint4* tc = T4 + (base >> 2);
       const uint4* tn = T4 + ((flip_end ? base + kSteps : base) >> 2);
-      steps<0>(c, prank, base, iter, a_end, tq, tn, rb);
+      steps<0>(c, prank, base, iter, a_end, tq, tc, tn, rb);
       if (flip_end) {
         const uint64_t ilast = base + kSteps - 1;
         apply_dyn_row(c, a_end, rb, ((gray_code(ilast) >> a_end) & 1u) == 0);

@@ -406,16 +406,29 @@ struct Walker {
     return c.t_global ? __ldg(p) : *p;
   }
 
+  // Walked energies are read in quads (int4) through a ring of kRing quads. When a quad has been
+  // consumed, the quad kRing positions ahead (in this iteration or the next) is loaded into its
+  // slot, so each load has kRing * 4 steps to arrive while few registers hold them. kRing
+  // divides the quads of an iteration, so slot q % kRing holds quad q in every iteration.
+  static constexpr int kQuads = kSteps >= 4 ? kSteps / 4 : 1;
+  static constexpr int kRing = kQuads < 4 ? kQuads : 4;  // divides kQuads
+  static_assert(kQuads % kRing == 0, "the ring must divide an iteration's quads");
+
   // Steps L.. of one iteration, unrolled by recursion so that every register row index, every
-  // flip sign and every prefetch point is a compile-time constant. `tq` holds this iteration's
-  // walked energies; `tn` points at the next iteration's (or at this one's, on the last).
+  // flip sign and every prefetch point is a compile-time constant. `tq` is the ring; `tc` points
+  // at this iteration's walked energies, `tn` at the next iteration's (or at this one's, on the
+  // last).
   template <int L>
   __device__ __forceinline__ void steps_fast(const WalkCtx& c, uint64_t prank, uint64_t base, int64_t iter,
-                                             int a_end, int4* tq, const int4* tn, RowBuf& rb,
+                                             int a_end, int4* tq, const int4* tc, const int4* tn, RowBuf& rb,
                                              const double* __restrict__ U64, uint64_t gkey) {
     if constexpr (L < kSteps) {
-      step(c, prank, base + L, comp<L & 3>(tq[L >> 2]), U64, gkey);
-      if constexpr ((L & 3) == 3) tq[L >> 2] = load_t4(c, tn + (L >> 2));
+      step(c, prank, base + L, comp<L & 3>(tq[(L >> 2) % kRing]), U64, gkey);
+      if constexpr ((L & 3) == 3) {
+        constexpr int q = L >> 2;
+        if constexpr (q + kRing < kQuads) tq[q % kRing] = load_t4(c, tc + q + kRing);
+        else tq[q % kRing] = load_t4(c, tn + (q + kRing - kQuads));
+      }
       if constexpr (L == kMid - 1 - kAhead) load_dyn_row(c, R, rb);
       if constexpr (L == kSteps - 1 - kAhead) load_dyn_row(c, a_end, rb);
       if constexpr (L + 1 < kSteps) {
@@ -435,7 +448,7 @@ struct Walker {
           }
         }
       }
-      steps_fast<L + 1>(c, prank, base, iter, a_end, tq, tn, rb, U64, gkey);
+      steps_fast<L + 1>(c, prank, base, iter, a_end, tq, tc, tn, rb, U64, gkey);
     }
   }
 
@@ -456,10 +469,10 @@ struct Walker {
                                        uint64_t prank, const double* __restrict__ U64, uint64_t gkey) {
     if constexpr (CPT >= 4 && kSteps >= 4) {
       const int4* T4 = reinterpret_cast<const int4*>(c.T);
-      int4 tq[kSteps / 4];
+      int4 tq[kRing];
       if (it0 < it1) {
 #pragma unroll
-        for (int q = 0; q < kSteps / 4; ++q) tq[q] = load_t4(c, T4 + (static_cast<uint64_t>(it0) << (R - 1)) + q);
+        for (int q = 0; q < kRing; ++q) tq[q] = load_t4(c, T4 + (static_cast<uint64_t>(it0) << (R - 1)) + q);
       }
       RowBuf rb;
       for (int64_t iter = it0; iter < it1; ++iter) {
@@ -467,8 +480,9 @@ struct Walker {
         const bool flip_end = iter + 1 < it_flip_end;
         // a_end is only read when flip_end; otherwise a valid row (R) is read and left unused
         const int a_end = flip_end ? R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1 : R;
+        const int4* tc = T4 + (base >> 2);
         const int4* tn = T4 + (((iter + 1 < it1) ? base + kSteps : base) >> 2);
-        steps_fast<0>(c, prank, base, iter, a_end, tq, tn, rb, U64, gkey);
+        steps_fast<0>(c, prank, base, iter, a_end, tq, tc, tn, rb, U64, gkey);
         if (flip_end) {
           const uint64_t ilast = base + kSteps - 1;
           apply_dyn_row(c, a_end, rb, ((gray_code(ilast) >> a_end) & 1u) == 0);
