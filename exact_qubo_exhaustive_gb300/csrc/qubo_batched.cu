@@ -718,7 +718,7 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   if ((e = set_smem(kb, bp.smem_biased)) != cudaSuccess) return e;
   kb<<<bp.blocks, bp.threads, bp.smem_biased, stream>>>(t);
   ++nl;
-  auto ki = bwalk_kernel<kFastR, int, kModeMin>;
+  auto ki = bwalk_kernel<kIntMinR, int, kModeMin>;
   if ((e = set_smem(ki, bp.smem_int)) != cudaSuccess) return e;
   ki<<<bp.blocks, bp.threads, bp.smem_int, stream>>>(t);
   ++nl;

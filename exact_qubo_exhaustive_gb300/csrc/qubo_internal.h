@@ -25,6 +25,7 @@ constexpr int kFastCPT = 16;
 constexpr int kFastR = 4;
 constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
 constexpr int kPackedR = 5;  // register rows of the packed 16x2 minimum pass
+constexpr int kIntMinR = 5;  // register rows of the int32 minimum pass (the resolve passes keep kFastR)
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 

@@ -367,7 +367,11 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
       ++nl;
     }
     // ... and the int32 CUDA-core pass (exits at once when another pass ran)
-    if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) return e;
+    if (p.variant == kFast && p.w >= kIntMinR + 1) {
+      if ((e = launch_search_int_min5(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
+    } else if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) {
+      return e;
+    }
     ++nl;
     if (kp.unit_end < p.total_units && abort_flag) {
       // long run: wait for this chunk so a cancellation request is honoured promptly

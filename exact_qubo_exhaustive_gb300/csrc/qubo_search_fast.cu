@@ -1,6 +1,6 @@
 // Register-cached enumeration kernel: 16 columns per thread, the lowest walked rows in
-// registers (4 for the int32 passes, 5 for the biased-binade minimum pass), the other walked
-// rows in shared memory.
+// registers (5 for the minimum passes, 4 for the resolution passes), the other walked rows in
+// shared memory.
 #include "qubo_search_kernel.cuh"
 
 namespace qgb {
@@ -28,6 +28,15 @@ cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threa
 
 cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
   auto k = search_kernel<kFastCPT, kBiasedR, kModeMin, true>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  k<<<blocks, threads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+// int32 minimum pass with five register rows (needs at least 2^6 walked steps per unit).
+cudaError_t launch_search_int_min5(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
+  auto k = search_kernel<kFastCPT, kIntMinR, kModeMin, false>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k<<<blocks, threads, smem, s>>>(p);
