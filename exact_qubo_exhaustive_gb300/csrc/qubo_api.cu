@@ -161,7 +161,7 @@ bool fast_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
   const int w = n - F - C;
   if (C < 9 || C > 12 || F < 0 || F > 31 || w < kFastR + 1 || w > kMaxWalkedBits) return false;
   const size_t sm = (size_t)(w - kFastR) << (C + 2);
-  if (sm + kStaticSmemReserve > smem_optin) return false;
+  if (sm + kStaticSmemReserve + kFastScanSlotBytes > smem_optin) return false;
   *smem = sm;
   return true;
 }

@@ -399,6 +399,7 @@ __global__ void __launch_bounds__(256, 1) bwalk_kernel(BatchTables b) {
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
   __shared__ int s_red[32];
+  __shared__ __align__(16) int s_slot[MODE != kModeMin ? kFastThreadsMax * kFastCPT : 4];
   constexpr int kClass = std::is_same<VT, float>::value ? kBatchBiased : kBatchInt;
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int n = b.n, C = b.C, F = b.F, w = b.w;
@@ -419,6 +420,7 @@ __global__ void __launch_bounds__(256, 1) bwalk_kernel(BatchTables b) {
   c.rows4 = s_rows4;
   c.rows1 = nullptr;
   c.t_global = true;
+  c.scratch = MODE != kModeMin ? reinterpret_cast<uint32_t*>(s_slot) : nullptr;
   // a contiguous range of units per block, so that a block stages each instance's rows once
   const uint64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
   for (uint64_t u = u_begin; u < u_end; ++u) {

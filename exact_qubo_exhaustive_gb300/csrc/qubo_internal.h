@@ -22,6 +22,9 @@ enum Variant : int {
   kFast = 1,     // 16 columns per thread, the lowest kFastR walked rows in registers
 };
 constexpr int kFastCPT = 16;
+constexpr int kFastThreadsMax = 256;  // 2^C / kFastCPT for C <= 12
+// static shared memory of the fast resolve passes: one scan slot of kFastCPT ints per thread
+constexpr size_t kFastScanSlotBytes = (size_t)kFastThreadsMax * kFastCPT * 4;
 constexpr int kFastR = 4;
 constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
 constexpr int kPackedR = 5;  // register rows of the packed 16x2 minimum pass

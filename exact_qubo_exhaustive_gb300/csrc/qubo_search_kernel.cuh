@@ -89,6 +89,8 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
   __shared__ int s_red[32];
+  // resolve modes: per-thread slots for the out-of-line candidate scan
+  __shared__ __align__(16) int s_slot[(MODE != kModeMin && CPT >= 4) ? kFastThreadsMax * CPT : 4];
   if (p.hdr->status != QUBO_OK) return;
   if constexpr (MODE == kModeMin) {
     if (min_pass_owner(p) != (BIASED ? kOwnerBiased : kOwnerInt)) return;  // another pass does it
@@ -138,6 +140,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   c.cand = p.cand;
   c.cand_count = p.cand_count;
   c.cand_cap = p.cand_cap;
+  c.scratch = (MODE != kModeMin && CPT >= 4) ? reinterpret_cast<uint32_t*>(s_slot) : nullptr;
 
   const int64_t niter = walk_iterations<R>(w);
   const int lane = tid & 31, warp = tid >> 5;

@@ -159,7 +159,7 @@ struct WalkCtx {
   KeyCand* cand;              // kModeCollectKey: candidate buffer of cand_cap entries
   unsigned long long* cand_count;
   uint32_t cand_cap;
-  uint32_t* scratch;          // packed ties scan: 16 words per thread (shared memory)
+  uint32_t* scratch;          // out-of-line candidate scans: 16 words per thread (shared memory), or null
 };
 
 // Column of (thread t, slot jj). Fast layout: quads of 4 consecutive columns, quad k of thread t
@@ -168,6 +168,58 @@ template <int CPT>
 __device__ __forceinline__ int column_of(int t, int nthreads, int jj) {
   if constexpr (CPT == 1) return t;
   else return ((((jj >> 2) * nthreads) + t) << 2) | (jj & 3);
+}
+
+// Result of a candidate scan (resolve modes).
+struct CandScan {
+  uint64_t cnt, rmin, kmin;
+};
+
+// Resolve-mode scan of one thread's CPT columns (fast layout) at Gray step i, out of line: the
+// running energies are read back from the thread's shared-memory slot. Candidates are the
+// columns with V + T <= aux (energy <= the mode's threshold); what is counted or kept per mode
+// is the same as in Walker::visit_candidates. Called only when a column of the step passes the
+// filter, so the unrolled walk stays small.
+template <int CPT, int MODE>
+static __device__ __noinline__ CandScan scan_candidates(const int* slot, int thread, int nthreads, int C, int n,
+                                                       uint64_t prank, uint64_t i, int tv, int aux, int s,
+                                                       const double* __restrict__ U64, uint64_t gkey, int theta,
+                                                       uint64_t rho, KeyCand* cand, unsigned long long* cand_count,
+                                                       uint32_t cand_cap) {
+  CandScan r = {0, ~0ull, ~0ull};
+  const uint64_t ib = prank | (gray_code(i) << C);
+  for (int jj = 0; jj < CPT; ++jj) {
+    const int v = slot[jj];
+    if (v + tv > aux) continue;
+    const int col = ((((jj >> 2) * nthreads) + thread) << 2) | (jj & 3);
+    const uint64_t rank = ib | static_cast<uint64_t>(col);
+    if constexpr (MODE == kModeTiesInt) {
+      ++r.cnt;
+      r.rmin = rank < r.rmin ? rank : r.rmin;
+    } else if constexpr (MODE == kModeKeyFp) {
+      const uint64_t k = order_key(eval64_rank(U64, n, rank));
+      r.kmin = k < r.kmin ? k : r.kmin;
+    } else if constexpr (MODE == kModeTiesFp) {
+      if (order_key(eval64_rank(U64, n, rank)) == gkey) {
+        ++r.cnt;
+        r.rmin = rank < r.rmin ? rank : r.rmin;
+      }
+    } else if constexpr (MODE == kModeCountKey || MODE == kModeCollectKey) {
+      const int E = v + tv + s;
+      if (E < theta || rank < rho) {
+        if constexpr (MODE == kModeCountKey) {
+          ++r.cnt;
+        } else {
+          const unsigned long long idx = atomicAdd(cand_count, 1ull);
+          if (idx < cand_cap) {
+            cand[idx].e = E;
+            cand[idx].rank = rank;
+          }
+        }
+      }
+    }
+  }
+  return r;
 }
 
 template <int CPT, int R, int MODE, typename VT = int>
@@ -345,7 +397,24 @@ struct Walker {
     } else {
       const bool hit = valid && (m + tv <= aux);
       if (__any_sync(0xffffffffu, hit)) {
-        if (hit) visit_candidates(c, prank, i, tv, U64, gkey);
+        if constexpr (CPT >= 4) {
+          if (hit && c.scratch != nullptr) {
+            // hand the columns to the out-of-line scan (keeps the unrolled walk small)
+            int4* slot = reinterpret_cast<int4*>(c.scratch) + (CPT / 4) * c.thread;
+#pragma unroll
+            for (int k = 0; k < CPT / 4; ++k) slot[k] = make_int4(V[4 * k], V[4 * k + 1], V[4 * k + 2], V[4 * k + 3]);
+            const CandScan r = scan_candidates<CPT, MODE>(reinterpret_cast<const int*>(slot), c.thread, c.nthreads,
+                                                           c.C, c.n, prank, i, tv, aux, s, U64, gkey, c.theta, c.rho,
+                                                           c.cand, c.cand_count, c.cand_cap);
+            cnt += r.cnt;
+            rmin = r.rmin < rmin ? r.rmin : rmin;
+            kmin = r.kmin < kmin ? r.kmin : kmin;
+          } else if (hit) {
+            visit_candidates(c, prank, i, tv, U64, gkey);
+          }
+        } else {
+          if (hit) visit_candidates(c, prank, i, tv, U64, gkey);
+        }
       }
     }
   }
