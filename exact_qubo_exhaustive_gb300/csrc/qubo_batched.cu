@@ -228,6 +228,7 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
 // lowest rank and the tie count.
 // ------------------------------------------------------------------------------------------------
 constexpr int kBatchTabMaxN = 32;
+constexpr int kPackedTiesR = 4;  // register rows of the packed re-walk of the minimum units
 constexpr int kBatchTabC = 12;
 
 struct BatchTables {
@@ -491,7 +492,7 @@ __global__ void __launch_bounds__(256, 1) bwalk_kernel(BatchTables b) {
 
 // Packed 16x2 passes over the units of the instances with sum |U| <= kPackedMaxAbsSum: the
 // minimum (kModeMin) or the re-walk of the units at the instance minimum (kModeTiesInt).
-template <int MODE>
+template <int R, int MODE>
 __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
@@ -500,9 +501,9 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int n = b.n, C = b.C, F = b.F, w = b.w;
   const int ncols = 1 << C, nwords = ncols >> 1;
-  const int ndyn = w - kPackedR;
+  const int ndyn = w - R;
   const uint64_t units = (uint64_t)b.batch << F;
-  const int64_t niter = walk_iterations<kPackedR>(w);
+  const int64_t niter = walk_iterations<R>(w);
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t* s_words = reinterpret_cast<uint32_t*>(s_rows4);
   int staged = -1;
@@ -532,7 +533,7 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
 #pragma unroll 4
       for (int idx = tid; idx < ndyn * nq4; idx += nthreads) {
         const int rr = idx / nq4, q = idx - rr * nq4;
-        const int v = n - C - 1 - (kPackedR + rr);
+        const int v = n - C - 1 - (R + rr);
         const int4 m = reinterpret_cast<const int4*>(M + (size_t)v * ncols)[q];
         reinterpret_cast<uint2*>(s_words)[idx] = make_uint2(packed::combine(m.x, m.y), packed::combine(m.z, m.w));
       }
@@ -543,7 +544,7 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
     c.T = reinterpret_cast<const int*>(b.T2 + (size_t)g * b.st);
-    packed::PackedWalker<kPackedR, MODE> W;
+    packed::PackedWalker<R, MODE> W;
     W.init(c, b.Ec + (size_t)g * b.se, b.M + (size_t)g * b.sm, cP);
     if constexpr (MODE == kModeMin) {
       int best = W.walk(c, niter);
@@ -660,8 +661,8 @@ bool plan_batched(int batch, int n, BatchPlan* bp) {
                                                       p.smem_int) != cudaSuccess || occ < 1)
       occ = 1;
     p.blocks = std::max(1, di.sms) * occ;
-    if (set_smem(bpacked_kernel<kModeMin>, p.smem_packed) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bpacked_kernel<kModeMin>, (1 << p.C) / 32,
+    if (set_smem(bpacked_kernel<kPackedR, kModeMin>, p.smem_packed) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, bpacked_kernel<kPackedR, kModeMin>, (1 << p.C) / 32,
                                                       p.smem_packed) != cudaSuccess ||
         occ < 1)
       occ = 1;
@@ -713,8 +714,8 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   btables_kernel<<<bp.batch, 256, 0, stream>>>(t);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = set_smem(bpacked_kernel<kModeMin>, bp.smem_packed)) != cudaSuccess) return e;
-  bpacked_kernel<kModeMin><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
+  if ((e = set_smem(bpacked_kernel<kPackedR, kModeMin>, bp.smem_packed)) != cudaSuccess) return e;
+  bpacked_kernel<kPackedR, kModeMin><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
   ++nl;
   auto kb = bwalk_kernel<kBiasedR, float, kModeMin>;
   if ((e = set_smem(kb, bp.smem_biased)) != cudaSuccess) return e;
@@ -726,8 +727,10 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   ++nl;
   bgroup_kernel<<<(bp.batch + 127) / 128, 128, 0, stream>>>(t);
   ++nl;
-  if ((e = set_smem(bpacked_kernel<kModeTiesInt>, bp.smem_packed)) != cudaSuccess) return e;
-  bpacked_kernel<kModeTiesInt><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
+  // the re-walk uses four register rows: a shorter unrolled body for the step with the tie test
+  const size_t smem_ties = (size_t)(bp.w - kPackedTiesR) << (bp.C + 1);
+  if ((e = set_smem(bpacked_kernel<kPackedTiesR, kModeTiesInt>, smem_ties)) != cudaSuccess) return e;
+  bpacked_kernel<kPackedTiesR, kModeTiesInt><<<bp.packed_blocks, (1 << bp.C) / 32, smem_ties, stream>>>(t);
   ++nl;
   auto kr = bwalk_kernel<kFastR, int, kModeTiesInt>;
   if ((e = set_smem(kr, bp.smem_int)) != cudaSuccess) return e;
