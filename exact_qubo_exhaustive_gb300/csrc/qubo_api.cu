@@ -4,6 +4,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <cmath>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -199,13 +200,32 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
     const int F_hi = n - C - (kFastR + 1);
     int F_lo = std::max(K, n - C - kMaxWalkedBits);
     if (F_hi < F_lo) return false;
-    const int want_s = ceil_log2_u64((target + units_base - 1) / units_base);
+    // Cost model of the persistent minimum pass: the units run in waves of one unit per block,
+    // and every unit pays a fixed set-up (linear terms, register rows, block reduction) worth
+    // about 2^18 states of walking on this part. Pick the F with the smallest
+    // waves * (states per unit + set-up); keep at least kFastR + 5 walked bits when possible, so
+    // that the resolve passes can split a unit into segments.
     const int F_keep = n - C - (kFastR + 5);
-    int Fv = std::min(K + want_s, F_keep);
-    Fv = std::max(Fv, F_lo);
-    Fv = std::min(Fv, F_hi);
-    *F = Fv;
-    return fast_fits(n, C, Fv, di.smem_optin, &smem);
+    const double sms = (double)(di.sms > 0 ? di.sms : 1);
+    int best_F = -1;
+    double best_cost = 0.0;
+    size_t best_smem = 0;
+    for (int Fv = F_lo; Fv <= F_hi; ++Fv) {
+      if (Fv > F_keep && best_F >= 0) break;
+      size_t sm = 0;
+      if (!fast_fits(n, C, Fv, di.smem_optin, &sm)) continue;
+      const double units = (double)units_base * std::ldexp(1.0, Fv - K);
+      const double cost = std::ceil(units / sms) * (std::ldexp(1.0, n - Fv) + std::ldexp(1.0, 18));
+      if (best_F < 0 || cost <= best_cost) {
+        best_F = Fv;
+        best_cost = cost;
+        best_smem = sm;
+      }
+    }
+    if (best_F < 0) return false;
+    *F = best_F;
+    smem = best_smem;
+    return true;
   };
   for (int C : Cs) {
     int F;

@@ -50,6 +50,15 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
 
   const uint64_t total_states = (uint64_t)1 << n;
   const uint64_t want = (uint64_t)k < total_states ? (uint64_t)k : total_states;
+  // The collect pass re-walks at least `want` whole units, so with the planner's default split
+  // it could re-walk a large share of the states; prefer about 16 units per wanted state when
+  // the kernels can run that split.
+  if (k_prefix <= 0) {
+    int F = p.F;
+    while (F < 31 && ((uint64_t)1 << F) < 16 * want) ++F;
+    Plan q;
+    if (F > p.F && plan_whole_problem(n, dtype, F, cache_bits, &q) == QUBO_OK) p = q;
+  }
   const uint64_t cap = std::max<uint64_t>(2 * want, (uint64_t)1 << 18);
 
   // one allocation: workspace | Q | candidates | counter
