@@ -144,6 +144,41 @@ def oracle_sample(seconds: float):
                       f"{dt:.1f} s, Gray-walk oracle (O(n) per state) on all host threads"}
 
 
+def oracle_configs(seconds_each: float):
+    """States/s of the CPU oracle on every workload, on one core and on all host cores: a bounded
+    sample of each (whole search for small n, leading slices otherwise)."""
+    import oracle
+    O = oracle.get()
+    all_cores = O.num_threads()
+    cases = [
+        ("n20_int32", qi.workload_n20(), 0),
+        ("n32_int32", qi.workload_n32(), 12),
+        ("n32_mattis_int32", qi.workload_n32_mattis()[0], 12),
+        ("n40_int32", qi.workload_n40(), 18),
+        ("n36_fp32", qi.workload_n36_f32(), 14),
+        ("batched_n24_int32", qi.workload_batched(64)[0], 0),
+    ]
+    out = {"cores_all": all_cores}
+    for name, Q, k in cases:
+        n = Q.shape[0]
+        row = {}
+        for label, threads in (("one_core", 1), ("all_cores", all_cores)):
+            O.set_threads(threads)
+            t0 = time.perf_counter()
+            done = 0
+            states = 0
+            while True:
+                O.solve_slice(Q, k, done % (1 << k)) if k else O.solve(Q)
+                done += 1
+                states += 1 << (n - k)
+                if time.perf_counter() - t0 >= seconds_each or (k == 0 and done >= 3):
+                    break
+            row[label] = states / (time.perf_counter() - t0)
+        out[name] = row
+    O.set_threads(all_cores)
+    return out
+
+
 def config_dict(plan=None):
     cfg = {"workload": WORKLOAD, "n": N, "states_per_step": STATES, "seed": qi.MASTER_SEED + 2,
            "l2": "flushed between steps (256 MB device write outside the timed events)"}
@@ -340,6 +375,7 @@ def other_configs(q, torch, dev, stream):
 
     for name, n, Q, dt in (("n40_narrow_int32", 40, qi.workload_n40_narrow(), q.INT32),
                            ("n36_fp32", 36, qi.workload_n36_f32(), q.FP32), ("n32_int32", 32, qi.workload_n32(), q.INT32),
+                           ("n32_mattis_int32", 32, qi.workload_n32_mattis()[0], q.INT32),
                            ("n20_int32", 20, qi.workload_n20(), q.INT32)):
         dq = torch.from_numpy(Q).to(dev)
         nb = q.workspace_bytes(n, dt)
@@ -440,6 +476,8 @@ def main(argv=None):
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="only run two searches of an N-variable instance (for ncu), print no JSON")
     ap.add_argument("--profile-dtype", choices=["int32", "fp32", "int32_narrow"], default="int32")
+    ap.add_argument("--oracle-configs", type=float, default=0.0, metavar="SECONDS",
+                    help="time the CPU oracle on every workload (one core and all cores) and exit")
     ap.add_argument("--profile-batched", type=int, default=0, metavar="B",
                     help="run two batched searches of the first B instances of the batched workload (for ncu)")
     args = ap.parse_args(argv)
@@ -447,6 +485,9 @@ def main(argv=None):
         return profile_case(args.profile_case, args.profile_dtype)
     if args.profile_batched:
         return profile_batched(args.profile_batched)
+    if args.oracle_configs:
+        print(json.dumps(oracle_configs(args.oracle_configs)))
+        return 0
     if args.warmup < 3:
         log("warmup raised to 3 (timing rule)")
         args.warmup = 3

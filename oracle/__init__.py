@@ -63,6 +63,7 @@ def _load(mutant: int = 0) -> ctypes.CDLL:
         lib.oracle_fold_i32.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_fold_f32.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
         lib.oracle_fold_f64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+        lib.oracle_set_threads.argtypes = [ctypes.c_int]
         lib.oracle_lowest_i64.restype = ctypes.c_int
         lib.oracle_lowest_i64.argtypes = [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, ctypes.c_uint64, ctypes.c_uint64,
                                           ctypes.c_void_p, ctypes.c_void_p]
@@ -113,6 +114,9 @@ class Oracle:
 
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
+
+    def set_threads(self, t: int) -> None:
+        self.lib.oracle_set_threads(int(t))
 
     # -- folding and energies
     def fold_i32(self, Q) -> np.ndarray:

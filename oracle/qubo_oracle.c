@@ -70,6 +70,15 @@ static int thread_count(void) {
 
 ORACLE_API int oracle_num_threads(void) { return thread_count(); }
 
+/* Threads of the following parallel regions (timing of the oracle on one core or on all). */
+ORACLE_API void oracle_set_threads(int t) {
+#ifdef _OPENMP
+  if (t > 0) omp_set_num_threads(t);
+#else
+  (void)t;
+#endif
+}
+
 /* ---------------------------------------------------------------- folding */
 
 /* U (n x n, row-major) from int32 Q: U_ii = Q_ii, U_ij = Q_ij + Q_ji for i < j, 0 below. */
