@@ -18,11 +18,17 @@ import os
 import numpy as np
 
 __all__ = [
-    "QuboError", "INT32", "FP32", "solve", "solve_slices", "solve_slice_range", "solve_batched",
-    "solve_device", "solve_batched_device", "workspace_bytes", "batched_workspace_bytes", "plan",
-    "probe_alu", "last_launch_count", "slice_range_workspace_bytes", "solve_slice_range_device",
-    "enable_kernel_timing", "kernel_time_ms", "solve_device_no_alloc", "NO_ALLOC_SCRATCH_BYTES", "status_string", "last_error", "request_abort", "clear_abort",
-    "library_path", "RESULT_DTYPE",
+    "QuboError", "INT32", "FP32", "FP64", "RESULT_DTYPE", "library_path",
+    # whole problems, slices, ranges, batches
+    "solve", "solve_slices", "solve_slice_range", "solve_batched",
+    "solve_device", "solve_slice_range_device", "solve_batched_device", "solve_device_no_alloc",
+    "workspace_bytes", "slice_range_workspace_bytes", "batched_workspace_bytes", "NO_ALLOC_SCRATCH_BYTES",
+    # the k lowest energies, Ising input, long runs
+    "solve_lowest", "LOWEST_MAX_K", "solve_ising", "ising_to_qubo",
+    "solve_checkpointed", "checkpoint_read", "fnv1a64", "INCOMPLETE",
+    # planner, measurement, status, cancellation
+    "plan", "probe_alu", "enable_kernel_timing", "kernel_time_ms", "last_launch_count",
+    "status_string", "last_error", "request_abort", "clear_abort", "rank_to_bits",
 ]
 
 INT32 = 0
