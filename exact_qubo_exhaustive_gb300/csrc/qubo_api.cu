@@ -149,6 +149,9 @@ const DevInfo& device_info() {
 namespace {
 
 constexpr size_t kStaticSmemReserve = 2048;
+// Work units of one call: unit indices are 32-bit (the tied-unit list), and every unit keeps an
+// int32 minimum in the workspace.
+constexpr double kMaxUnits = 2147483648.0;
 
 // QUBO_TENSOR_CORES=1 in the environment selects the tensor-core minimum pass where it applies.
 // It is exact and tested, but on this part its per-tile commit round trip keeps it below the
@@ -160,7 +163,7 @@ bool tensor_cores_enabled() {
 
 bool fast_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
   const int w = n - F - C;
-  if (C < 9 || C > 12 || F < 0 || F > 31 || w < kFastR + 1 || w > kMaxWalkedBits) return false;
+  if (C < 9 || C > 12 || F < 0 || w < kFastR + 1 || w > kMaxWalkedBits) return false;
   const size_t sm = (size_t)(w - kFastR) << (C + 2);
   if (sm + kStaticSmemReserve + kFastScanSlotBytes > smem_optin) return false;
   *smem = sm;
@@ -169,7 +172,7 @@ bool fast_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
 
 bool generic_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
   const int w = n - F - C;
-  if (C < 0 || C > kGenericMaxC || F < 0 || F > 31 || w < 0 || w > kMaxWalkedBits) return false;
+  if (C < 0 || C > kGenericMaxC || F < 0 || w < 0 || w > kMaxWalkedBits) return false;
   const size_t sm = (size_t)w << (C + 2);
   if (sm + kStaticSmemReserve > smem_optin) return false;
   *smem = sm < 16 ? 16 : sm;
@@ -195,6 +198,7 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   auto pick_F_fast = [&](int C, int* F) {
     if (explicit_F) {
       *F = k_prefix;
+      if ((double)units_base * std::ldexp(1.0, k_prefix - K) > kMaxUnits) return false;
       return fast_fits(n, C, *F, di.smem_optin, &smem);
     }
     const int F_hi = n - C - (kFastR + 1);
@@ -215,6 +219,7 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
       size_t sm = 0;
       if (!fast_fits(n, C, Fv, di.smem_optin, &sm)) continue;
       const double units = (double)units_base * std::ldexp(1.0, Fv - K);
+      if (units > kMaxUnits) continue;
       const double cost = std::ceil(units / sms) * (std::ldexp(1.0, n - Fv) + std::ldexp(1.0, 18));
       if (best_F < 0 || cost <= best_cost) {
         best_F = Fv;
@@ -244,7 +249,7 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
       // spread small problems over a few blocks when possible
       while (F - K < 8 && n - C - F > 0 && ((units_base << (F - K)) < target)) ++F;
     }
-    if (generic_fits(n, C, F, di.smem_optin, &smem)) {
+    if ((double)units_base * std::ldexp(1.0, F - K) <= kMaxUnits && generic_fits(n, C, F, di.smem_optin, &smem)) {
       p.variant = kGeneric;
       p.C = C;
       p.F = F;

@@ -251,6 +251,27 @@ def test_n40_slices_against_oracle(q, minpass):
         assert (x[s] == want[1]).all()
 
 
+def test_maximum_size_n62_slices_against_oracle(q):
+    # n = 62, the largest size the ABI takes: slices of 2^24 states (int32) and 2^22 (fp32)
+    n = 62
+    Q = qi.random_upper_int(n, -100, 100, 6262)
+    k = 38
+    ids = qi.Stream(6263).integers(0, (1 << k) - 1, 3).astype(np.uint64)
+    e, x, t = q.solve_slices(Q, k, ids)
+    for s, sid in enumerate(ids):
+        want = O.solve_slice(Q, k, int(sid))
+        assert (int(e[s]), int(t[s])) == (want[0], want[2]) and (x[s] == want[1]).all()
+    Qf = qi.random_symmetric_normal_f32(n, 6264)
+    k = 40
+    ids = qi.Stream(6265).integers(0, (1 << k) - 1, 2).astype(np.uint64)
+    e, x, t = q.solve_slices(Qf, k, ids)
+    U = O.fold_f32(Qf)
+    for s, sid in enumerate(ids):
+        want = O.solve_slice(Qf, k, int(sid))
+        assert O.eval64(U, x[s]) == e[s] and abs(e[s] - want[0]) <= fp32_tol(Qf)
+        assert (x[s] == want[1]).all()
+
+
 def test_n40_full_solve_consistent_with_sampled_slices(q):
     Q = qi.workload_n40()
     e, x, t = q.solve(Q)
