@@ -14,10 +14,13 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
   const unsigned one = (unsigned)(seed > 0 ? 1 : 2);  // 1 at run time (seed is 1), unknown to the compiler
   int a[kChains];
   float f[kChains];
+  unsigned long long f2[kChains];  // kind 9: pairs of fp32 in one 64-bit register
 #pragma unroll
   for (int k = 0; k < kChains; ++k) {
     a[k] = (threadIdx.x * 7 + k * 13 + seed) & 1023;
     f[k] = (float)a[k] * 0.5f;
+    const float lo = f[k], hi = f[k] + 1.0f;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(f2[k]) : "f"(lo), "f"(hi));
   }
   const unsigned long long c0 = clock64();
   unsigned long long g0;
@@ -35,6 +38,7 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
       if (KIND == 5) f[k] = fminf(f[k], f[(k + 1) % kChains]);
       if (KIND == 6) a[k] = (int)__vimin3_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 7) a[k] = (int)__viaddmin_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
+      if (KIND == 9) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(f2[k]) : "l"(f2[(k + 1) % kChains]));
       if (KIND == 8) {
         // int32 adds, half of them as multiply-adds by a run-time one, so that the ALU and the
         // FMA pipe's integer multiply-add unit share them
@@ -51,7 +55,11 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(g1));
   int s = 0;
 #pragma unroll
-  for (int k = 0; k < kChains; ++k) s += a[k] + (int)f[k];
+  for (int k = 0; k < kChains; ++k) {
+    float lo, hi;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(f2[k]));
+    s += a[k] + (int)f[k] + (int)lo + (int)hi;
+  }
   out[blockIdx.x * blockDim.x + threadIdx.x] = s;
   if (threadIdx.x == 0) {
     clk[2 * blockIdx.x] = c1 - c0;
@@ -88,7 +96,8 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       case 5: return launch<5>(blocks, it, out, clk);
       case 6: return launch<6>(blocks, it, out, clk);
       case 7: return launch<7>(blocks, it, out, clk);
-      default: return launch<8>(blocks, it, out, clk);
+      case 8: return launch<8>(blocks, it, out, clk);
+      default: return launch<9>(blocks, it, out, clk);
     }
   };
   cudaEvent_t e0 = nullptr, e1 = nullptr;
@@ -111,7 +120,8 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       ns += (double)h[2 * b + 1];
     }
     *sm_mhz = ns > 0 ? cy / ns * 1e3 : 0.0;
-    *ops_per_s = (double)blocks * 256.0 * iters * kChains / (ms * 1e-3);
+    // kind 9 performs two fp32 adds per instruction
+    *ops_per_s = (double)blocks * 256.0 * iters * kChains * (kind == 9 ? 2 : 1) / (ms * 1e-3);
   }
 done:
   if (e0) cudaEventDestroy(e0);
