@@ -14,7 +14,7 @@ so the stream can be produced in vectorised blocks.
   rounded to fp32 afterwards;
 * matrices are filled row-major over the upper triangle i <= j, one draw per entry.
 
-The pages benchmark on "a uniformly random matrix" without a range or a seed
+The pages benchmark on uniformly random matrices without stating a range or a seed
 (Terastate-per-second QUBO Brute-Force, §V-C); the ranges and the master seed below are
 the workload definition used throughout this repository.
 """
