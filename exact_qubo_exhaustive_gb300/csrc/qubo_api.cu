@@ -152,6 +152,8 @@ constexpr size_t kStaticSmemReserve = 2048;
 // Work units of one call: unit indices are 32-bit (the tied-unit list), and every unit keeps an
 // int32 minimum in the workspace.
 constexpr double kMaxUnits = 2147483648.0;
+// Problems with at least this many variables also launch the packed and biased minimum passes.
+constexpr int kNarrowPassesMinN = 30;
 
 // QUBO_TENSOR_CORES=1 in the environment selects the tensor-core minimum pass where it applies.
 // It is exact and tested, but on this part its per-tile commit round trip keeps it below the
@@ -207,15 +209,12 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
     // Cost model of the persistent minimum pass: the units run in waves of one unit per block,
     // and every unit pays a fixed set-up (linear terms, register rows, block reduction) worth
     // about 2^18 states of walking on this part. Pick the F with the smallest
-    // waves * (states per unit + set-up); keep at least kFastR + 5 walked bits when possible, so
-    // that the resolve passes can split a unit into segments.
-    const int F_keep = n - C - (kFastR + 5);
+    // waves * (states per unit + set-up).
     const double sms = (double)(di.sms > 0 ? di.sms : 1);
     int best_F = -1;
     double best_cost = 0.0;
     size_t best_smem = 0;
     for (int Fv = F_lo; Fv <= F_hi; ++Fv) {
-      if (Fv > F_keep && best_F >= 0) break;
       size_t sm = 0;
       if (!fast_fits(n, C, Fv, di.smem_optin, &sm)) continue;
       const double units = (double)units_base * std::ldexp(1.0, Fv - K);
@@ -274,10 +273,14 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   p.seg_bits = (niter > 0) ? seg : 0;
   // Biased-binade minimum pass (int32 input; it needs at least one iteration of 2^(kBiasedR+1)
   // Gray steps and stages fewer shared rows than the int32 pass, so the same launch shape fits).
-  p.biased = p.variant == kFast && dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
+  // Below 2^30 states a search takes tens of microseconds, mostly kernel launches: the alternative
+  // minimum passes (each launched, the ones that do not apply exiting at once) would cost more
+  // than they save, so small problems run the int32 pass alone.
+  const bool narrow_passes = n >= kNarrowPassesMinN;
+  p.biased = narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
   // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
   // shared rows are 2 bytes per column.
-  if (p.variant == kFast && dtype == QUBO_INT32 && p.C >= 10 && p.w >= kPackedR + 1) {
+  if (narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.C >= 10 && p.w >= kPackedR + 1) {
     p.packed_threads = (1 << p.C) / 32;
     p.packed_smem = packed_smem_bytes(p.C, p.w);
     int pocc = 0;

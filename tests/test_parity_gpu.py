@@ -130,8 +130,8 @@ def test_biased_walk_range_limit_is_exact(q, sign):
     # The CUDA-core minimum walk keeps column energies in the fp32 binade [2^23, 2^24) for
     # sum |U| <= 2^22 - 1 and in int32 above. Both sides of the limit, with running values pushed
     # to the extremes: all-negative entries reach E = -sum |U| at x = 1, all-positive ones +sum |U|.
-    n = 26
-    lo, hi = {"mixed": (-20000, 20000), "negative": (-20000, -1), "positive": (1, 20000)}[sign]
+    n = 30
+    lo, hi = {"mixed": (-15000, 15000), "negative": (-15000, -1), "positive": (1, 15000)}[sign]
     for total in ((1 << 22) - 1, 1 << 22):
         Q = np.triu(qi.random_upper_int(n, lo, hi, 2300 + total % 7))
         if sign == "positive":
@@ -168,8 +168,7 @@ def test_fewer_threads_than_variables(q):
 
 # ---------------------------------------------------------------- packed 16x2 minimum pass
 
-@pytest.mark.parametrize("n,lo,hi,seed", [(19, -30, 30, 1), (22, -20, 20, 2), (26, -9, 9, 3), (30, -3, 3, 4),
-                                          (31, 0, 2, 5)])
+@pytest.mark.parametrize("n,lo,hi,seed", [(30, -30, 30, 1), (30, -9, 9, 3), (31, -3, 3, 4), (31, 0, 2, 5)])
 def test_packed_pass_small_range(q, n, lo, hi, seed):
     Q = qi.random_upper_int(n, lo, hi, 2400 + seed)
     assert int(np.abs(Q.astype(np.int64)).sum()) <= (1 << 14) - 1
@@ -180,8 +179,8 @@ def test_packed_pass_small_range(q, n, lo, hi, seed):
 @pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
 def test_packed_range_limit_is_exact(q, sign):
     # sum |U| = 2^14 - 1 runs the packed pass (values pushed to +-sum |U|), 2^14 the biased one
-    n = 24
-    lo, hi = {"mixed": (-80, 80), "negative": (-80, -1), "positive": (1, 80)}[sign]
+    n = 30
+    lo, hi = {"mixed": (-50, 50), "negative": (-50, -1), "positive": (1, 50)}[sign]
     for total in ((1 << 14) - 1, 1 << 14):
         Q = np.triu(qi.random_upper_int(n, lo, hi, 2450 + total % 5))
         if sign == "positive":
@@ -198,8 +197,16 @@ def test_packed_range_limit_is_exact(q, sign):
 
 def test_packed_pass_all_ties(q):
     # Q = 0: every state ties; the packed minimum is 0 and the resolve pass counts 2^n
-    e, x, t = q.solve(np.zeros((27, 27), np.int32))
-    assert (e, t) == (0, 1 << 27) and not x.any()
+    assert q.plan(30)["packed"] == 1
+    e, x, t = q.solve(np.zeros((30, 30), np.int32))
+    assert (e, t) == (0, 1 << 30) and not x.any()
+
+
+def test_small_problems_run_the_int32_pass_alone(q):
+    # below 30 variables only the int32 minimum pass is launched (launch-bound sizes)
+    p = q.plan(24)
+    assert p["packed"] == 0 and p["biased"] == 0
+    check_int(q, qi.random_upper_int(24, -5, 5, 2480))
 
 
 def test_n40_narrow_slices_against_oracle(q):
