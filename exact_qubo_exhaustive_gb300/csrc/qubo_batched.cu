@@ -228,14 +228,16 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
 // lowest rank and the tie count.
 // ------------------------------------------------------------------------------------------------
 constexpr int kBatchTabMaxN = 32;
-constexpr int kPackedTiesR = 4;  // register rows of the packed re-walk of the minimum units
+constexpr int kPackedTiesR = 5;  // register rows of the packed re-walk of the minimum units
 constexpr int kBatchTabC = 12;
+static_assert(kBatchTabC == 12, "packed::HalfRows splits the cached bits 6 + 6");
 
 struct BatchTables {
   int batch, n, C, F, w;
   const int32_t* Q;
   int32_t* U;  // batch x n*n        folded triangle
-  int32_t* M;  // batch x (n-C)*2^C  interaction rows
+  int32_t* M;  // batch x (n-C)*2^C  interaction rows (instances of the biased and int32 passes)
+  int32_t* H;  // batch x (n-C)*128  half-subset sums of the rows (packed pass: M[v][j] from two)
   int32_t* Ec; // batch x 2^C        cached self energies
   int32_t* T;  // batch x 2^w        walked energies in Gray order
   uint32_t* T2;  // batch x 2^w      T's low 16 bits in both halves (packed pass)
@@ -245,7 +247,7 @@ struct BatchTables {
   int32_t* gmin;
   unsigned long long* grank;
   unsigned long long* gties;
-  size_t su, sm, se, st;  // per-instance strides of U, M, Ec, T / T2
+  size_t su, sm, sh, se, st;  // per-instance strides of U, M, H, Ec, T / T2
 };
 
 enum BatchClass : int { kBatchPacked = 0, kBatchBiased = 1, kBatchInt = 2 };
@@ -349,10 +351,19 @@ __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
   }
   __syncthreads();
   const int ncols = 1 << C;
-  int32_t* M = b.M + (size_t)g * b.sm;
-  for (int idx = tid; idx < nv * ncols; idx += nt) {
-    const int v = idx >> C, j = idx & (ncols - 1);
-    M[idx] = sA[v][j & (nlo - 1)] + sB[v][j >> lo];
+  if (batch_class(b.S[g]) == kBatchPacked) {
+    // the packed pass forms its rows from the half sums (packed::HalfRows): no M table
+    int32_t* H = b.H + (size_t)g * b.sh;
+    for (int idx = tid; idx < nv * packed::HalfRows::kStride; idx += nt) {
+      const int v = idx / packed::HalfRows::kStride, r = idx % packed::HalfRows::kStride;
+      H[idx] = r < 64 ? sA[v][r] : sB[v][r - 64];
+    }
+  } else {
+    int32_t* M = b.M + (size_t)g * b.sm;
+    for (int idx = tid; idx < nv * ncols; idx += nt) {
+      const int v = idx >> C, j = idx & (ncols - 1);
+      M[idx] = sA[v][j & (nlo - 1)] + sB[v][j >> lo];
+    }
   }
   int32_t* Ec = b.Ec + (size_t)g * b.se;
   for (int j = tid; j < ncols; j += nt) {
@@ -436,7 +447,7 @@ __global__ void __launch_bounds__(256, 1) bwalk_kernel(BatchTables b) {
     __syncthreads();  // the previous unit is done with sL and the staged rows
     if (g != staged) {
       const int4* M4 = reinterpret_cast<const int4*>(b.M + (size_t)g * b.sm);
-#pragma unroll 4
+#pragma unroll 8
       for (int idx = tid; idx < ndyn * nq; idx += nthreads) {
         const int rr = idx / nq, q = idx - rr * nq;
         const int v = n - C - 1 - (R + rr);
@@ -498,9 +509,9 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   __shared__ int sL[64];
   __shared__ int s_red[32];
   __shared__ __align__(16) uint32_t s_scan[MODE == kModeTiesInt ? 128 * 16 : 4];
+  __shared__ __align__(16) int sH[(kBatchTabMaxN - kBatchTabC) * packed::HalfRows::kStride];
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int n = b.n, C = b.C, F = b.F, w = b.w;
-  const int ncols = 1 << C, nwords = ncols >> 1;
   const int ndyn = w - R;
   const uint64_t units = (uint64_t)b.batch << F;
   const int64_t niter = walk_iterations<R>(w);
@@ -527,14 +538,17 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
     if (b.status[g] != QUBO_OK || batch_class(b.S[g]) != kBatchPacked) continue;
     if (MODE == kModeTiesInt && b.unit_min[u] != b.gmin[g]) continue;
     __syncthreads();
+    const packed::HalfRows rows{sH};
     if (g != staged) {
-      const int32_t* M = b.M + (size_t)g * b.sm;
-      const int nq4 = nwords >> 1;  // two words per 16-byte load
-#pragma unroll 4
-      for (int idx = tid; idx < ndyn * nq4; idx += nthreads) {
-        const int rr = idx / nq4, q = idx - rr * nq4;
-        const int v = n - C - 1 - (R + rr);
-        const int4 m = reinterpret_cast<const int4*>(M + (size_t)v * ncols)[q];
+      // the instance's half sums, then its shared rows (positions >= R) formed from them
+      const int nh = (n - C) * packed::HalfRows::kStride;
+      const int4* H4 = reinterpret_cast<const int4*>(b.H + (size_t)g * b.sh);
+      for (int idx = tid; idx < (nh >> 2); idx += nthreads) reinterpret_cast<int4*>(sH)[idx] = H4[idx];
+      __syncthreads();
+      const int lq = C - 2;  // log2 of the int4 quads per row (two words each)
+      for (int idx = tid; idx < (ndyn << lq); idx += nthreads) {
+        const int rr = idx >> lq, q = idx & ((1 << lq) - 1);
+        const int4 m = rows.quad(n - C - 1 - (R + rr), q);
         reinterpret_cast<uint2*>(s_words)[idx] = make_uint2(packed::combine(m.x, m.y), packed::combine(m.z, m.w));
       }
       staged = g;
@@ -544,8 +558,8 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
     c.T = reinterpret_cast<const int*>(b.T2 + (size_t)g * b.st);
-    packed::PackedWalker<R, MODE> W;
-    W.init(c, b.Ec + (size_t)g * b.se, b.M + (size_t)g * b.sm, cP);
+    packed::PackedWalker<R, MODE, packed::HalfRows> W;
+    W.init(c, b.Ec + (size_t)g * b.se, rows, cP);
     if constexpr (MODE == kModeMin) {
       int best = W.walk(c, niter);
 #pragma unroll
@@ -609,6 +623,7 @@ BatchTables batch_tables(const BatchPlan& bp, unsigned char* base, size_t* bytes
   t.w = bp.w;
   t.su = (size_t)bp.n * bp.n;
   t.sm = (size_t)(bp.n - bp.C) << bp.C;
+  t.sh = (size_t)(bp.n - bp.C) * packed::HalfRows::kStride;
   t.se = (size_t)1 << bp.C;
   t.st = (size_t)1 << bp.w;
   size_t off = 0;
@@ -620,6 +635,7 @@ BatchTables batch_tables(const BatchPlan& bp, unsigned char* base, size_t* bytes
   const size_t B = (size_t)bp.batch;
   t.U = reinterpret_cast<int32_t*>(take(B * t.su * 4));
   t.M = reinterpret_cast<int32_t*>(take(B * t.sm * 4));
+  t.H = reinterpret_cast<int32_t*>(take(B * t.sh * 4));
   t.Ec = reinterpret_cast<int32_t*>(take(B * t.se * 4));
   t.T = reinterpret_cast<int32_t*>(take(B * t.st * 4));
   t.T2 = reinterpret_cast<uint32_t*>(take(B * t.st * 4));
@@ -729,7 +745,6 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   ++nl;
   bgroup_kernel<<<(bp.batch + 127) / 128, 128, 0, stream>>>(t);
   ++nl;
-  // the re-walk uses four register rows: a shorter unrolled body for the step with the tie test
   const size_t smem_ties = (size_t)(bp.w - kPackedTiesR) << (bp.C + 1);
   if ((e = set_smem(bpacked_kernel<kPackedTiesR, kModeTiesInt>, smem_ties)) != cudaSuccess) return e;
   bpacked_kernel<kPackedTiesR, kModeTiesInt><<<bp.packed_blocks, (1 << bp.C) / 32, smem_ties, stream>>>(t);

@@ -51,36 +51,109 @@ __device__ __forceinline__ uint32_t pmin_all(const uint32_t* v) {
 // Two signed values as the exact signed combination hi * 2^16 + lo.
 __device__ __forceinline__ uint32_t combine(int lo, int hi) { return (uint32_t)(hi * 65536 + lo); }
 
+// Where a walker reads the interaction rows M[v][*] of the cached columns (int4 q holds columns
+// 4q .. 4q+3): a table in global memory, or the row's two half-subset sums in shared memory.
+struct GlobalRows {
+  const int* M;
+  int ncols;
+  __device__ __forceinline__ int4 quad(int v, int q) const {
+    return reinterpret_cast<const int4*>(M + (size_t)v * ncols)[q];
+  }
+};
+// 12 cached bits split 6 + 6: M[v][j] = H[v][j mod 64] + H[v][64 + j / 64], with H[v][l] the sum
+// of U[v][c] over the cached variables c of the low subset l and H[v][64 + h] over the high
+// subset h.
+struct HalfRows {
+  static constexpr int kStride = 128;
+  const int* H;
+  __device__ __forceinline__ int4 quad(int v, int q) const {
+    const int* h = H + v * kStride;
+    const int4 a = reinterpret_cast<const int4*>(h)[q & 15];
+    const int b = h[64 + (q >> 4)];
+    return make_int4(a.x + b, a.y + b, a.z + b, a.w + b);
+  }
+};
+
 struct TieScan {
   uint64_t cnt, rmin;
 };
 
-// The columns of one thread's 16 words (read back from `slot`) at Gray step i whose energy
-// relative to s, (half + T) mod 2^16, equals the target t: their number and lowest rank.
-static __device__ __noinline__ TieScan scan_ties(const uint4* slot, int thread, int nthreads, int C, uint64_t prank,
-                                                 uint64_t i, uint32_t tv, uint32_t t) {
-  TieScan r = {0, ~0ull};
-  const uint64_t ib = prank | (gray_code(i) << C);
-  for (int k = 0; k < kPW / 4; ++k) {
+// The states of one half-iteration (2^R Gray steps from step i0, over which only the register
+// rows a < R flip) whose energy relative to s, (half + T) mod 2^16, equals the target t: their
+// number and lowest rank. `slot` holds the thread's 16 words at the half's last step; each flip
+// forms its register row again from the rows of M and the unit's linear terms sL, as the
+// walker's init does. Over a half the register bits run through the reflected Gray code of R bits
+// once, so they start at 0 and end at 2^(R-1) in the first half and the other way round in the
+// second. Each step is tested with the walk's own minimum tree; only a step that reaches the
+// target is searched column by column.
+template <int R, class RS>
+static __device__ __noinline__ TieScan scan_half(const uint4* slot, RS rows, const int* sL, int n, int C, int thread,
+                                                 int nthreads, uint64_t prank, uint64_t i0, bool second,
+                                                 const uint32_t* __restrict__ T2, uint32_t t) {
+  constexpr int kW = 16, kH = 1 << R;
+  uint32_t V[kW];
+#pragma unroll
+  for (int k = 0; k < kW / 4; ++k) {
     const uint4 q = slot[k];
-    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-    for (int e = 0; e < 4; ++e)
-      for (int h = 0; h < 2; ++h) {
-        const uint32_t val = (((words[e] >> (16 * h)) & 0xffffu) + tv) & 0xffffu;
-        if (val == t) {
-          const uint64_t rank = ib | (uint64_t)((((k * nthreads + thread) << 3)) | (e << 1) | h);
-          ++r.cnt;
-          r.rmin = rank < r.rmin ? rank : r.rmin;
+    V[4 * k] = q.x;
+    V[4 * k + 1] = q.y;
+    V[4 * k + 2] = q.z;
+    V[4 * k + 3] = q.w;
+  }
+  // V += sign * (register row a), the row formed again from M and L (kept out of registers)
+  auto flip = [&](int a, bool up) {
+    const int v = n - C - 1 - a;
+    const int Lv = sL[v];
+#pragma unroll
+    for (int k = 0; k < kW / 4; ++k) {
+      const int qi = k * nthreads + thread;
+      const int4 m0 = rows.quad(v, 2 * qi), m1 = rows.quad(v, 2 * qi + 1);
+      const uint32_t r[4] = {(uint32_t)((m0.y + Lv) * 65536 + (m0.x + Lv)), (uint32_t)((m0.w + Lv) * 65536 + (m0.z + Lv)),
+                             (uint32_t)((m1.y + Lv) * 65536 + (m1.x + Lv)), (uint32_t)((m1.w + Lv) * 65536 + (m1.z + Lv))};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) V[4 * k + e] = up ? V[4 * k + e] + r[e] : V[4 * k + e] - r[e];
+    }
+  };
+  // back to the half's first state
+  flip(R - 1, second);
+  unsigned cur = second ? (1u << (R - 1)) : 0u;  // register bits at the half's first state
+  TieScan r = {0, ~0ull};
+  uint32_t tnext = __ldg(T2 + i0);
+  for (int L = 0; L < kH; ++L) {
+    const uint64_t i = i0 + L;
+    const uint32_t tw = tnext;
+    if (L + 1 < kH) tnext = __ldg(T2 + i + 1);
+    const uint32_t m = __viaddmin_u16x2(pmin_all<kW>(V), tw, 0xffffffffu);
+    if ((m & 0xffffu) <= t || (m >> 16) <= t) {
+      const uint32_t tv = tw & 0xffffu;
+      const uint64_t ib = prank | (gray_code(i) << C);
+#pragma unroll 1
+      for (int jj = 0; jj < kW; ++jj)
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t val = (((V[jj] >> (16 * h)) & 0xffffu) + tv) & 0xffffu;
+          if (val == t) {
+            const int k = jj >> 2, e = jj & 3;
+            const uint64_t rank = ib | (uint64_t)((((k * nthreads + thread) << 3)) | (e << 1) | h);
+            ++r.cnt;
+            r.rmin = rank < r.rmin ? rank : r.rmin;
+          }
         }
-      }
+    }
+    if (L + 1 < kH) {
+      const int a = __ffs(L + 1) - 1;
+      flip(a, !((cur >> a) & 1u));
+      cur ^= 1u << a;
+    }
   }
   return r;
 }
 
 // MODE kModeMin: running per-half minimum. MODE kModeTiesInt: count the states whose energy
 // equals a target (the known minimum) and keep the lowest rank among them; `aux` then holds the
-// target relative to s, B + (target - s), in both halves.
-template <int R, int MODE = kModeMin>
+// target relative to s, B + (target - s), in both halves. The ties walk does the minimum walk's
+// work per step and tests once per half-iteration; only a half that reaches the target is
+// scanned state by state.
+template <int R, int MODE = kModeMin, class RS = GlobalRows>
 struct PackedWalker {
   static_assert(MODE == kModeMin || MODE == kModeTiesInt, "");
   static_assert(R >= 1, "");
@@ -95,15 +168,17 @@ struct PackedWalker {
   int s;          // c(P) + sum of L over set walked positions >= R
   uint32_t aux;   // per half: B + (running best - s), or B + (target - s)
   uint64_t cnt = 0, rmin = ~0ull;  // kModeTiesInt
+  uint32_t hq = 0xffffffffu;       // kModeTiesInt: per-half minimum of the current half-iteration
+  RS rows;                         // the unit's rows of M (register rows for scan_half)
   struct RowBuf {
     uint4 q[kPW / 4];
   };
 
-  __device__ __forceinline__ void init(const WalkCtx& c, const int* __restrict__ Ec, const int* __restrict__ M,
-                                       int cP) {
+  __device__ __forceinline__ void init(const WalkCtx& c, const int* __restrict__ Ec, const RS& rs, int cP) {
     const int t = c.thread, T = c.nthreads, n = c.n, C = c.C;
     s = cP;
     aux = 0xffffffffu;
+    rows = rs;
     const int lt = 31 - __clz(T);
     int Lt = 0;
     for (int b = 0; b < lt; ++b)
@@ -126,16 +201,14 @@ struct PackedWalker {
         V[4 * k + e] = ((kHalfBias + (uint32_t)hi) << 16) | ((kHalfBias + (uint32_t)lo) & 0xffffu);
       }
     }
-    const int ncols = 1 << C;
 #pragma unroll
     for (int a = 0; a < R; ++a) {
       const int v = n - C - 1 - a;
       const int Lv = c.sL[v];
-      const int4* Mv4 = reinterpret_cast<const int4*>(M + (size_t)v * ncols);
 #pragma unroll
       for (int k = 0; k < kPW / 4; ++k) {
         const int qi = k * T + t;
-        const int4 m0 = Mv4[2 * qi], m1 = Mv4[2 * qi + 1];
+        const int4 m0 = rs.quad(v, 2 * qi), m1 = rs.quad(v, 2 * qi + 1);
         Row[a][4 * k + 0] = combine(m0.x + Lv, m0.y + Lv);
         Row[a][4 * k + 1] = combine(m0.z + Lv, m0.w + Lv);
         Row[a][4 * k + 2] = combine(m1.x + Lv, m1.y + Lv);
@@ -191,19 +264,26 @@ struct PackedWalker {
       if constexpr (MODE == kModeMin) {
         aux = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[(L >> 2) % kRing]), aux);
       } else {
-        // per half m + T (no state lies below the target, so a hit is an equal half)
-        const uint32_t q = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[(L >> 2) % kRing]), 0xffffffffu);
-        const uint32_t t = aux & 0xffffu;
-        const bool hit = (q & 0xffffu) <= t || (q >> 16) <= t;
-        if (__any_sync(0xffffffffu, hit) && hit) {
-          // rare: hand the thread's words to an out-of-line scan (keeps the unrolled walk small)
-          uint4* slot = reinterpret_cast<uint4*>(c.scratch) + 4 * c.thread;
+        // running per-half minimum of m + T over the half-iteration; s and the target are
+        // constant inside a half, so one test at its end finds every half that reaches the
+        // target (no state lies below it, so a hit is an equal value)
+        hq = __viaddmin_u16x2(pmin_all<kPW>(V), comp<L & 3>(tq[(L >> 2) % kRing]), hq);
+        if constexpr (L == kMid - 1 || L == kSteps - 1) {
+          const uint32_t t = aux & 0xffffu;
+          const bool hit = (hq & 0xffffu) <= t || (hq >> 16) <= t;
+          hq = 0xffffffffu;
+          if (__any_sync(0xffffffffu, hit) && hit) {
+            // rare: re-scan the half state by state out of line (keeps the unrolled walk small)
+            uint4* slot = reinterpret_cast<uint4*>(c.scratch) + 4 * c.thread;
 #pragma unroll
-          for (int k = 0; k < kPW / 4; ++k) slot[k] = make_uint4(V[4 * k], V[4 * k + 1], V[4 * k + 2], V[4 * k + 3]);
-          const TieScan r = scan_ties(slot, c.thread, c.nthreads, c.C, prank, base + L,
-                                      comp<L & 3>(tq[(L >> 2) % kRing]) & 0xffffu, t);
-          cnt += r.cnt;
-          rmin = r.rmin < rmin ? r.rmin : rmin;
+            for (int k = 0; k < kPW / 4; ++k) slot[k] = make_uint4(V[4 * k], V[4 * k + 1], V[4 * k + 2], V[4 * k + 3]);
+            constexpr bool second = L == kSteps - 1;
+            const TieScan r = scan_half<R, RS>(slot, rows, c.sL, c.n, c.C, c.thread, c.nthreads, prank,
+                                           base + (second ? kMid : 0), second,
+                                           reinterpret_cast<const uint32_t*>(c.T), t);
+            cnt += r.cnt;
+            rmin = r.rmin < rmin ? r.rmin : rmin;
+          }
         }
       }
       if constexpr ((L & 3) == 3) {

@@ -427,6 +427,30 @@ def test_batched_mixed_passes_against_oracle(q):
         assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), b
 
 
+def test_batched_packed_ties_across_steps_halves_and_columns(q):
+    # n = 24 instances of the packed pass (12 cached bits, 3 prefix bits, 9 walked bits) with
+    # variables whose couplings are all zero: each doubles the minimum's multiplicity, and the
+    # tied states then differ in a register-row bit (x_7..x_11; x_7 flips between the halves of
+    # an iteration), the shared row flipped mid-iteration (x_6), a row flipped between
+    # iterations (x_3..x_5), a cached bit (x_12..x_23) or a prefix bit (x_0..x_2)
+    n = 24
+    free_sets = [(1, 6, 9, 20), (4, 11), (7,), (0, 3, 5, 8, 10, 12, 23), ()]
+    Qs = []
+    for k, free in enumerate(free_sets):
+        Q = qi.random_upper_int(n, -20, 20, 540 + k)
+        for v in free:
+            Q[v, :] = 0
+            Q[:, v] = 0
+        Qs.append(Q)
+    Qs = np.stack(Qs)
+    assert np.abs(Qs.astype(np.int64)).sum(axis=(1, 2)).max() <= (1 << 14) - 1
+    e, x, t = q.solve_batched(Qs)
+    for b, free in enumerate(free_sets):
+        want = O.solve(Qs[b])
+        assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), b
+        assert want[2] % (1 << len(free)) == 0
+
+
 @pytest.mark.parametrize("n,batch", [(18, 40), (21, 12), (28, 2)])
 def test_batched_sizes_and_unit_splits(q, n, batch):
     # n = 18, 21: one unit per instance; n = 28: 2^7 units per instance
