@@ -258,33 +258,8 @@ __device__ __forceinline__ int batch_class(int64_t S) {
   return kBatchInt;
 }
 
-__global__ void __launch_bounds__(256) bprep_kernel(BatchTables b) {
-  __shared__ unsigned long long s_sum;
-  const int g = blockIdx.x, n = b.n;
-  const int32_t* Q = b.Q + (size_t)g * n * n;
-  int32_t* U = b.U + (size_t)g * b.su;
-  if (threadIdx.x == 0) s_sum = 0;
-  __syncthreads();
-  unsigned long long local = 0;
-  for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
-    long long u;
-    fold_entry(Q, n, idx / n, idx % n, &u);
-    local += (unsigned long long)(u < 0 ? -u : u);
-    U[idx] = (int32_t)u;  // only used when the range check passes
-  }
-  atomicAdd(&s_sum, local);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    b.S[g] = (int64_t)s_sum;
-    b.status[g] = s_sum > (unsigned long long)kMaxAbsSum ? QUBO_ERR_RANGE : QUBO_OK;
-    b.gmin[g] = kIntInf;
-    b.grank[g] = ~0ull;
-    b.gties[g] = 0;
-  }
-}
-
-// The caches of every instance (the single-problem tables, §II-C Table I), one block per instance.
-// The C cached bits split into a low half (lo bits) and a high half; with the partial sums of the
+// Fold, range check and caches of every instance (the single-problem tables, §II-C Table I), one
+// block per instance. The C cached bits split into a low half (lo bits) and a high half; with the partial sums of the
 // halves in shared memory every table entry is a few adds:
 //   M[v][j] = A_v[j_lo] + B_v[j_hi]                         (A, B: subset sums of U[v][cached])
 //   E(U_B)[j] = El[j_lo] + Eh[j_hi] + sum_{b in j_lo} Y[j_hi][b]   (Y: coupling of a high subset
@@ -297,14 +272,37 @@ __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
   __shared__ int sB[kBatchTabMaxN][kBatchMaxHalf];
   __shared__ int sEl[kBatchMaxHalf], sEh[kBatchMaxHalf];
   __shared__ int sY[kBatchMaxHalf][kBatchTabC / 2];
+  __shared__ unsigned long long s_sum;
   const int g = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
-  if (b.status[g] != QUBO_OK) return;
   const int n = b.n, C = b.C, w = b.w;
   const int lo = C / 2, hi = C - lo;
   const int nlo = 1 << lo, nhi = 1 << hi;
-  const int32_t* U = b.U + (size_t)g * b.su;
-  for (int i = tid; i < n * n; i += nt) sU[i] = U[i];
+  // U = the folded triangle of Q and S = sum |U|; the instance is searched when S fits int32
+  if (tid == 0) s_sum = 0;
   __syncthreads();
+  {
+    const int32_t* Q = b.Q + (size_t)g * n * n;
+    int32_t* U = b.U + (size_t)g * b.su;
+    unsigned long long local = 0;
+    for (int idx = tid; idx < n * n; idx += nt) {
+      long long u;
+      fold_entry(Q, n, idx / n, idx % n, &u);
+      local += (unsigned long long)(u < 0 ? -u : u);
+      sU[idx] = (int32_t)u;  // only used when the range check passes
+      U[idx] = (int32_t)u;
+    }
+    atomicAdd(&s_sum, local);
+  }
+  __syncthreads();
+  const int64_t S = (int64_t)s_sum;
+  if (tid == 0) {
+    b.S[g] = S;
+    b.status[g] = S > kMaxAbsSum ? QUBO_ERR_RANGE : QUBO_OK;
+    b.gmin[g] = kIntInf;
+    b.grank[g] = ~0ull;
+    b.gties[g] = 0;
+  }
+  if (S > kMaxAbsSum) return;
   const int nv = n - C;
   // cached bit k (0 = fastest) is variable n - 1 - k; low half k < lo, high half k >= lo
   for (int idx = tid; idx < nv * (nlo + nhi); idx += nt) {
@@ -351,7 +349,7 @@ __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
   }
   __syncthreads();
   const int ncols = 1 << C;
-  if (batch_class(b.S[g]) == kBatchPacked) {
+  if (batch_class(S) == kBatchPacked) {
     // the packed pass forms its rows from the half sums (packed::HalfRows): no M table
     int32_t* H = b.H + (size_t)g * b.sh;
     for (int idx = tid; idx < nv * packed::HalfRows::kStride; idx += nt) {
@@ -435,15 +433,18 @@ __global__ void __launch_bounds__(256, 1) bwalk_kernel(BatchTables b) {
   c.scratch = MODE != kModeMin ? reinterpret_cast<uint32_t*>(s_slot) : nullptr;
   // a contiguous range of units per block, so that a block stages each instance's rows once
   const uint64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
-  for (uint64_t u = u_begin; u < u_end; ++u) {
+  for (uint64_t u = u_begin, next; u < u_end; u = next) {
     const int g = (int)(u >> F);
     const uint64_t P = u & (((uint64_t)1 << F) - 1);
-    if (b.status[g] != QUBO_OK) continue;
-    if constexpr (MODE == kModeMin) {
-      if (batch_class(b.S[g]) != kClass) continue;
-    } else {
-      if (batch_class(b.S[g]) == kBatchPacked || b.unit_min[u] != b.gmin[g]) continue;  // packed: own re-walk
+    next = u + 1;
+    // instances this pass does not own are skipped whole (packed instances have their own re-walk)
+    const bool owned = b.status[g] == QUBO_OK &&
+                       (MODE == kModeMin ? batch_class(b.S[g]) == kClass : batch_class(b.S[g]) != kBatchPacked);
+    if (!owned) {
+      next = (uint64_t)(g + 1) << F;
+      continue;
     }
+    if (MODE != kModeMin && b.unit_min[u] != b.gmin[g]) continue;
     __syncthreads();  // the previous unit is done with sL and the staged rows
     if (g != staged) {
       const int4* M4 = reinterpret_cast<const int4*>(b.M + (size_t)g * b.sm);
@@ -508,7 +509,6 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
   __shared__ int s_red[32];
-  __shared__ __align__(16) uint32_t s_scan[MODE == kModeTiesInt ? 128 * 16 : 4];
   __shared__ __align__(16) int sH[(kBatchTabMaxN - kBatchTabC) * packed::HalfRows::kStride];
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int n = b.n, C = b.C, F = b.F, w = b.w;
@@ -529,13 +529,18 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   c.rows4 = s_rows4;
   c.rows1 = nullptr;
   c.t_global = true;
-  c.scratch = s_scan;
+  // kModeTiesInt: the scan slots (packed::scan_slot_words<R>() words per thread) follow the rows
+  c.scratch = MODE == kModeTiesInt ? s_words + ((size_t)ndyn << (C - 1)) : nullptr;
   // a contiguous range of units per block, so that a block stages each instance's rows once
   const uint64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
-  for (uint64_t u = u_begin; u < u_end; ++u) {
+  for (uint64_t u = u_begin, next; u < u_end; u = next) {
     const int g = (int)(u >> F);
     const uint64_t P = u & (((uint64_t)1 << F) - 1);
-    if (b.status[g] != QUBO_OK || batch_class(b.S[g]) != kBatchPacked) continue;
+    next = u + 1;
+    if (b.status[g] != QUBO_OK || batch_class(b.S[g]) != kBatchPacked) {  // not this pass's: skip it whole
+      next = (uint64_t)(g + 1) << F;
+      continue;
+    }
     if (MODE == kModeTiesInt && b.unit_min[u] != b.gmin[g]) continue;
     __syncthreads();
     const packed::HalfRows rows{sH};
@@ -727,8 +732,6 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   BatchTables t = batch_tables(bp, static_cast<unsigned char*>(d_ws), nullptr);
   t.Q = static_cast<const int32_t*>(d_Q);
   int nl = 0;
-  bprep_kernel<<<bp.batch, 256, 0, stream>>>(t);
-  ++nl;
   btables_kernel<<<bp.batch, 256, 0, stream>>>(t);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
@@ -745,7 +748,8 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   ++nl;
   bgroup_kernel<<<(bp.batch + 127) / 128, 128, 0, stream>>>(t);
   ++nl;
-  const size_t smem_ties = (size_t)(bp.w - kPackedTiesR) << (bp.C + 1);
+  const size_t smem_ties = ((size_t)(bp.w - kPackedTiesR) << (bp.C + 1)) +
+                           (size_t)((1 << bp.C) / 32) * packed::scan_slot_words<kPackedTiesR>() * 4;
   if ((e = set_smem(bpacked_kernel<kPackedTiesR, kModeTiesInt>, smem_ties)) != cudaSuccess) return e;
   bpacked_kernel<kPackedTiesR, kModeTiesInt><<<bp.packed_blocks, (1 << bp.C) / 32, smem_ties, stream>>>(t);
   ++nl;

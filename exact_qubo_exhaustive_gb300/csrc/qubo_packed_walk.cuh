@@ -78,51 +78,53 @@ struct TieScan {
   uint64_t cnt, rmin;
 };
 
-// The states of one half-iteration (2^R Gray steps from step i0, over which only the register
-// rows a < R flip) whose energy relative to s, (half + T) mod 2^16, equals the target t: their
-// number and lowest rank. `slot` holds the thread's 16 words at the half's last step; each flip
-// forms its register row again from the rows of M and the unit's linear terms sL, as the
-// walker's init does. Over a half the register bits run through the reflected Gray code of R bits
-// once, so they start at 0 and end at 2^(R-1) in the first half and the other way round in the
-// second. Each step is tested with the walk's own minimum tree; only a step that reaches the
-// target is searched column by column.
-template <int R, class RS>
-static __device__ __noinline__ TieScan scan_half(const uint4* slot, RS rows, const int* sL, int n, int C, int thread,
-                                                 int nthreads, uint64_t prank, uint64_t i0, bool second,
-                                                 const uint32_t* __restrict__ T2, uint32_t t) {
+// Words per thread of the tie walk's scan slot: the 16 column words and the R register rows.
+template <int R>
+constexpr int scan_slot_words() { return 16 * (1 + R); }
+
+// The states of one half-iteration of thread `owner` (2^R Gray steps from step i0, over which
+// only the register rows a < R flip) whose energy relative to s, (half + T) mod 2^16, equals the
+// target t: their number and lowest rank. Called by all 32 lanes of a warp together; lane L
+// tests steps L, L + 32, ... of the half. `slot` holds the owner's 16 words at the half's last
+// step and its register rows. The words at step i differ from those at the last step by the
+// register rows whose bits differ between the two Gray codes (+row where step i has the bit,
+// -row where the last step has it). Each step is tested with the walk's minimum tree; only a
+// step that reaches the target is searched column by column.
+template <int R>
+static __device__ __noinline__ TieScan scan_half(const uint32_t* slot, int owner, int nthreads, int C,
+                                                 uint64_t prank, uint64_t i0, const uint32_t* __restrict__ T2,
+                                                 uint32_t t) {
   constexpr int kW = 16, kH = 1 << R;
-  uint32_t V[kW];
-#pragma unroll
-  for (int k = 0; k < kW / 4; ++k) {
-    const uint4 q = slot[k];
-    V[4 * k] = q.x;
-    V[4 * k + 1] = q.y;
-    V[4 * k + 2] = q.z;
-    V[4 * k + 3] = q.w;
-  }
-  // V += sign * (register row a), the row formed again from M and L (kept out of registers)
-  auto flip = [&](int a, bool up) {
-    const int v = n - C - 1 - a;
-    const int Lv = sL[v];
+  const uint4* s4 = reinterpret_cast<const uint4*>(slot);  // quads 0..3: words; 4 + 4a ..: row a
+  const unsigned rmask = (1u << R) - 1;
+  const unsigned cend = (unsigned)gray_code(i0 + kH - 1) & rmask;
+  TieScan r = {0, ~0ull};
+  for (int L = threadIdx.x & 31; L < kH; L += 32) {
+    const uint64_t i = i0 + L;
+    const unsigned cur = (unsigned)gray_code(i) & rmask;
+    uint32_t V[kW];
 #pragma unroll
     for (int k = 0; k < kW / 4; ++k) {
-      const int qi = k * nthreads + thread;
-      const int4 m0 = rows.quad(v, 2 * qi), m1 = rows.quad(v, 2 * qi + 1);
-      const uint32_t r[4] = {(uint32_t)((m0.y + Lv) * 65536 + (m0.x + Lv)), (uint32_t)((m0.w + Lv) * 65536 + (m0.z + Lv)),
-                             (uint32_t)((m1.y + Lv) * 65536 + (m1.x + Lv)), (uint32_t)((m1.w + Lv) * 65536 + (m1.z + Lv))};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) V[4 * k + e] = up ? V[4 * k + e] + r[e] : V[4 * k + e] - r[e];
+      const uint4 q = s4[k];
+      V[4 * k] = q.x;
+      V[4 * k + 1] = q.y;
+      V[4 * k + 2] = q.z;
+      V[4 * k + 3] = q.w;
     }
-  };
-  // back to the half's first state
-  flip(R - 1, second);
-  unsigned cur = second ? (1u << (R - 1)) : 0u;  // register bits at the half's first state
-  TieScan r = {0, ~0ull};
-  uint32_t tnext = __ldg(T2 + i0);
-  for (int L = 0; L < kH; ++L) {
-    const uint64_t i = i0 + L;
-    const uint32_t tw = tnext;
-    if (L + 1 < kH) tnext = __ldg(T2 + i + 1);
+#pragma unroll
+    for (int a = 0; a < R; ++a) {
+      const unsigned here = (cur >> a) & 1u, last = (cend >> a) & 1u;
+      if (here != last) {
+#pragma unroll
+        for (int k = 0; k < kW / 4; ++k) {
+          const uint4 q = s4[4 + 4 * a + k];
+          const uint32_t rw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) V[4 * k + e] = here ? V[4 * k + e] + rw[e] : V[4 * k + e] - rw[e];
+        }
+      }
+    }
+    const uint32_t tw = __ldg(T2 + i);
     const uint32_t m = __viaddmin_u16x2(pmin_all<kW>(V), tw, 0xffffffffu);
     if ((m & 0xffffu) <= t || (m >> 16) <= t) {
       const uint32_t tv = tw & 0xffffu;
@@ -133,16 +135,11 @@ static __device__ __noinline__ TieScan scan_half(const uint4* slot, RS rows, con
           const uint32_t val = (((V[jj] >> (16 * h)) & 0xffffu) + tv) & 0xffffu;
           if (val == t) {
             const int k = jj >> 2, e = jj & 3;
-            const uint64_t rank = ib | (uint64_t)((((k * nthreads + thread) << 3)) | (e << 1) | h);
+            const uint64_t rank = ib | (uint64_t)((((k * nthreads + owner) << 3)) | (e << 1) | h);
             ++r.cnt;
             r.rmin = rank < r.rmin ? rank : r.rmin;
           }
         }
-    }
-    if (L + 1 < kH) {
-      const int a = __ffs(L + 1) - 1;
-      flip(a, !((cur >> a) & 1u));
-      cur ^= 1u << a;
     }
   }
   return r;
@@ -169,7 +166,6 @@ struct PackedWalker {
   uint32_t aux;   // per half: B + (running best - s), or B + (target - s)
   uint64_t cnt = 0, rmin = ~0ull;  // kModeTiesInt
   uint32_t hq = 0xffffffffu;       // kModeTiesInt: per-half minimum of the current half-iteration
-  RS rows;                         // the unit's rows of M (register rows for scan_half)
   struct RowBuf {
     uint4 q[kPW / 4];
   };
@@ -178,7 +174,6 @@ struct PackedWalker {
     const int t = c.thread, T = c.nthreads, n = c.n, C = c.C;
     s = cP;
     aux = 0xffffffffu;
-    rows = rs;
     const int lt = 31 - __clz(T);
     int Lt = 0;
     for (int b = 0; b < lt; ++b)
@@ -272,17 +267,31 @@ struct PackedWalker {
           const uint32_t t = aux & 0xffffu;
           const bool hit = (hq & 0xffffu) <= t || (hq >> 16) <= t;
           hq = 0xffffffffu;
-          if (__any_sync(0xffffffffu, hit) && hit) {
-            // rare: re-scan the half state by state out of line (keeps the unrolled walk small)
-            uint4* slot = reinterpret_cast<uint4*>(c.scratch) + 4 * c.thread;
+          if (__any_sync(0xffffffffu, hit)) {
+            // rare: the warp re-scans each hitting thread's half out of line, one step per lane
+            // (keeps the unrolled walk small); the counts may land in any lane of the warp, whose
+            // totals are summed at the end of the unit
+            constexpr int kSlot = scan_slot_words<R>();
+            if (hit) {
+              uint4* slot = reinterpret_cast<uint4*>(c.scratch + kSlot * c.thread);
 #pragma unroll
-            for (int k = 0; k < kPW / 4; ++k) slot[k] = make_uint4(V[4 * k], V[4 * k + 1], V[4 * k + 2], V[4 * k + 3]);
+              for (int k = 0; k < kPW / 4; ++k) slot[k] = make_uint4(V[4 * k], V[4 * k + 1], V[4 * k + 2], V[4 * k + 3]);
+#pragma unroll
+              for (int a = 0; a < R; ++a)
+#pragma unroll
+                for (int k = 0; k < kPW / 4; ++k)
+                  slot[4 + 4 * a + k] = make_uint4(Row[a][4 * k], Row[a][4 * k + 1], Row[a][4 * k + 2], Row[a][4 * k + 3]);
+            }
+            __syncwarp();
             constexpr bool second = L == kSteps - 1;
-            const TieScan r = scan_half<R, RS>(slot, rows, c.sL, c.n, c.C, c.thread, c.nthreads, prank,
-                                           base + (second ? kMid : 0), second,
-                                           reinterpret_cast<const uint32_t*>(c.T), t);
-            cnt += r.cnt;
-            rmin = r.rmin < rmin ? r.rmin : rmin;
+            for (unsigned hm = __ballot_sync(0xffffffffu, hit); hm; hm &= hm - 1) {
+              const int owner = (c.thread & ~31) + __ffs(hm) - 1;
+              const TieScan r = scan_half<R>(c.scratch + kSlot * owner, owner, c.nthreads, c.C, prank,
+                                             base + (second ? kMid : 0), reinterpret_cast<const uint32_t*>(c.T), t);
+              cnt += r.cnt;
+              rmin = r.rmin < rmin ? r.rmin : rmin;
+            }
+            __syncwarp();
           }
         }
       }
