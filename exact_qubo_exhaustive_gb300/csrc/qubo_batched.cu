@@ -228,7 +228,10 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
 // lowest rank and the tie count.
 // ------------------------------------------------------------------------------------------------
 constexpr int kBatchTabMaxN = 32;
-constexpr int kPackedTiesR = 5;  // register rows of the packed re-walk of the minimum units
+constexpr int kPackedTiesR = 4;  // register rows of the packed re-walk of the minimum iterations
+static_assert(kPackedTiesR <= kPackedR, "a minimum-pass iteration is a whole number of re-walk iterations");
+constexpr int kBatchMaxWalked = 10;     // walked bits per unit (plan_batched)
+constexpr int kBatchMaxIters = 1 << (kBatchMaxWalked - kPackedR - 1);  // packed iterations per unit
 constexpr int kBatchTabC = 12;
 static_assert(kBatchTabC == 12, "packed::HalfRows splits the cached bits 6 + 6");
 
@@ -244,6 +247,7 @@ struct BatchTables {
   int64_t* S;    // batch            sum |U|
   int32_t* status;
   int32_t* unit_min;  // batch x 2^F
+  int32_t* seg_min;   // batch x 2^F x (packed iterations per unit): packed instances' iteration minima
   int32_t* gmin;
   unsigned long long* grank;
   unsigned long long* gties;
@@ -510,11 +514,12 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   __shared__ int sL[64];
   __shared__ int s_red[32];
   __shared__ __align__(16) int sH[(kBatchTabMaxN - kBatchTabC) * packed::HalfRows::kStride];
+  __shared__ int s_seg[kBatchMaxIters];  // kModeMin: per-iteration minima of the current unit
   const int tid = threadIdx.x, nthreads = blockDim.x;
   const int n = b.n, C = b.C, F = b.F, w = b.w;
   const int ndyn = w - R;
   const uint64_t units = (uint64_t)b.batch << F;
-  const int64_t niter = walk_iterations<R>(w);
+  const int niter = (int)walk_iterations<R>(w);  // <= kBatchMaxIters (plan_batched)
   const int lane = tid & 31, warp = tid >> 5;
   uint32_t* s_words = reinterpret_cast<uint32_t*>(s_rows4);
   int staged = -1;
@@ -559,14 +564,17 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
       staged = g;
     }
     bunit_terms(b.U + (size_t)g * b.su, n, F, P, sL);
+    if (MODE == kModeMin && tid < niter) s_seg[tid] = kIntInf;
     __syncthreads();
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
     c.T = reinterpret_cast<const int*>(b.T2 + (size_t)g * b.st);
     packed::PackedWalker<R, MODE, packed::HalfRows> W;
-    W.init(c, b.Ec + (size_t)g * b.se, rows, cP);
+    // one minimum per iteration of the minimum pass (kPackedR register rows) of the unit
+    int32_t* seg_min = b.seg_min + (size_t)u * walk_iterations<kPackedR>(w);
     if constexpr (MODE == kModeMin) {
-      int best = W.walk(c, niter);
+      W.init(c, b.Ec + (size_t)g * b.se, rows, cP);
+      int best = W.walk(c, 0, niter, 0, s_seg);
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
       if (lane == 0) s_red[warp] = best;
@@ -576,9 +584,20 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
         for (int k = 1; k < (nthreads >> 5); ++k) m = min(m, s_red[k]);
         b.unit_min[u] = m;
       }
+      if (tid < niter) seg_min[tid] = s_seg[tid];
     } else {
-      W.aux = ((uint32_t)((int)packed::kHalfBias + b.gmin[g] - W.s) & 0xffffu) * 0x10001u;
-      W.walk(c, niter, (F > 0) ? (P << (n - F)) : 0);
+      // only the iterations whose minimum is the instance minimum
+      const int gm = b.gmin[g];
+      const uint64_t prank = (F > 0) ? (P << (n - F)) : 0;
+      constexpr int f = 1 << (kPackedR - R);  // re-walk iterations per minimum-pass iteration
+      const int nseg = niter / f;
+      for (int it = 0; it < nseg; ++it) {
+        if (seg_min[it] != gm) continue;
+        W.init(c, b.Ec + (size_t)g * b.se, rows, cP);
+        W.seek(c, it * f);
+        W.aux = ((uint32_t)((int)packed::kHalfBias + gm - W.s) & 0xffffu) * 0x10001u;
+        W.walk(c, it * f, (it + 1) * f, prank);
+      }
       uint64_t cnt = W.cnt, rmin = W.rmin;
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
@@ -647,6 +666,7 @@ BatchTables batch_tables(const BatchPlan& bp, unsigned char* base, size_t* bytes
   t.S = reinterpret_cast<int64_t*>(take(B * 8));
   t.status = reinterpret_cast<int32_t*>(take(B * 4));
   t.unit_min = reinterpret_cast<int32_t*>(take((B << bp.F) * 4));
+  t.seg_min = reinterpret_cast<int32_t*>(take((B << bp.F) * walk_iterations<kPackedR>(bp.w) * 4));
   t.gmin = reinterpret_cast<int32_t*>(take(B * 4));
   t.grank = reinterpret_cast<unsigned long long*>(take(B * 8));
   t.gties = reinterpret_cast<unsigned long long*>(take(B * 8));
@@ -669,9 +689,10 @@ bool plan_batched(int batch, int n, BatchPlan* bp) {
     p.batch = batch;
     p.n = n;
     p.C = kBatchTabC;
-    // units of 2^(n - F) states with at most 9 walked bits (on 4096 x n=24: 8 bits 3.69 ms,
-    // 9 bits 3.59 ms, 10 bits 4.03 ms; fewer bits cost more unit set-ups, more cost the re-walk)
-    p.F = n - p.C - 9 > 0 ? n - p.C - 9 : 0;
+    // units of 2^(n - F) states with at most 10 walked bits (on 4096 x n=24: 9 bits 2.81 ms,
+    // 10 bits 2.69 ms, 11 bits 2.74 ms, 12 bits 3.22 ms per call; fewer bits cost more unit
+    // set-ups, more leave fewer units to balance over the blocks)
+    p.F = n - p.C - kBatchMaxWalked > 0 ? n - p.C - kBatchMaxWalked : 0;
     p.w = n - p.C - p.F;
     p.threads = (1 << p.C) / kFastCPT;
     p.tabled = true;

@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(128, 2) packed_min_kernel(const KParams p) {
     for (int f = 0; f < F; ++f) cP += sL[f];
     PackedWalker<R> W;
     W.init(c, p.Ec, packed::GlobalRows{p.M, 1 << C}, cP);
-    int best = W.walk(c, niter);
+    int best = W.walk(c, 0, niter);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
     if (lane == 0) s_red[warp] = best;

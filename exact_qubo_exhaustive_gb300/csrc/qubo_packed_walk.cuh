@@ -321,25 +321,58 @@ struct PackedWalker {
     }
   }
 
-  // The whole walk of one unit (iterations [0, niter)); returns this thread's best energy
-  // (kModeMin). prank: the unit's prefix bits in rank position (kModeTiesInt).
-  __device__ __forceinline__ int walk(const WalkCtx& c, int64_t niter, uint64_t prank = 0) {
+  // Moves the walk to the first state of iteration it0 (Gray step it0 * 2^(R+1)): there the
+  // register bits are 0 and the shared-row positions hold that step's Gray code bits.
+  __device__ __forceinline__ void seek(const WalkCtx& c, int64_t it0) {
+    const uint64_t g0 = gray_code(static_cast<uint64_t>(it0) << (R + 1));
+    RowBuf rb;
+    for (int a = R; a < c.w; ++a)
+      if ((g0 >> a) & 1u) {
+        load_dyn_row(c, a, rb);
+        apply_dyn_row(c, a, rb, true);
+      }
+  }
+
+  // The walk of iterations [it0, it1) of one unit (from the state `seek` gives); returns this
+  // thread's best energy (kModeMin). prank: the unit's prefix bits in rank position
+  // (kModeTiesInt). With s_seg (kModeMin), the minimum of each iteration over the block goes to
+  // s_seg[iteration] (shared; atomicMin from each warp).
+  __device__ __forceinline__ int walk(const WalkCtx& c, int64_t it0, int64_t it1, uint64_t prank = 0,
+                                      int* s_seg = nullptr) {
     const uint4* T4 = reinterpret_cast<const uint4*>(c.T);
     uint4 tq[kRing];
 #pragma unroll
-    for (int q = 0; q < kRing; ++q) tq[q] = __ldg(T4 + q);
+    for (int q = 0; q < kRing; ++q) tq[q] = __ldg(T4 + (static_cast<uint64_t>(it0) << (R - 1)) + q);
     RowBuf rb;
-    for (int64_t iter = 0; iter < niter; ++iter) {
+    int best = kIntInf;
+    for (int64_t iter = it0; iter < it1; ++iter) {
       const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
-      const bool flip_end = iter + 1 < niter;
+      const bool flip_end = iter + 1 < it1;
       const int a_end = flip_end ? R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1 : R;
       const uint4* tc = T4 + (base >> 2);
       const uint4* tn = T4 + ((flip_end ? base + kSteps : base) >> 2);
       steps<0>(c, prank, base, iter, a_end, tq, tc, tn, rb);
+      if constexpr (MODE == kModeMin) {
+        if (s_seg) {
+          // this iteration's minimum (s is constant from the middle flip to here)
+          const int m = min((int)(aux & 0xffffu), (int)(aux >> 16)) - (int)kHalfBias + s;
+          best = min(best, m);
+          const int wm = __reduce_min_sync(0xffffffffu, m);
+          if ((c.thread & 31) == 0) atomicMin(s_seg + iter, wm);
+        }
+      }
       if (flip_end) {
         const uint64_t ilast = base + kSteps - 1;
         apply_dyn_row(c, a_end, rb, ((gray_code(ilast) >> a_end) & 1u) == 0);
       }
+      if constexpr (MODE == kModeMin) {
+        // a fresh running minimum for the next iteration, set after the flip (the flip's shift
+        // of aux by -L would wrap the all-ones start value)
+        if (s_seg) aux = 0xffffffffu;
+      }
+    }
+    if constexpr (MODE == kModeMin) {
+      if (s_seg) return best;
     }
     const int lo = (int)(aux & 0xffffu) - (int)kHalfBias;
     const int hi = (int)(aux >> 16) - (int)kHalfBias;
