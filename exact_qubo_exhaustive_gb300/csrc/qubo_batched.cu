@@ -219,13 +219,14 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
 
 // ------------------------------------------------------------------------------------------------
 // Table-based pipeline (18 <= n <= kBatchTabMaxN). Every instance gets the energy-component cache
-// of the single-problem search in the workspace (M_int rows, E(U_B), the Gray-ordered walked
-// energies), built for all instances by one grid-stride kernel. Each instance is split into 2^F
-// work units (§III-C1), and persistent minimum passes walk the units of every instance with the
-// same walkers as the single-problem kernels: the packed 16x2 pass, the biased fp32-binade pass
-// or the int32 pass, chosen per instance by its sum |U| (a pass skips the units of instances it
-// does not own). A last pass re-walks only the units that reach their instance's minimum, for the
-// lowest rank and the tie count.
+// of the single-problem search in the workspace (the rows of M_int or their half-subset sums,
+// E(U_B), the Gray-ordered walked energies), built by one kernel with a block per instance. Each
+// instance is split into 2^F work units (§III-C1), and persistent minimum passes walk the units
+// of every instance with the same walkers as the single-problem kernels: the packed 16x2 pass,
+// the biased fp32-binade pass or the int32 pass, chosen per instance by its sum |U| (a pass skips
+// the instances it does not own). A last pass re-walks, for the lowest rank and the tie count,
+// only the parts that reach their instance's minimum: the iterations (packed pass, which records
+// every iteration's minimum) or the units (the other passes).
 // ------------------------------------------------------------------------------------------------
 constexpr int kBatchTabMaxN = 32;
 constexpr int kPackedTiesR = 4;  // register rows of the packed re-walk of the minimum iterations
