@@ -11,8 +11,8 @@
 //     least k states have E <= theta); with fewer than k units, theta grows from the largest
 //     unit minimum until the count reaches k;
 //  3. one collect pass re-walks only the units whose minimum is <= theta and appends every state
-//     with E <= theta; if they fit the candidate buffer, sorting them on the host and keeping k
-//     finishes;
+//     with E <= theta; if they fit the candidate buffer, selecting the k smallest keys on the
+//     host finishes;
 //  4. otherwise (a very degenerate spectrum) count passes bisect theta down to the smallest value
 //     with at least k states, then bisect the rank bound rho inside that energy level, and the
 //     final collect pass returns exactly the k smallest keys.
@@ -175,9 +175,10 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
   if ((e = cudaMemcpyAsync(h.data(), cand, (size_t)c * sizeof(KeyCand), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
       (e = cudaStreamSynchronize(s)) != cudaSuccess)
     return record_cuda_error(e, "candidates");
-  std::sort(h.begin(), h.end(), [](const KeyCand& a, const KeyCand& b) {
-    return a.e != b.e ? a.e < b.e : a.rank < b.rank;
-  });
+  // the `want` smallest keys first (linear-time selection), then only those sorted
+  const auto key_less = [](const KeyCand& a, const KeyCand& b) { return a.e != b.e ? a.e < b.e : a.rank < b.rank; };
+  std::nth_element(h.begin(), h.begin() + (want - 1), h.end(), key_less);
+  std::sort(h.begin(), h.begin() + want, key_less);
   for (uint64_t i = 0; i < want; ++i) {
     out_energies[i] = (double)h[i].e;
     for (int v = 0; v < n; ++v) out_x[i * n + v] = (uint8_t)((h[i].rank >> (n - 1 - v)) & 1u);

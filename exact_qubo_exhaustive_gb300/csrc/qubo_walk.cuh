@@ -237,6 +237,7 @@ struct Walker {
   int col0;     // generic: this thread's column
   // resolve accumulators
   uint64_t cnt, rmin, kmin;
+  int hq = kIntInf;  // resolve modes, fast layout: minimum of (chunk minimum + T) over the current half
 
   // --- set-up: running energies of all columns at walked assignment 0, and register rows.
   __device__ __forceinline__ void init(const WalkCtx& c, const int* __restrict__ Ec, const int* __restrict__ M,
@@ -483,6 +484,40 @@ struct Walker {
   static constexpr int kRing = kQuads < 4 ? kQuads : 4;  // divides kQuads
   static_assert(kQuads % kRing == 0, "the ring must divide an iteration's quads");
 
+  // Resolve modes, fast layout: the warp walks the half-iteration that starts at step i0 once
+  // more, now with the per-step filter and candidate scan (`step`). Over a half only the register
+  // rows flip; their bits follow the reflected Gray code of R bits, from 0 to 2^(R-1) in the
+  // first half and back in the second, so the half's first state is one row away from its last.
+  // The walk ends where it began, at the half's last state. Runs only when a thread of the warp
+  // has a candidate in the half.
+  __device__ __forceinline__ void rescan_half(const WalkCtx& c, uint64_t prank, uint64_t i0, bool second,
+                                           const double* __restrict__ U64, uint64_t gkey) {
+    if constexpr (MODE != kModeMin && CPT >= 4 && R >= 1) {
+      add_reg_row(R - 1, second);
+      unsigned cur = second ? (1u << (R - 1)) : 0u;
+      for (int l = 0; l < kMid; ++l) {
+        const uint64_t i = i0 + l;
+        const int tv = c.t_global ? __ldg(c.T + i) : c.T[i];
+        step(c, prank, i, tv, U64, gkey);
+        if (l + 1 < kMid) {
+          const int a = __ffs(l + 1) - 1;
+          add_reg_row(a, !((cur >> a) & 1u));
+          cur ^= 1u << a;
+        }
+      }
+    }
+  }
+
+  // V += Row[a] (up) or V -= Row[a], for a run-time register position a.
+  __device__ __forceinline__ void add_reg_row(int a, bool up) {
+#pragma unroll
+    for (int b = 0; b < R; ++b)
+      if (b == a) {
+#pragma unroll
+        for (int jj = 0; jj < CPT; ++jj) V[jj] = up ? O::add(V[jj], Row[b][jj]) : O::sub(V[jj], Row[b][jj]);
+      }
+  }
+
   // Steps L.. of one iteration, unrolled by recursion so that every register row index, every
   // flip sign and every prefetch point is a compile-time constant. `tq` is the ring; `tc` points
   // at this iteration's walked energies, `tn` at the next iteration's (or at this one's, on the
@@ -492,7 +527,17 @@ struct Walker {
                                              int a_end, int4* tq, const int4* tc, const int4* tn, RowBuf& rb,
                                              const double* __restrict__ U64, uint64_t gkey) {
     if constexpr (L < kSteps) {
-      step(c, prank, base + L, comp<L & 3>(tq[(L >> 2) % kRing]), U64, gkey);
+      if constexpr (MODE == kModeMin) {
+        step(c, prank, base + L, comp<L & 3>(tq[(L >> 2) % kRing]), U64, gkey);
+      } else {
+        // resolve modes: the minimum pass's work per step, one filter test per half-iteration
+        hq = __viaddmin_s32(vmin_bits<VT, CPT>(V), comp<L & 3>(tq[(L >> 2) % kRing]), hq);
+        if constexpr (L == kMid - 1 || L == kSteps - 1) {
+          const bool hit = hq <= aux;
+          hq = kIntInf;
+          if (__any_sync(0xffffffffu, hit)) rescan_half(c, prank, base + (L == kMid - 1 ? 0 : kMid), L == kSteps - 1, U64, gkey);
+        }
+      }
       if constexpr ((L & 3) == 3) {
         constexpr int q = L >> 2;
         if constexpr (q + kRing < kQuads) tq[q % kRing] = load_t4(c, tc + q + kRing);

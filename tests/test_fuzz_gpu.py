@@ -1,0 +1,78 @@
+"""Seeded random parity sweep: many small problems of every representation against the oracle.
+
+Each trial draws a size, an entry range (packed-narrow, biased, wide int32, non-negative or
+fp32 N(0,1)), a few decoupled variables (zero rows and columns, which multiply the minimum's
+multiplicity), and sometimes an explicit (k_prefix, cache_bits) split; batched trials mix
+instances of different ranges in one call. int32 results must be bit-exact (energy, lowest-rank
+argmin, tie count); fp32 energies within 1e-3 * sum|Q| * 2^-20 with the oracle's argmin.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import qubo_instances as qi
+
+pytestmark = pytest.mark.gpu
+
+O = oracle.get()
+
+
+@pytest.fixture(scope="module")
+def q():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_qubo_exhaustive_gb300 as lib
+    return lib
+
+
+def _instance(rng, n, kind, seed):
+    if kind == "fp32":
+        Q = qi.random_symmetric_normal_f32(n, seed)
+    else:
+        lo, hi = {"narrow": (-int(rng.integers(1, 20)), int(rng.integers(1, 20))), "mid": (-1000, 1000),
+                  "wide": (-(1 << 20), 1 << 20), "pos": (0, 5)}[kind]
+        Q = qi.random_upper_int(n, lo, hi, seed)
+    for v in rng.choice(n, size=int(rng.integers(0, min(4, n) + 1)), replace=False):
+        Q[v, :] = 0
+        Q[:, v] = 0
+    return Q
+
+
+@pytest.mark.parametrize("seed", [1, 2])
+def test_random_single_problems(q, seed):
+    rng = np.random.default_rng(seed)
+    checked = 0
+    while checked < 60:
+        n = int(rng.integers(1, 25))
+        kind = str(rng.choice(["narrow", "mid", "wide", "pos", "fp32"]))
+        Q = _instance(rng, n, kind, int(rng.integers(0, 1 << 30)))
+        kw = {}
+        if rng.random() < 0.4 and n > 2:
+            kw = dict(k_prefix=int(rng.integers(0, n)), cache_bits=int(rng.integers(0, n)))
+        try:
+            e, x, t = q.solve(Q, **kw)
+        except q.QuboError as err:
+            assert kw and err.status == -4, (n, kind, kw, err.status)  # QUBO_ERR_PLAN: infeasible split
+            continue
+        want = O.solve(Q)
+        if kind == "fp32":
+            assert abs(e - want[0]) <= 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+            assert (x == want[1]).all() and t == want[2], (n, kw)
+        else:
+            assert (e, t) == (want[0], want[2]) and (x == want[1]).all(), (n, kind, kw)
+        checked += 1
+
+
+@pytest.mark.parametrize("seed", [3, 4])
+def test_random_batches(q, seed):
+    rng = np.random.default_rng(seed)
+    for _ in range(4):
+        n = int(rng.integers(18, 25))
+        batch = int(rng.integers(1, 12))
+        base = int(rng.integers(0, 1 << 30))
+        Qs = np.stack([_instance(rng, n, str(rng.choice(["narrow", "mid", "pos"])), base + b) for b in range(batch)])
+        e, x, t = q.solve_batched(Qs)
+        for b in range(batch):
+            want = O.solve(Qs[b])
+            assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), (n, b)
