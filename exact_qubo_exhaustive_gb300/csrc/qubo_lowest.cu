@@ -17,6 +17,7 @@
 //     with at least k states, then bisect the rank bound rho inside that energy level, and the
 //     final collect pass returns exactly the k smallest keys.
 #include <algorithm>
+#include <cmath>
 #include <cstring>
 #include <vector>
 
@@ -51,13 +52,27 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
   const uint64_t total_states = (uint64_t)1 << n;
   const uint64_t want = (uint64_t)k < total_states ? (uint64_t)k : total_states;
   // The collect pass re-walks at least `want` whole units, so with the planner's default split
-  // it could re-walk a large share of the states; prefer about 16 units per wanted state when
-  // the kernels can run that split.
+  // it could re-walk a large share of the states. Smaller units cost the minimum pass more unit
+  // set-ups (each worth about 2^18 states of walking). Pick the split that minimises
+  //   ceil(units / blocks) * (S_u + 2^18)  +  kCollectCost * want / blocks * (S_u + 2^18),
+  // with S_u the states per unit; a collect pass costs about 4x a minimum pass per state (its
+  // units hold the candidates, whose half-iterations are walked twice).
   if (k_prefix <= 0) {
-    int F = p.F;
-    while (F < 31 && ((uint64_t)1 << F) < 16 * want) ++F;
-    Plan q;
-    if (F > p.F && plan_whole_problem(n, dtype, F, cache_bits, &q) == QUBO_OK) p = q;
+    constexpr double kSetup = 262144.0, kCollectCost = 4.0;
+    auto cost = [&](const Plan& q) {
+      const double spu = std::ldexp(1.0, n - q.F), blocks = (double)std::max(1, q.blocks);
+      return std::ceil((double)q.total_units / blocks) * (spu + kSetup) + kCollectCost * (double)want / blocks * (spu + kSetup);
+    };
+    double best = cost(p);
+    for (int F = p.F + 1; F <= std::min(31, n); ++F) {
+      Plan q;
+      if (plan_whole_problem(n, dtype, F, cache_bits, &q) != QUBO_OK) continue;
+      const double c = cost(q);
+      if (c < best) {
+        best = c;
+        p = q;
+      }
+    }
   }
   const uint64_t cap = std::max<uint64_t>(2 * want, (uint64_t)1 << 18);
 
