@@ -53,12 +53,14 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
   const uint64_t want = (uint64_t)k < total_states ? (uint64_t)k : total_states;
   // The collect pass re-walks at least `want` whole units, so with the planner's default split
   // it could re-walk a large share of the states. Smaller units cost the minimum pass more unit
-  // set-ups (each worth about 2^18 states of walking). Pick the split that minimises
-  //   ceil(units / blocks) * (S_u + 2^18)  +  kCollectCost * want / blocks * (S_u + 2^18),
-  // with S_u the states per unit; a collect pass costs about 4x a minimum pass per state (its
-  // units hold the candidates, whose half-iterations are walked twice).
+  // set-ups. Pick the split that minimises
+  //   ceil(units / blocks) * (S_u + kSetup)  +  kCollectCost * want / blocks * (S_u + kSetup),
+  // with S_u the states per unit. Measured at n=40: a unit set-up costs about 2^20 states of
+  // walking when blocks run hundreds of units, and the collect pass costs about 1.5x the
+  // minimum pass per state (its units hold the candidates, whose half-iterations are walked
+  // twice).
   if (k_prefix <= 0) {
-    constexpr double kSetup = 262144.0, kCollectCost = 4.0;
+    constexpr double kSetup = 1048576.0, kCollectCost = 1.5;
     auto cost = [&](const Plan& q) {
       const double spu = std::ldexp(1.0, n - q.F), blocks = (double)std::max(1, q.blocks);
       return std::ceil((double)q.total_units / blocks) * (spu + kSetup) + kCollectCost * (double)want / blocks * (spu + kSetup);
@@ -104,9 +106,7 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
     return record_cuda_error(e, "unit minima");
   if (hdr.status != QUBO_OK) return hdr.status;
 
-  std::vector<int32_t> sorted(um);
-  std::sort(sorted.begin(), sorted.end());
-  const int64_t E0 = sorted.front();
+  const int64_t E0 = *std::min_element(um.begin(), um.end());
   const int64_t Smax = hdr.abs_sum;  // every energy lies in [-S, S]
 
   // One pass: count (or collect) the states with key (E, rank) < (theta, rho) over the units
@@ -124,7 +124,13 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
     if ((ee = cudaMemcpyAsync(&w.hdr->tied_count, &nt, 4, cudaMemcpyHostToDevice, s)) != cudaSuccess ||
         (ee = cudaMemsetAsync(counter, 0, 8, s)) != cudaSuccess)
       return record_cuda_error(ee, "pass set-up");
-    if ((ee = run_key_pass(p, kp, mode, (int)theta, rho, cand, (uint32_t)cap, counter, s)) != cudaSuccess)
+    // split each listed unit into just enough segments to give every block a few items (the
+    // plan's split is for a single tied unit; every segment pays a unit set-up)
+    KParams kps = kp;
+    int seg = 0;
+    while (seg < p.seg_bits && ((uint64_t)nt << seg) < 4 * (uint64_t)p.blocks) ++seg;
+    kps.seg_bits = seg;
+    if ((ee = run_key_pass(p, kps, mode, (int)theta, rho, cand, (uint32_t)cap, counter, s)) != cudaSuccess)
       return record_cuda_error(ee, "kernel launch");
     ++launches;
     unsigned long long c = 0;
@@ -137,7 +143,14 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
   const uint64_t kAllRanks = ~0ull;
 
   // 2. an upper threshold with at least `want` states at or below it
-  int64_t theta = (p.total_units >= want) ? sorted[want - 1] : sorted.back();
+  int64_t theta;
+  if (p.total_units >= want) {  // the want-th smallest unit minimum (linear-time selection)
+    std::vector<int32_t> sel(um);
+    std::nth_element(sel.begin(), sel.begin() + (want - 1), sel.end());
+    theta = sel[want - 1];
+  } else {
+    theta = *std::max_element(um.begin(), um.end());
+  }
   uint64_t c = 0;
   if ((st = pass(kModeCollectKey, theta, kAllRanks, &c))) return st;
   int64_t lo = E0 - 1;  // count(E <= lo) = 0 < want
