@@ -15,7 +15,8 @@
 // variables) is the bias row; the remaining walked variables are visited in Gray order (§III-B,
 // eq. 9), so each step adds one row of M_int to V on the CUDA cores and issues one MMA.
 // The accumulator lives in tensor memory (two buffers: the tensor core fills one while the CUDA
-// cores reduce the other with 3-input fp32 minima: half an ALU instruction per state); the
+// cores reduce the other with 3-input integer minima on the accumulator bits, which the bias
+// offset kTcOffset keeps non-negative: half an ALU instruction per state); the
 // walked self energy of each row, in Gray order (§IV-B.3), is added once per row after the
 // column minimum.
 #include <cuda_fp16.h>
@@ -27,6 +28,11 @@ namespace qgb {
 
 namespace {
 constexpr uint32_t kTmemCols = 512;            // two 128 x 256 fp32 accumulators
+// Added to every column bias: with sum |U| <= 2^21 every accumulator value D = (partial energy)
+// + 2^21 lies in [0, 2^22], a non-negative float whose bit pattern orders like its value, so the
+// column minimum runs as 3-input integer minima on the raw accumulator bits.
+constexpr int kTcOffset = 1 << 21;
+static_assert(kTcMaxAbsSum <= kTcOffset, "accumulators must stay non-negative");
 constexpr uint32_t kIdesc = tc::idesc_f16_f32(128, 256);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: an MMA takes ~0.1 us
 
@@ -207,7 +213,7 @@ __global__ void __launch_bounds__(kBlock, 1) tc_min_kernel(const KParams p, int 
 #pragma unroll
     for (int b = 0; b < kTcC; ++b)
       if ((col >> b) & 1) v0 += sL[n - 1 - b];
-    float Vn = (float)v0;
+    float Vn = (float)(v0 + kTcOffset);
     {
       uint32_t slot = gslot;
       for (int64_t i = 0; i < 3 && i < ntiles; ++i) {
@@ -255,11 +261,19 @@ __global__ void __launch_bounds__(kBlock, 1) tc_min_kernel(const KParams p, int 
         }
       }
       __syncwarp();
-      float m[4] = {__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]), __uint_as_float(v[3])};
+      // 3-input integer minima on the bit patterns (non-negative floats below 2^31 as integers
+      // order like their values): 8 independent chains, chain k over v[k + 8 j], j = 0..15, in
+      // 7 three-input and 1 two-input minima; about one ALU instruction per two states
+      int m[8];
 #pragma unroll
-      for (int c = 4; c < 128; c += 2)  // 3-input minima: one ALU instruction per two states
-        m[(c >> 1) & 3] = fminf(fminf(m[(c >> 1) & 3], __uint_as_float(v[c])), __uint_as_float(v[c + 1]));
-      const int rmin = __float2int_rn(fminf(fminf(m[0], m[1]), fminf(m[2], m[3])));
+      for (int k = 0; k < 8; ++k) {
+        int a = __vimin3_s32((int)v[k], (int)v[k + 8], (int)v[k + 16]);
+#pragma unroll
+        for (int j = 3; j < 15; j += 2) a = __vimin3_s32(a, (int)v[k + 8 * j], (int)v[k + 8 * j + 8]);
+        m[k] = min(a, (int)v[k + 120]);
+      }
+      const int mb = min(__vimin3_s32(m[0], m[1], m[2]), __vimin3_s32(m[3], m[4], __vimin3_s32(m[5], m[6], m[7])));
+      const int rmin = __float2int_rn(__int_as_float(mb)) - kTcOffset;
       best = min(best, rmin + t_cur + Lrow + s);
       if (i + 1 < ntiles) {  // offset of the next tile: its Gray flip's linear term
         const int h = __ffsll((long long)(i + 1)) - 1;
