@@ -264,11 +264,13 @@ __device__ __forceinline__ int batch_class(int64_t S) {
 }
 
 // Fold, range check and caches of every instance (the single-problem tables, §II-C Table I), one
-// block per instance. The C cached bits split into a low half (lo bits) and a high half; with the partial sums of the
-// halves in shared memory every table entry is a few adds:
+// block per instance. The C cached bits split into a low half (lo bits) and a high half, and the w
+// walked bits likewise; with the partial sums of the halves in shared memory every table entry
+// is a few adds:
 //   M[v][j] = A_v[j_lo] + B_v[j_hi]                         (A, B: subset sums of U[v][cached])
 //   E(U_B)[j] = El[j_lo] + Eh[j_hi] + sum_{b in j_lo} Y[j_hi][b]   (Y: coupling of a high subset
 //                                                                   to low bit b)
+//   T[i] = Tl[g_lo] + Th[g_hi] + sum_{a in g_lo} TY[g_hi][a]       (g = gray(i), walked bits)
 constexpr int kBatchMaxHalf = 64;  // 2^(C/2) for C = kBatchTabC
 
 __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
@@ -277,9 +279,13 @@ __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
   __shared__ int sB[kBatchTabMaxN][kBatchMaxHalf];
   __shared__ int sEl[kBatchMaxHalf], sEh[kBatchMaxHalf];
   __shared__ int sY[kBatchMaxHalf][kBatchTabC / 2];
+  // the walked bits split the same way: wl low positions, wh high ones
+  __shared__ int sTl[1 << (kBatchMaxWalked / 2)], sTh[1 << (kBatchMaxWalked - kBatchMaxWalked / 2)];
+  __shared__ int sTY[1 << (kBatchMaxWalked - kBatchMaxWalked / 2)][kBatchMaxWalked / 2];
   __shared__ unsigned long long s_sum;
   const int g = blockIdx.x, tid = threadIdx.x, nt = blockDim.x;
   const int n = b.n, C = b.C, w = b.w;
+  const int wl = w / 2, wh = w - wl;  // w <= kBatchMaxWalked (plan_batched)
   const int lo = C / 2, hi = C - lo;
   const int nlo = 1 << lo, nhi = 1 << hi;
   // U = the folded triangle of Q and S = sum |U|; the instance is searched when S fits int32
@@ -352,6 +358,27 @@ __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
       sY[h][k] = acc;
     }
   }
+  // walked position a is variable n - C - 1 - a (a = 0 flips fastest)
+  for (int idx = tid; idx < (1 << wl) + (1 << wh) + (1 << wh) * wl; idx += nt) {
+    int acc = 0;
+    if (idx < (1 << wl) + (1 << wh)) {  // energy of a low (or high) subset of walked positions alone
+      const int base = idx < (1 << wl) ? 0 : wl, nb = idx < (1 << wl) ? wl : wh;
+      const int sub = idx < (1 << wl) ? idx : idx - (1 << wl);
+      for (int k1 = 0; k1 < nb; ++k1) {
+        if (!((sub >> k1) & 1)) continue;
+        const int va = n - C - 1 - (base + k1);
+        for (int k2 = k1; k2 < nb; ++k2)
+          if ((sub >> k2) & 1) acc += sU[(n - C - 1 - (base + k2)) * n + va];
+      }
+      if (idx < (1 << wl)) sTl[sub] = acc;
+      else sTh[sub] = acc;
+    } else {  // coupling of high subset h to low position a
+      const int r = idx - (1 << wl) - (1 << wh), h = r / wl, a = r - h * wl;
+      for (int k = 0; k < wh; ++k)
+        if ((h >> k) & 1) acc += sU[(n - C - 1 - (wl + k)) * n + (n - C - 1 - a)];
+      sTY[h][a] = acc;
+    }
+  }
   __syncthreads();
   const int ncols = 1 << C;
   if (batch_class(S) == kBatchPacked) {
@@ -380,13 +407,10 @@ __global__ void __launch_bounds__(256) btables_kernel(BatchTables b) {
   uint32_t* T2 = b.T2 + (size_t)g * b.st;
   for (int i = tid; i < (1 << w); i += nt) {
     const unsigned gc = (unsigned)(i ^ (i >> 1));
-    int acc = 0;
-    for (int a = 0; a < w; ++a) {
-      if (!((gc >> a) & 1u)) continue;
-      const int va = n - C - 1 - a;
-      for (int c2 = a; c2 < w; ++c2)
-        if ((gc >> c2) & 1u) acc += sU[(n - C - 1 - c2) * n + va];
-    }
+    const int l = (int)(gc & ((1u << wl) - 1)), h = (int)(gc >> wl);
+    int acc = sTl[l] + sTh[h];
+    for (int a = 0; a < wl; ++a)
+      if ((l >> a) & 1) acc += sTY[h][a];
     T[i] = acc;
     T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
   }
