@@ -76,3 +76,16 @@ def test_random_batches(q, seed):
         for b in range(batch):
             want = O.solve(Qs[b])
             assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), (n, b)
+
+
+@pytest.mark.parametrize("seed", [5])
+def test_random_lowest_spectra(q, seed):
+    # the k lowest (energy, rank) keys, bit-exact against the oracle's sorted top-k
+    rng = np.random.default_rng(seed)
+    for _ in range(20):
+        n = int(rng.integers(2, 21))
+        Q = _instance(rng, n, str(rng.choice(["narrow", "mid", "pos"])), int(rng.integers(0, 1 << 30)))
+        k = int(rng.integers(1, 400))
+        e, x = q.solve_lowest(Q, k)
+        we, wx = O.lowest(Q, k)
+        assert np.array_equal(e, we) and np.array_equal(x, wx), (n, k)
