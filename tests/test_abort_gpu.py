@@ -59,7 +59,15 @@ def test_abort_keeps_checkpointed_progress(q, tmp_path):
     Q = qi.random_upper_int(42, -1000, 1000, 42)
     path = str(tmp_path / "run.ckpt")
     th, out = run_in_thread(lambda: q.solve_checkpointed(Q, 7, path, slices_per_chunk=2))
-    time.sleep(0.1)
+    # abort as soon as a chunk is on disk (no fixed sleep: a slow start cannot make it early)
+    deadline = time.perf_counter() + 30
+    while time.perf_counter() < deadline and th.is_alive():
+        try:
+            if q.checkpoint_read(path)["next_slice"] > 0:
+                break
+        except q.QuboError:
+            pass  # no chunk written yet
+        time.sleep(0.002)
     q.request_abort()
     th.join(timeout=30)
     assert isinstance(out.get("error"), q.QuboError) and out["error"].status == -7
