@@ -231,7 +231,7 @@ __global__ void __launch_bounds__(256, 1) batched_kernel(int n, int C, const int
 constexpr int kBatchTabMaxN = 32;
 constexpr int kPackedTiesR = 4;  // register rows of the packed re-walk of the minimum iterations
 static_assert(kPackedTiesR <= kPackedR, "a minimum-pass iteration is a whole number of re-walk iterations");
-constexpr int kBatchMaxWalked = 10;     // walked bits per unit (plan_batched)
+constexpr int kBatchMaxWalked = 11;     // walked bits per unit (plan_batched)
 constexpr int kBatchMaxIters = 1 << (kBatchMaxWalked - kPackedR - 1);  // packed iterations per unit
 constexpr int kBatchTabC = 12;
 static_assert(kBatchTabC == 12, "packed::HalfRows splits the cached bits 6 + 6");
@@ -714,9 +714,10 @@ bool plan_batched(int batch, int n, BatchPlan* bp) {
     p.batch = batch;
     p.n = n;
     p.C = kBatchTabC;
-    // units of 2^(n - F) states with at most 10 walked bits (on 4096 x n=24: 9 bits 2.81 ms,
-    // 10 bits 2.69 ms, 11 bits 2.74 ms, 12 bits 3.22 ms per call; fewer bits cost more unit
-    // set-ups, more leave fewer units to balance over the blocks)
+    // units of 2^(n - F) states with at most 11 walked bits (on 4096 x n=24: 10 bits 2.63 ms,
+    // 11 bits 2.59 ms per call; earlier, with slower tables, 9 bits 2.81, 10 bits 2.69, 11 bits
+    // 2.74, 12 bits 3.22 ms; fewer bits cost more unit set-ups, more leave fewer units to
+    // balance over the blocks)
     p.F = n - p.C - kBatchMaxWalked > 0 ? n - p.C - kBatchMaxWalked : 0;
     p.w = n - p.C - p.F;
     p.threads = (1 << p.C) / kFastCPT;

@@ -428,11 +428,11 @@ def test_batched_mixed_passes_against_oracle(q):
 
 
 def test_batched_packed_ties_across_steps_halves_and_columns(q):
-    # n = 24 instances of the packed pass (12 cached bits, 2 prefix bits, 10 walked bits) with
+    # n = 24 instances of the packed pass (12 cached bits, 1 prefix bit, 11 walked bits) with
     # variables whose couplings are all zero: each doubles the minimum's multiplicity, and the
     # tied states then differ in a register-row bit (x_7..x_11 in the minimum pass, x_8..x_11 in
     # the re-walk), a shared row flipped mid-iteration (x_6, or x_7 in the re-walk), a row
-    # flipped between iterations (x_2..x_5), a cached bit (x_12..x_23) or a prefix bit (x_0, x_1)
+    # flipped between iterations (x_1..x_5), a cached bit (x_12..x_23) or the prefix bit (x_0)
     n = 24
     free_sets = [(1, 6, 9, 20), (4, 11), (7,), (0, 3, 5, 8, 10, 12, 23), ()]
     Qs = []
@@ -453,7 +453,7 @@ def test_batched_packed_ties_across_steps_halves_and_columns(q):
 
 @pytest.mark.parametrize("n,batch", [(18, 40), (21, 12), (28, 2)])
 def test_batched_sizes_and_unit_splits(q, n, batch):
-    # n = 18, 21: one unit per instance; n = 28: 2^6 units per instance
+    # n = 18, 21: one unit per instance; n = 28: 2^5 units per instance
     Qs = qi.batched_upper_int(batch, n, -60, 60, 520 + n)
     e, x, t = q.solve_batched(Qs)
     for b in range(batch):
