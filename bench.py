@@ -15,8 +15,14 @@ record) through the library's C ABI.
   cpu_baseline / --impl reference: the CPU oracle (test infrastructure, plain C + OpenMP) on a
           bounded sample of the same workload, on the host's cores.
 
-Multi-GPU (torchrun, one process per GPU): weak scaling -- every rank solves its own independent
-n=40 instance (independent problems need no exchange); value counts the states of all ranks.
+Multi-GPU (torchrun, one process per GPU): ONE n=40 search sharded over the ranks (§III-C1 and
+§IV-C of the paper: the 2^12 slices of the first 12 variables are independent subproblems, and each
+GPU builds its own caches). Rank i searches its contiguous share of the slices
+(qubo_solve_slice_range_device), then one all-gather of the 32-byte result records is the only
+exchange; value = 2^40 / the slowest rank's step time (strong scaling: the total work is fixed).
+
+Every run checks the answer it timed against the stored full oracle search of the workload
+(tests/golden/full_oracle_n40_int32.txt) and exits non-zero on a mismatch.
 """
 from __future__ import annotations
 
@@ -49,8 +55,44 @@ PROFILE = os.path.join(ROOT, "profiles", "search_kernel_n40.md")
 KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_fast.cu", "qubo_internal.h"]
 
 
+SHARD_K = 12                 # slices of the multi-GPU split: 2^12, divisible by 1, 2, 4 and 8 ranks
+
+
 def log(*a):
     print(*a, file=sys.stderr, flush=True)
+
+
+def golden(name: str):
+    """(E_min, rank of the lowest-rank minimiser, ties) stored by the full oracle search of a workload."""
+    path = os.path.join(ROOT, "tests", "golden", f"full_oracle_{name}.txt")
+    with open(path) as f:
+        row = [ln.split() for ln in f if ln.strip() and not ln.startswith("#")][0]
+    e = float(row[0]) if ("." in row[0] or "e" in row[0]) else int(row[0])
+    return e, int(row[1]), int(row[2])
+
+
+class ResultMismatch(RuntimeError):
+    pass
+
+
+def check_result(name: str, e, rank: int, ties: int, tol: float = 0.0) -> str:
+    """Compares a timed search's answer with the stored full oracle search; raises on a mismatch."""
+    ge, grank, gties = golden(name)
+    if abs(float(e) - float(ge)) > tol or int(rank) != grank or int(ties) != gties:
+        raise ResultMismatch(f"{name}: got ({e}, {rank}, {ties}), full oracle search gave ({ge}, {grank}, {gties})")
+    return "matches the full oracle search"
+
+
+def combine_gathered(raw: bytes, world: int, result_dtype):
+    """Reduces the per-rank result records of one sharded step (the bytes of an all-gather of
+    `world` qubo_result records): lowest energy; among equal energies the lowest rank and the summed
+    tie counts. Raises if a rank reports an error status."""
+    from exact_qubo_exhaustive_gb300.distributed import combine
+    recs = np.frombuffer(raw, dtype=result_dtype)
+    assert recs.shape[0] == world, (recs.shape, world)
+    if (recs["status"] != 0).any():
+        raise RuntimeError(f"a shard failed: statuses {recs['status'].tolist()}")
+    return combine((float(r["min_energy"]), int(r["argmin_rank"]), int(r["tie_count"])) for r in recs)
 
 
 def dist_env():
@@ -213,7 +255,7 @@ def run_reference(args):
     sample = f"each step: {per_step} slices x 2^{N - k} states of the n=40 workload; CPU oracle, all host threads"
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3 / args.steps,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int64",
+            "higher_is_better": True, "scaling": "strong", "vs_baseline": None, "dtype": "int64",
             "data": "synthetic", "config": config_dict(),
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": O.num_threads(), "kind": "oracle",
                              "sample": sample},
@@ -235,14 +277,13 @@ def max_over_ranks(values, device):
 def run_gb300(args):
     import torch
     rank, world, local = dist_env()
+    if world > 1:
+        return run_gb300_sharded(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
     import exact_qubo_exhaustive_gb300 as q
 
-    Q = qi.workload_n40() if rank == 0 else qi.random_upper_int(N, -1000, 1000, qi.MASTER_SEED + 2 + 7919 * rank)
+    Q = qi.workload_n40()
     plan = q.plan(N)
     dq = torch.from_numpy(Q).to(dev)
     nbytes = q.workspace_bytes(N)
@@ -288,6 +329,8 @@ def run_gb300(args):
     r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
     if int(r["status"]) != 0:
         raise RuntimeError(f"search failed: status {int(r['status'])}")
+    checks = {"n40_int32": check_result("n40_int32", float(r["min_energy"]), int(r["argmin_rank"]),
+                                        int(r["tie_count"]))}
 
     # end to end through the host API, from pinned host memory
     pinned = torch.empty((N, N), dtype=torch.int32, pin_memory=True)
@@ -299,15 +342,13 @@ def run_gb300(args):
         flush.fill_(i & 0xFF)
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        q.solve(Qh)
+        he, hx, ht = q.solve(Qh)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
     e2e = sum(e2e_ms) / len(e2e_ms)
+    checks["n40_int32_host_api"] = check_result("n40_int32", he, int("".join(map(str, hx)), 2), ht)
 
-    if world > 1:
-        ms, e2e, kern = max_over_ranks([ms, e2e, kern], dev)
-
-    value = world * STATES / (ms * 1e-3)
-    e2e_value = world * STATES / (e2e * 1e-3)
+    value = STATES / (ms * 1e-3)
+    e2e_value = STATES / (e2e * 1e-3)
     achieved = STATES / (kern * 1e-3) / 1e12  # int32 adds (one per state) per second, in T/s
     peak = SMS * LANES_PER_CLK * MAX_SM_MHZ * 1e6 / 1e12
     # the measured INT32-add roofline: the best int32 add throughput of the add microbenchmark
@@ -319,42 +360,139 @@ def run_gb300(args):
     traffic, traffic_src = profiled_traffic()
 
     extra = {}
-    if rank == 0 and world == 1 and not args.no_extra:
+    if not args.no_extra:
         extra = other_configs(q, torch, dev, stream)
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu:
+    if not args.no_cpu:
         cpu = oracle_sample(args.cpu_seconds)
 
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
+        "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded uniform integers, no dataset)",
+        "config": config_dict(plan),
+        "result": {"min_energy": float(r["min_energy"]), "argmin_rank": int(r["argmin_rank"]),
+                   "tie_count": int(r["tie_count"]), "checks": checks},
+        "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "search_kernel<16,5,min,biased> (enumeration, biased fp32-binade minimum pass)", "kernel_ms": kern,
+                     "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
+                                   "add per state) x 2.07 GHz max SM clock",
+                     "traffic_source": traffic_src,
+                     "measured_int32_add_peak": r_int,
+                     "frac_of_measured_int32_add": achieved / r_int,
+                     "measured_int32_add_basis": (f"qubo_probe_alu int32 add chains: {best_ops / (SMS * probe_mhz * 1e6):.1f} "
+                                                  f"lanes/clk/SM at {probe_mhz:.0f} MHz x {SMS} SMs"),
+                     "frac_at_measured_clock": (achieved / (SMS * LANES_PER_CLK * clocks["sm_mhz"] * 1e-6)
+                                                if clocks.get("sm_mhz") else None)},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": N * N * 4,
+                "d2h_bytes_per_step": 32, "ms_per_step": e2e},
+        "cpu_baseline": cpu,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+        "other_configs": extra,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gb300_sharded(args):
+    """N > 1: one n=40 search sharded over the ranks by contiguous ranges of its 2^SHARD_K slices."""
+    import torch
+    import torch.distributed as dist
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist.init_process_group("nccl", device_id=dev)
+    import exact_qubo_exhaustive_gb300 as q
+    from exact_qubo_exhaustive_gb300 import distributed as qd
+
+    Q = qi.workload_n40()
+    first, count = qd.shard_range(1 << SHARD_K, rank, world)
+    dq = torch.from_numpy(Q).to(dev)
+    nbytes = max(q.slice_range_workspace_bytes(N, q.INT32, SHARD_K, count), 256)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    res = torch.zeros(32, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    q.enable_kernel_timing(True)
+
+    def step(out):
+        q.solve_slice_range_device(N, dq, q.INT32, SHARD_K, first, count, ws, nbytes, stream.cuda_stream, res)
+        dist.all_gather_into_tensor(out, res)  # the one exchange: 32 bytes per rank
+
+    scratch = torch.empty(world * 32, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        step(scratch)
+    torch.cuda.synchronize()
+    launches_per_step = q.last_launch_count()
+    gathered = [torch.empty(world * 32, dtype=torch.uint8, device=dev) for _ in range(args.steps)]
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    props = torch.cuda.get_device_properties(dev)
+    gpu_id = f"GPU-{props.uuid}" if getattr(props, "uuid", None) else str(local)
+    kernel_ms = []
+    dist.barrier()
+    torch.cuda.synchronize()
+    sampler = ClockSampler(gpu_id)
+    time.sleep(0.3)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step(gathered[i])
+        ends[i].record(stream)
+        kernel_ms.append(q.kernel_time_ms())
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = sampler.stop()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends)) / args.steps
+    kern = sum(kernel_ms) / len(kernel_ms)
+    checks = {}
+    for i, g in enumerate(gathered):
+        e, r, t = combine_gathered(g.cpu().numpy().tobytes(), world, q.RESULT_DTYPE)
+        checks["sharded_step"] = check_result("n40_int32", e, r, t)
+
+    # end to end through the public sharded API: host Q per rank, host result, one all-gather
+    qd.solve_distributed(Q, SHARD_K)
+    e2e_ms = []
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        torch.cuda.synchronize()
+        dist.barrier()
+        t0 = time.perf_counter()
+        he, hx, ht = qd.solve_distributed(Q, SHARD_K)
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+    e2e = sum(e2e_ms) / len(e2e_ms)
+    checks["solve_distributed"] = check_result("n40_int32", he, int("".join(map(str, hx)), 2), ht)
+    ms, e2e, kern_max = max_over_ranks([ms, e2e, kern], dev)
+    rank_states = count << (N - SHARD_K)
+    achieved = rank_states / (kern * 1e-3) / 1e12
+    peak = SMS * LANES_PER_CLK * MAX_SM_MHZ * 1e6 / 1e12
     if rank == 0:
+        cfg = config_dict()
+        cfg.update({"parallelism": f"slice shards x{world}", "shard_k_prefix": SHARD_K,
+                    "slices_per_rank": count})
         line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "metric": METRIC, "value": STATES / (ms * 1e-3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "strong",
             "vs_baseline": None, "dtype": "int32", "data": "synthetic (seeded uniform integers, no dataset)",
-            "config": config_dict(plan),
-            "result": {"min_energy": float(r["min_energy"]), "argmin_rank": int(r["argmin_rank"]),
-                       "tie_count": int(r["tie_count"])},
+            "config": cfg,
+            "result": {"min_energy": float(he), "argmin_rank": int("".join(map(str, hx)), 2), "tie_count": int(ht),
+                       "checks": checks},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
-                         "frac": achieved / peak, "traffic": traffic,
-                         "kernel": "search_kernel<16,5,min,biased> (enumeration, biased fp32-binade minimum pass)", "kernel_ms": kern,
-                         "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
-                                       "add per state) x 2.07 GHz max SM clock",
-                         "traffic_source": traffic_src,
-                         "measured_int32_add_peak": r_int,
-                         "frac_of_measured_int32_add": achieved / r_int,
-                         "measured_int32_add_basis": (f"qubo_probe_alu int32 add chains: {best_ops / (SMS * probe_mhz * 1e6):.1f} "
-                                                      f"lanes/clk/SM at {probe_mhz:.0f} MHz x {SMS} SMs"),
-                         "frac_at_measured_clock": (achieved / (SMS * LANES_PER_CLK * clocks["sm_mhz"] * 1e-6)
-                                                    if clocks.get("sm_mhz") else None)},
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": N * N * 4,
-                    "d2h_bytes_per_step": 32, "ms_per_step": e2e},
-            "cpu_baseline": cpu,
+                         "frac": achieved / peak, "traffic": None,
+                         "kernel": "search_kernel<16,5,min,biased> on rank 0's shard", "kernel_ms": kern,
+                         "kernel_ms_max_over_ranks": kern_max,
+                         "peak_basis": "152 SMs x 128 lanes/clk x 2.07 GHz max SM clock"},
+            "e2e": {"value": STATES / (e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": world * N * N * 4,
+                    "d2h_bytes_per_step": world * 32, "ms_per_step": e2e,
+                    "api": "exact_qubo_exhaustive_gb300.distributed.solve_distributed"},
+            "cpu_baseline": None,
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
-            "other_configs": extra,
         }
         print(json.dumps(line), flush=True)
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    dist.destroy_process_group()
     return 0
 
 
@@ -385,6 +523,11 @@ def other_configs(q, torch, dev, stream):
         kern = q.kernel_time_ms()
         out[name] = {"ms": ms, "states_per_s": (1 << n) / (ms * 1e-3), "min_pass_ms": kern,
                      "min_pass_states_per_s": (1 << n) / (kern * 1e-3) if kern > 0 else None}
+        if name == "n36_fp32":
+            r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
+            tol = 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+            out[name]["check"] = check_result("n36_fp32", float(r["min_energy"]), int(r["argmin_rank"]),
+                                              int(r["tie_count"]), tol)
         if name == "n40_narrow_int32":
             out[name]["workload"] = ("n=40 dense QUBO, int32 upper-triangular, entries uniform in [-4,4] "
                                      "(sum |U| = 1822: the packed 16x2 minimum pass)")
@@ -493,7 +636,11 @@ def main(argv=None):
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
-    return run_gb300(args)
+    try:
+        return run_gb300(args)
+    except ResultMismatch as exc:
+        log(f"RESULT MISMATCH: {exc}")
+        return 1
 
 
 if __name__ == "__main__":

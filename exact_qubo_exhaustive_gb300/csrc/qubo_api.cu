@@ -155,14 +155,6 @@ constexpr double kMaxUnits = 2147483648.0;
 // Problems with at least this many variables also launch the packed and biased minimum passes.
 constexpr int kNarrowPassesMinN = 30;
 
-// QUBO_TENSOR_CORES=1 in the environment selects the tensor-core minimum pass where it applies.
-// It is exact and tested, but on this part its per-tile commit round trip keeps it below the
-// CUDA-core pass, so the CUDA-core pass is the default.
-bool tensor_cores_enabled() {
-  const char* v = getenv("QUBO_TENSOR_CORES");
-  return v && v[0] == '1';
-}
-
 bool fast_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
   const int w = n - F - C;
   if (C < 9 || C > 12 || F < 0 || w < kFastR + 1 || w > kMaxWalkedBits) return false;
@@ -289,15 +281,6 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
       p.packed = true;
       p.packed_blocks = std::max(1, di.sms) * pocc;
     }
-  }
-  // Tensor-core minimum pass for int32 input on sm_10x: the split needs >= 8 walked bits
-  // (7 MMA row bits + at least one Gray-walked bit) and a Gray table of at most 2^24 entries.
-  const int w8 = n - p.F - kTcC;
-  if (p.variant == kFast && dtype == QUBO_INT32 && tensor_cores_enabled() && di.cc_major == 10 &&
-      w8 >= kTcRowBits + 1 && w8 <= kMaxWalkedBits && tc_smem_bytes(w8) + 1024 <= di.smem_optin) {
-    p.tc = true;
-    p.w8 = w8;
-    p.tc_blocks = std::max(1, di.sms);
   }
   *out = p;
   return QUBO_OK;
@@ -685,7 +668,6 @@ int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* ou
   out->units = p.total_units;
   out->workspace_bytes = layout_workspace(p, nullptr).bytes;
   out->smem_bytes = p.smem_bytes;
-  out->tensor_cores = p.tc ? 1 : 0;
   out->packed = p.packed ? 1 : 0;
   out->biased = p.biased ? 1 : 0;
   return QUBO_OK;

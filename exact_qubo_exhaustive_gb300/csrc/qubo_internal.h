@@ -32,11 +32,6 @@ constexpr int kIntMinR = 5;  // register rows of the int32 minimum pass (the res
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 
-// Tensor-core minimum pass: 8 cached variables (256 MMA columns), 7 row variables (128 MMA rows).
-constexpr int kTcC = 8;
-constexpr int kTcRowBits = 7;
-constexpr int kTcThreads = 256;
-constexpr int64_t kTcMaxAbsSum = int64_t(1) << 21;  // every MMA operand piece and partial sum exact
 // Biased fp32 minimum walk: every running column energy is a sum of distinct U entries, so
 // |V| <= sum |U| < 2^22 keeps 1.5 * 2^23 + V inside the binade [2^23, 2^24).
 constexpr int64_t kBiasedWalkMaxAbsSum = (int64_t(1) << 22) - 1;
@@ -80,14 +75,11 @@ struct Plan {
   size_t smem_bytes = 0;   // dynamic shared memory of the enumeration kernels
   bool host_gbase = false; // group bases uploaded by the host (else one group, written on device)
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
-  bool tc = false;         // tensor-core minimum pass (int32, sum |U| <= kTcMaxAbsSum)
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
   int packed_threads = 0;  // 2^C / 32
   int packed_blocks = 0;
   size_t packed_smem = 0;
-  int w8 = 0;              // walked bits of the tensor-core split: n - F - kTcC
-  int tc_blocks = 0;       // grid of the tensor-core pass (one block per SM)
 };
 
 // Device pointers into one workspace.
@@ -107,9 +99,6 @@ struct Work {
   uint64_t* gties = nullptr;
   uint64_t* gkey = nullptr;
   qubo_result* results = nullptr;  // one per group
-  int32_t* M8 = nullptr;   // tensor-core split: (n - 8) x 256 interaction rows
-  int32_t* E8 = nullptr;   // 256 cached self energies
-  int32_t* T8 = nullptr;   // 2^w8 walked self energies, [Gray step][row]
   size_t bytes = 0;
 };
 

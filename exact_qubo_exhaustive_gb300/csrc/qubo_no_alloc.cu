@@ -14,6 +14,14 @@
 // rewrites the header (status, band, tied-unit count), and every table and accumulator after it
 // is written before it is read. Two calls whose work overlaps on the GPU (two streams, or two
 // host threads) race on the array; order them on one stream.
+//
+// The array's device address belongs to the CUDA context the module was loaded into. It is
+// looked up (cudaGetSymbolAddress) on the first call in a context and kept together with that
+// context's unique id; a call from another context (after cudaDeviceReset, or under a context the
+// caller created with the driver API) looks it up again. Make the first call in each context
+// before any stream capture.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "qubo_internal.h"
@@ -23,21 +31,67 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_no_alloc_scratch[QUBO_NO_ALLOC_SCRATCH_BYTES];
 
-std::mutex g_setup_mu;
-void* g_scratch_ptr[64] = {nullptr};  // device address of the array, per device
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
 
-// Device address of the scratch array on device `dev` (which must be current). In host code the
-// array's name is only a stand-in, so the address is looked up once per device.
+struct ScratchSlot {
+  unsigned long long ctx_id = 0;  // id of the context the address belongs to (0: none yet)
+  void* ptr = nullptr;
+};
+
+std::mutex g_setup_mu;
+ScratchSlot g_slot[64];  // per device
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+// The driver's context queries, through the runtime (no link-time dependency on the driver).
+int driver_entry_points() {
+  if (g_ctx_get_current && g_ctx_get_id) return QUBO_OK;
+  void* f1 = nullptr;
+  void* f2 = nullptr;
+  cudaDriverEntryPointQueryResult q1 = cudaDriverEntryPointSymbolNotFound, q2 = cudaDriverEntryPointSymbolNotFound;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f1, 12000, cudaEnableDefault, &q1);
+  if (e != cudaSuccess || q1 != cudaDriverEntryPointSuccess || !f1)
+    return record_cuda_error(e != cudaSuccess ? e : cudaErrorSymbolNotFound, "driver entry point cuCtxGetCurrent");
+  e = cudaGetDriverEntryPointByVersion("cuCtxGetId", &f2, 12000, cudaEnableDefault, &q2);
+  if (e != cudaSuccess || q2 != cudaDriverEntryPointSuccess || !f2)
+    return record_cuda_error(e != cudaSuccess ? e : cudaErrorSymbolNotFound, "driver entry point cuCtxGetId");
+  g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(f1);
+  g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(f2);
+  return QUBO_OK;
+}
+
+// Unique id of the calling thread's current context; 0 when none is current yet.
+int current_context_id(unsigned long long* id) {
+  *id = 0;
+  CUcontext ctx = nullptr;
+  if (g_ctx_get_current(&ctx) != CUDA_SUCCESS) return record_cuda_error(cudaErrorContextIsDestroyed, "cuCtxGetCurrent");
+  if (ctx && g_ctx_get_id(ctx, id) != CUDA_SUCCESS) return record_cuda_error(cudaErrorContextIsDestroyed, "cuCtxGetId");
+  return QUBO_OK;
+}
+
+// Device address of the scratch array in the current context of device `dev` (which must be
+// current). In host code the array's name is only a stand-in, so the address is looked up with
+// cudaGetSymbolAddress once per context.
 int scratch_address(int dev, void** out) {
   if (dev < 0 || dev >= 64) return QUBO_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_setup_mu);
-  if (!g_scratch_ptr[dev]) {
+  int st = driver_entry_points();
+  if (st) return st;
+  unsigned long long id = 0;
+  if ((st = current_context_id(&id))) return st;
+  ScratchSlot& s = g_slot[dev];
+  if (id == 0 || s.ctx_id != id || !s.ptr) {
     void* ptr = nullptr;
+    // With no context current yet, this call initialises the device's primary context.
     cudaError_t e = cudaGetSymbolAddress(&ptr, g_no_alloc_scratch);
-    if (e != cudaSuccess || ptr == nullptr) return record_cuda_error(e, "cudaGetSymbolAddress(scratch)");
-    g_scratch_ptr[dev] = ptr;
+    if (e != cudaSuccess || ptr == nullptr)
+      return record_cuda_error(e != cudaSuccess ? e : cudaErrorInvalidSymbol, "cudaGetSymbolAddress(scratch)");
+    if (id == 0 && (st = current_context_id(&id))) return st;
+    s.ctx_id = id;
+    s.ptr = ptr;
   }
-  *out = g_scratch_ptr[dev];
+  *out = s.ptr;
   return QUBO_OK;
 }
 
@@ -51,6 +105,7 @@ extern "C" int qubo_solve_device_no_alloc(int n, const void* d_Q, int dtype, int
   if (n < 1 || n > 62 || d_Q == nullptr || d_result == nullptr || !valid_dtype(dtype))
     return QUBO_ERR_ARG;
   if (k_prefix > n || cache_bits > n) return QUBO_ERR_PLAN;
+  if (abort_requested()) return QUBO_ERR_ABORTED;
   int count = 0, dev = 0;
   cudaError_t e = cudaGetDeviceCount(&count);
   if (e != cudaSuccess || count == 0) return QUBO_ERR_NODEV;

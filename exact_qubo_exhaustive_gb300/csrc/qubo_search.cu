@@ -262,11 +262,6 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.gties = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
   w.gkey = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
   w.results = reinterpret_cast<qubo_result*>(take((size_t)p.ngroups * sizeof(qubo_result)));
-  if (p.tc) {
-    w.M8 = reinterpret_cast<int32_t*>(take((size_t)(p.n - kTcC) * 256 * 4));
-    w.E8 = reinterpret_cast<int32_t*>(take(256 * 4));
-    w.T8 = reinterpret_cast<int32_t*>(take(((size_t)1 << p.w8) * 4));
-  }
   w.bytes = off;
   return w;
 }
@@ -298,10 +293,6 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, nTpad);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if (p.tc) {
-    if ((e = launch_tc_tables(p.n, p.w8, w.hdr, w.U, w.M8, w.E8, w.T8, stream)) != cudaSuccess) return e;
-    ++nl;
-  }
 
   memset(&kp, 0, sizeof(kp));
   kp.n = p.n;
@@ -309,7 +300,6 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   kp.F = p.F;
   kp.w = p.w;
   kp.dtype = p.dtype;
-  kp.tc_active = p.tc ? 1 : 0;
   kp.biased_active = p.biased ? 1 : 0;
   kp.packed_active = p.packed ? 1 : 0;
   kp.seg_bits = p.seg_bits;
@@ -349,12 +339,6 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     kp.unit_end = (u0 + chunk < p.total_units) ? u0 + chunk : p.total_units;
     const uint64_t nunits = kp.unit_end - kp.unit_begin;
     const int blocks = (int)(nunits < (uint64_t)p.blocks ? nunits : (uint64_t)p.blocks);
-    if (p.tc) {
-      // tensor-core pass (exits at once when sum |U| is beyond its exact range) ...
-      const int tcb = (int)(nunits < (uint64_t)p.tc_blocks ? nunits : (uint64_t)p.tc_blocks);
-      if ((e = launch_tc_search(kp, p.w8, w.M8, w.E8, w.T8, tcb, stream)) != cudaSuccess) return e;
-      ++nl;
-    }
     if (p.packed) {
       // packed 16x2 CUDA-core pass (exits at once unless it owns the minimum pass) ...
       const int pb = (int)(nunits < (uint64_t)p.packed_blocks ? nunits : (uint64_t)p.packed_blocks);

@@ -11,7 +11,6 @@ namespace qgb {
 struct KParams {
   int n, C, F, w;           // w = walked bits per unit
   int dtype;
-  int tc_active;            // a tensor-core minimum pass runs when sum |U| <= kTcMaxAbsSum
   int biased_active;        // a biased-binade minimum pass runs when sum |U| <= kBiasedWalkMaxAbsSum
   int packed_active;        // a packed 16x2 minimum pass runs when sum |U| <= kPackedMaxAbsSum
   int seg_bits;             // resolve: segments per tied unit = 2^seg_bits
@@ -42,12 +41,10 @@ struct KParams {
 };
 
 // Which of the minimum passes of one launch sequence does the work; the others exit at once.
-// The tensor-core pass (opt-in) first, then the narrowest CUDA-core representation that the
-// proven range admits.
-enum MinPassOwner : int { kOwnerTc = 0, kOwnerPacked = 1, kOwnerBiased = 2, kOwnerInt = 3 };
+// The narrowest representation that the proven range admits wins.
+enum MinPassOwner : int { kOwnerPacked = 1, kOwnerBiased = 2, kOwnerInt = 3 };
 __device__ __forceinline__ int min_pass_owner(const KParams& p) {
   const int64_t S = p.hdr->abs_sum;
-  if (p.tc_active && S <= kTcMaxAbsSum) return kOwnerTc;
   if (p.packed_active && S <= kPackedMaxAbsSum) return kOwnerPacked;
   if (p.biased_active && S <= kBiasedWalkMaxAbsSum) return kOwnerBiased;
   return kOwnerInt;
@@ -252,10 +249,5 @@ cudaError_t run_key_pass(const Plan& p, const KParams& base, int mode, int theta
 cudaError_t launch_search_generic(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_fast(int threads, size_t smem, int* blocks_per_sm);
 cudaError_t occupancy_generic(int threads, size_t smem, int* blocks_per_sm);
-cudaError_t launch_tc_search(const KParams& p, int w8, const int32_t* M8, const int32_t* E8, const int32_t* T8,
-                             int blocks, cudaStream_t s);
-cudaError_t launch_tc_tables(int n, int w8, const DevHeader* hdr, const int32_t* U, int32_t* M8, int32_t* E8,
-                             int32_t* T8, cudaStream_t s);
-size_t tc_smem_bytes(int w8);
 
 }  // namespace qgb

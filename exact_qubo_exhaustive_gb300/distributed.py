@@ -97,6 +97,8 @@ def solve_distributed(Q, k_prefix: int, group=None, cache_bits: int = 0, solver=
     mine = _pack(rec, device)
     gathered = [torch.empty_like(mine) for _ in range(world)]
     dist.all_gather(gathered, mine, group=group)
-    integer = Q.dtype != np.float32
+    # integer input is searched as int32 and its energies are exact integers; float32 and float64
+    # input give fp64 energies, which must not be truncated
+    integer = Q.dtype.kind in "iu"
     e, r, t = combine(_unpack(g.cpu(), integer) for g in gathered)
     return e, rank_to_bits(n, r), t

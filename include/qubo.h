@@ -55,7 +55,11 @@ extern "C" {
 /* status codes (0 or negative) */
 #define QUBO_OK 0
 #define QUBO_ERR_ARG (-1)       /* n out of range, null pointer, bad dtype, bad slice id */
-#define QUBO_ERR_RANGE (-2)     /* int32: S > 2^30 - 1 */
+#define QUBO_ERR_RANGE (-2)     /* int32: S = sum |U_ij| > 2^30 - 1. Why 2^30 and not 2^31: §IV-B.5 keeps
+                                   every intermediate inside the integer type; besides sub-sums of U
+                                   (|v| <= S) the kernels form the difference of the running best and
+                                   a unit's offset, two sub-sums, so |v| <= 2S, and 2S < 2^31 needs
+                                   S <= 2^30 - 1. */
 #define QUBO_ERR_NONFINITE (-3) /* fp32/fp64: NaN or Inf in Q */
 #define QUBO_ERR_PLAN (-4)      /* explicit k_prefix / cache_bits the kernels cannot run */
 #define QUBO_ERR_CUDA (-5)      /* a CUDA call failed (message via qubo_last_error) */
@@ -87,8 +91,6 @@ typedef struct qubo_plan_desc {
   uint64_t units;      /* work units (fixed prefixes) per call */
   size_t workspace_bytes;
   size_t smem_bytes;
-  int tensor_cores;    /* 1: the minimum pass runs on tcgen05 tensor cores when sum |U_ij| <= 2^21
-                          (opt-in: environment QUBO_TENSOR_CORES=1); 0: on the CUDA-core kernel */
   int packed;          /* 1: int32 input whose sum |U_ij| <= 2^14 - 1 runs the minimum pass with two
                           16-bit energies per 32-bit word (§IV-B.5's narrow path); 0: not available */
   int biased;          /* 1: int32 input whose sum |U_ij| <= 2^22 - 1 (and not narrower) runs the
@@ -117,16 +119,25 @@ QUBO_API int qubo_solve_slice_range(int n, const void* Q, int dtype, int k_prefi
                            uint8_t* out_argmin_x, uint64_t* out_tie_count);
 
 /* Batched mode: `batch` independent problems of equal size n, Q = batch consecutive n*n
- * matrices (host pointer). One thread block solves one problem. Outputs are per problem:
- * out_min_energy[batch], out_argmin_x[batch * n], out_tie_count[batch]. int32 only. */
+ * matrices (host pointer). §III-C1: the search splits into independent subproblems, each solved
+ * by Algorithm 2 (§III-B); here every instance is one such problem and instances share no state.
+ * Small instances run one thread block per instance; 18 <= n <= 32 splits each instance into
+ * work units of the same persistent passes as qubo_solve. Outputs are per problem:
+ * out_min_energy[batch], out_argmin_x[batch * n], out_tie_count[batch]. int32 only; an instance
+ * whose range check fails makes the call return its status (QUBO_ERR_RANGE). */
 QUBO_API int qubo_solve_batched(int batch, int n, const void* Q, int dtype, double* out_min_energy,
                        uint8_t* out_argmin_x, uint64_t* out_tie_count);
 
 /* ---- device-resident entry points (PyTorch or the caller owns memory and streams) ----
+ * The same searches as the host entry points: Algorithm 2 of §III-B with the §III-C1 split
+ * (inputs Q, A/B sizes; outputs x_opt, E_min, plus the tie count), with every buffer in device
+ * memory owned by the caller.
  * d_Q: DEVICE pointer to the input; d_workspace: device buffer of at least the size the
  * matching *_workspace_bytes call returns (256-byte aligned); cuda_stream: a cudaStream_t
  * (NULL = legacy default stream). The call only enqueues work and returns; d_result is
- * written on the stream (status included). Host-detectable errors are returned directly. */
+ * written on the stream (status included: range and finiteness errors are found on the device
+ * and reported there). Host-detectable errors (arguments, plan, abort) are returned directly,
+ * before anything is enqueued. qubo_workspace_bytes returns 0 for arguments it cannot plan. */
 QUBO_API size_t qubo_workspace_bytes(int n, int dtype, int k_prefix, int cache_bits);
 QUBO_API int qubo_solve_device(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits, void* d_workspace,
                       size_t workspace_bytes, void* cuda_stream, qubo_result* d_result);
@@ -137,12 +148,15 @@ QUBO_API int qubo_solve_device(int n, const void* d_Q, int dtype, int k_prefix, 
  * has no counterpart: this is a deployment variant of qubo_solve_device with the same arguments
  * minus the workspace. Scratch memory is one file-scope device array of
  * QUBO_NO_ALLOC_SCRATCH_BYTES that every GPU loading the library keeps until exit; problems
- * whose workspace (qubo_workspace_bytes) exceeds it return QUBO_ERR_ARG. The first call on a
- * device looks the array's device address up (cudaGetSymbolAddress); make that first call before
- * any stream capture. All calls share the array and it keeps the last call's contents; every
- * call rewrites everything it reads, so nothing needs clearing. Calls that overlap on the GPU
- * race on the array: order them on one stream. No cudaMalloc, cudaFree or allocating routine is
- * called. d_Q, d_result: device pointers; cuda_stream: a cudaStream_t (NULL = legacy stream);
+ * whose workspace (qubo_workspace_bytes) exceeds it return QUBO_ERR_ARG. The first call in each
+ * CUDA context looks the array's device address up (cudaGetSymbolAddress) and keeps it with the
+ * context's unique id, so a call from another context (after cudaDeviceReset, or under a context
+ * made with the driver API) looks it up again; make the first call in a context before any
+ * stream capture. All calls share the array and it keeps the last call's contents; every call
+ * rewrites everything it reads, so nothing needs clearing. Calls that overlap on the GPU race on
+ * the array: order them on one stream. No cudaMalloc, cudaFree or allocating routine is called.
+ * A pending qubo_request_abort() refuses the call (QUBO_ERR_ABORTED) before any device work.
+ * d_Q, d_result: device pointers; cuda_stream: a cudaStream_t (NULL = legacy stream);
  * asynchronous like qubo_solve_device. */
 #define QUBO_NO_ALLOC_SCRATCH_BYTES (8u << 20)
 QUBO_API int qubo_solve_device_no_alloc(int n, const void* d_Q, int dtype, int k_prefix, int cache_bits,
@@ -239,7 +253,9 @@ QUBO_API double qubo_kernel_time_ms(void);
 /* Number of kernel launches the last host or device call enqueued. */
 QUBO_API int qubo_last_launch_count(void);
 
-/* Text for a status code; the last CUDA error text for QUBO_ERR_CUDA. */
+/* Text for a status code; the last CUDA error text for QUBO_ERR_CUDA. The paper defines no status
+ * codes: these are this library's own. The returned strings are static (never freed); the
+ * last-error text is overwritten by the next failing call. */
 QUBO_API const char* qubo_status_string(int status);
 QUBO_API const char* qubo_last_error(void);
 

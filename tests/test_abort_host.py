@@ -18,7 +18,10 @@ def test_pending_abort_refuses_calls(q, tmp_path):
     Q = qi.random_upper_int(12, -9, 9, 1)
     q.request_abort()
     for call in (lambda: q.solve(Q), lambda: q.solve_slices(Q, 2, [0, 1]), lambda: q.solve_lowest(Q, 3),
-                 lambda: q.solve_batched(np.stack([Q, Q])), lambda: q.solve_checkpointed(Q, 2, str(tmp_path / "a"))):
+                 lambda: q.solve_batched(np.stack([Q, Q])), lambda: q.solve_checkpointed(Q, 2, str(tmp_path / "a")),
+                 # the abort check comes before any use of these (never dereferenced) device pointers
+                 lambda: q.solve_device_no_alloc(12, 256, q.INT32, None, 512),
+                 lambda: q.solve_device(12, 256, q.INT32, 1024, 1 << 20, None, 512)):
         with pytest.raises(q.QuboError) as ei:
             call()
         assert ei.value.status == -7

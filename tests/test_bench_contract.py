@@ -39,3 +39,39 @@ def test_max_over_ranks_single_process_group():
         assert bench.max_over_ranks([1.5, 2.0], "cpu") == [1.5, 2.0]
     finally:
         dist.destroy_process_group()
+
+
+def test_self_check_against_the_stored_full_search():
+    # the timed answer is compared with tests/golden/full_oracle_n40_int32.txt; a wrong energy,
+    # rank or tie count raises, so bench.py exits non-zero instead of printing a rate
+    import pytest
+    sys.path.insert(0, ROOT)
+    import bench
+    e, r, t = bench.golden("n40_int32")
+    assert bench.check_result("n40_int32", e, r, t)
+    for bad in ((e + 1, r, t), (e, r + 1, t), (e, r, t + 1)):
+        with pytest.raises(bench.ResultMismatch):
+            bench.check_result("n40_int32", *bad)
+    e36, r36, t36 = bench.golden("n36_fp32")
+    assert bench.check_result("n36_fp32", e36 + 1e-9, r36, t36, tol=1e-6)
+    with pytest.raises(bench.ResultMismatch):
+        bench.check_result("n36_fp32", e36 + 1e-3, r36, t36, tol=1e-6)
+
+
+def test_sharded_step_records_combine():
+    # the all-gathered result records of the multi-GPU step: lowest energy wins, equal energies
+    # keep the lowest rank and add their ties, a failed shard raises
+    import numpy as np
+    import pytest
+    sys.path.insert(0, ROOT)
+    import bench
+    dt = np.dtype([("status", np.int32), ("reserved", np.int32), ("min_energy", np.float64),
+                   ("argmin_rank", np.uint64), ("tie_count", np.uint64)])
+    recs = np.zeros(3, dt)
+    recs["min_energy"] = [-7.0, -9.0, -9.0]
+    recs["argmin_rank"] = [5, 40, 12]
+    recs["tie_count"] = [1, 2, 3]
+    assert bench.combine_gathered(recs.tobytes(), 3, dt) == (-9.0, 12, 5)
+    recs["status"][1] = -2
+    with pytest.raises(RuntimeError):
+        bench.combine_gathered(recs.tobytes(), 3, dt)

@@ -122,6 +122,23 @@ def test_two_ranks_fp32(tmp_path):
     check_against_oracle(run_ranks(tmp_path, Q, 3, 2), Q, 3, 2)
 
 
+def test_two_ranks_fp64(tmp_path):
+    # fp64 input: the combined energy keeps its fraction (integer input alone is returned as int)
+    Q = qi.random_symmetric_normal_f32(12, 614).astype(np.float64) * 0.37
+    outs = run_ranks(tmp_path, Q, 3, 2)
+    check_against_oracle(outs, Q, 3, 2)
+    assert outs[0]["e"] != int(outs[0]["e"])
+
+
+def test_fp64_tie_across_shards(tmp_path):
+    # x_0 is free (Q_00 = 0, no coupling), so the two minimisers differ only in x_0 and lie in
+    # different shards of the k_prefix = 1 split; E_min = -2.25 is not an integer
+    Q = np.diag([0.0] + [-0.25] * 9)
+    outs = run_ranks(tmp_path, Q, 1, 2)
+    check_against_oracle(outs, Q, 1, 2)
+    assert outs[0]["e"] == -2.25 and outs[0]["t"] == 2 and outs[0]["x"] == [0] + [1] * 9
+
+
 def _bench_worker(rank, world, port, out_dir):
     os.environ["GLOO_SOCKET_IFNAME"] = "lo"
     dist.init_process_group("gloo", init_method=f"tcp://127.0.0.1:{port}", rank=rank, world_size=world)

@@ -29,6 +29,7 @@ def test_solve_distributed_single_rank_uses_the_cuda_path():
             we, wx, wt = oracle.get().solve(Q)
             if Q.dtype == np.float32:
                 assert abs(e - we) <= 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+                assert t == wt and (x == wx).all()  # the exact fp64 minimiser, lowest rank
             else:
                 assert (e, t) == (we, wt) and (x == wx).all()
     finally:

@@ -24,13 +24,6 @@ def q():
     return lib
 
 
-@pytest.fixture(params=["tensor", "cuda_core"])
-def minpass(request, monkeypatch):
-    """Runs a test with the tensor-core minimum pass (default) and with the CUDA-core one."""
-    monkeypatch.setenv("QUBO_TENSOR_CORES", "1" if request.param == "tensor" else "0")
-    return request.param
-
-
 def fp32_tol(Q):
     return 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
 
@@ -46,7 +39,7 @@ def check_int(q, Q, **kw):
 # ---------------------------------------------------------------- exhaustive small sweeps
 
 @pytest.mark.parametrize("n", list(range(1, 17)))
-def test_small_n_sweep(q, n, minpass):
+def test_small_n_sweep(q, n):
     for seed, (lo, hi) in enumerate([(-100, 100), (-2, 2), (-1, 1), (0, 3)]):
         check_int(q, qi.random_upper_int(n, lo, hi, 1000 * n + seed))
     check_int(q, qi.random_full_int(n, -50, 50, 7 * n))  # non-triangular input
@@ -72,7 +65,7 @@ def test_diagonal_closed_form(q, n):
     (16, 0, 9), (17, 0, 12), (18, 1, 12), (20, 3, 12), (20, 0, 9), (21, 4, 10), (22, 2, 11),
     (20, 6, 9), (14, 2, 6), (12, 0, 10), (13, 5, 3), (15, 14, 1), (10, 4, 6), (18, 8, 10), (9, 9, 0),
 ])
-def test_explicit_plans(q, n, k, c, minpass):
+def test_explicit_plans(q, n, k, c):
     for seed, (lo, hi) in enumerate([(-100, 100), (-1, 1)]):
         Q = qi.random_upper_int(n, lo, hi, 77 * n + 3 * k + c + seed)
         check_int(q, Q, k_prefix=k, cache_bits=c)
@@ -85,33 +78,19 @@ def test_infeasible_explicit_plan_is_an_error(q):
     assert ei.value.status == -4
 
 
-def test_plans_pick_fast_kernel_for_large_n(q, monkeypatch):
-    monkeypatch.delenv("QUBO_TENSOR_CORES", raising=False)
+def test_plans_pick_fast_kernel_for_large_n(q):
     p = q.plan(40)
-    assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024 and p["tensor_cores"] == 0
-    assert q.plan(8)["variant"] == 0 and q.plan(8)["tensor_cores"] == 0
-    monkeypatch.setenv("QUBO_TENSOR_CORES", "1")
-    assert q.plan(40)["tensor_cores"] == 1
-    assert q.plan(36, q.FP32)["tensor_cores"] == 0
+    assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
+    assert p["biased"] == 1 and p["packed"] == 1
+    assert q.plan(8)["variant"] == 0
+    assert q.plan(36, q.FP32)["biased"] == 0 and q.plan(36, q.FP32)["packed"] == 0
 
 
 @pytest.mark.parametrize("n,seed", [(16, 1), (17, 2), (19, 3), (23, 4), (27, 5)])
-def test_tensor_split_boundaries(q, n, seed, monkeypatch):
-    monkeypatch.setenv("QUBO_TENSOR_CORES", "1")
-    # n = 16 is the smallest tensor-core split (one Gray-walked bit, two tiles per unit)
+def test_fast_split_boundaries(q, n, seed):
+    # the smallest splits of the register-row kernel, wide and narrow entries
     check_int(q, qi.random_upper_int(n, -1000, 1000, seed))
     check_int(q, qi.random_upper_int(n, -3, 3, seed + 100))
-
-
-def test_tensor_range_limit_falls_back_exactly(q, monkeypatch):
-    monkeypatch.setenv("QUBO_TENSOR_CORES", "1")
-    # sum |U| just above the tensor-core limit (2^21) runs the CUDA-core pass; just below, the tensor one
-    for total in ((1 << 21) - 5, (1 << 21) + 5):
-        Q = qi.random_upper_int(22, -100, 100, 9)
-        Q[0, 0] = 0
-        Q[0, 0] = -(total - int(np.abs(Q).sum()))
-        assert int(np.abs(Q.astype(np.int64)).sum()) == total
-        check_int(q, Q)
 
 
 def _with_abs_sum(Q, total):
@@ -228,16 +207,16 @@ def test_n20_config(q):
     assert O.direct_i64(O.fold_i32(Q)) == (e, oracle.rank_of_bits(x), t)
 
 
-def test_n24_random_and_ties(q, minpass):
+def test_n24_random_and_ties(q):
     check_int(q, qi.random_upper_int(24, -1000, 1000, 5))
     check_int(q, qi.random_upper_int(24, -1, 1, 6))
 
 
-def test_n32_config(q, minpass):
+def test_n32_config(q):
     check_int(q, qi.workload_n32())
 
 
-def test_n32_mattis_planted(q, minpass):
+def test_n32_mattis_planted(q):
     Q, s_star, w, offset = qi.workload_n32_mattis()
     differ = np.not_equal.outer(s_star, s_star)
     e_want = -2 * int(np.triu(w * differ, 1).sum())
@@ -247,7 +226,7 @@ def test_n32_mattis_planted(q, minpass):
     assert e == e_want and t == 2 and (x == x_want).all()
 
 
-def test_n40_slices_against_oracle(q, minpass):
+def test_n40_slices_against_oracle(q):
     Q = qi.workload_n40()
     k = 12
     ids = qi.Stream(4040).integers(0, (1 << k) - 1, 6).astype(np.uint64)

@@ -60,6 +60,41 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(env):
             assert got["tie_count"] == want["tie_count"]
 
 
+def test_interleaved_problems_of_every_minimum_pass(env):
+    # every minimum pass works in the shared array: packed 16x2 (narrow int32, n >= 30), biased
+    # fp32 binade (wide int32, n >= 30) and int32 (fp32 input's fixed-point image, n >= 30), plus
+    # a small problem; two rounds, so every call follows another problem's leftovers
+    q, torch = env
+    cases = [(32, qi.random_upper_int(32, -3, 3, 81), q.INT32),
+             (31, qi.random_symmetric_normal_f32(31, 82), q.FP32),
+             (33, qi.random_upper_int(33, -1000, 1000, 83), q.INT32),
+             (20, qi.random_upper_int(20, -1, 1, 84), q.INT32),
+             (30, qi.random_upper_int(30, -2, 2, 85), q.INT32)]
+    plans = [q.plan(n, dt) for n, _, dt in cases]
+    assert plans[0]["packed"] == 1 and plans[2]["biased"] == 1 and plans[4]["packed"] == 1
+    wants = [with_workspace(q, torch, n, Q, dt) for n, Q, dt in cases]
+    for _ in range(2):
+        for (n, Q, dt), want in zip(cases, wants):
+            got = no_alloc(q, torch, n, Q, dt)
+            assert got["status"] == 0 and want["status"] == 0
+            assert (got["min_energy"], got["argmin_rank"], got["tie_count"]) == \
+                (want["min_energy"], want["argmin_rank"], want["tie_count"]), n
+
+
+def test_largest_problem_that_fits_the_array(env):
+    # the largest n whose default-plan workspace fits the array is accepted and exact
+    q, torch = env
+    n = max(m for m in range(20, 63) if q.workspace_bytes(m) <= q.NO_ALLOC_SCRATCH_BYTES)
+    assert q.workspace_bytes(n + 1) > q.NO_ALLOC_SCRATCH_BYTES
+    Q = qi.random_upper_int(n, -1000, 1000, 86)
+    want = with_workspace(q, torch, n, Q, q.INT32)
+    for _ in range(2):
+        got = no_alloc(q, torch, n, Q, q.INT32)
+        assert got["status"] == 0
+        assert (got["min_energy"], got["argmin_rank"], got["tie_count"]) == \
+            (want["min_energy"], want["argmin_rank"], want["tie_count"])
+
+
 def test_problems_beyond_the_array_are_rejected(env):
     q, torch = env
     n = 52
