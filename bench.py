@@ -52,7 +52,7 @@ SMS = 152
 LANES_PER_CLK = 128          # issue-limited int32 lanes per SM per clock (ALU + FMA-heavy pipes)
 MAX_SM_MHZ = 2070.0
 PROFILE = os.path.join(ROOT, "profiles", "search_kernel_n40.md")
-KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_fast.cu", "qubo_internal.h"]
+KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_pruned.cu", "qubo_internal.h"]
 
 
 SHARD_K = 12                 # slices of the multi-GPU split: 2^12, divisible by 1, 2, 4 and 8 ranks
@@ -375,7 +375,7 @@ def run_gb300(args):
                    "tie_count": int(r["tie_count"]), "checks": checks},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "search_kernel<16,5,min,biased> (enumeration, biased fp32-binade minimum pass)", "kernel_ms": kern,
+                     "kernel": "search_kernel<16,4,min,biased,pruned> (enumeration, biased fp32-binade minimum pass with block bounds)", "kernel_ms": kern,
                      "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
                                    "add per state) x 2.07 GHz max SM clock",
                      "traffic_source": traffic_src,
@@ -481,7 +481,7 @@ def run_gb300_sharded(args):
                        "checks": checks},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                          "frac": achieved / peak, "traffic": None,
-                         "kernel": "search_kernel<16,5,min,biased> on rank 0's shard", "kernel_ms": kern,
+                         "kernel": "search_kernel<16,4,min,biased,pruned> on rank 0's shard", "kernel_ms": kern,
                          "kernel_ms_max_over_ranks": kern_max,
                          "peak_basis": "152 SMs x 128 lanes/clk x 2.07 GHz max SM clock"},
             "e2e": {"value": STATES / (e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": world * N * N * 4,

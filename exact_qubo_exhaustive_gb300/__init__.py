@@ -59,7 +59,8 @@ class _PlanDesc(ctypes.Structure):
                 ("cache_bits", ctypes.c_int), ("walked_bits", ctypes.c_int), ("register_bits", ctypes.c_int),
                 ("columns_per_thread", ctypes.c_int), ("threads_per_block", ctypes.c_int), ("blocks", ctypes.c_int),
                 ("variant", ctypes.c_int), ("units", ctypes.c_uint64), ("workspace_bytes", ctypes.c_size_t),
-                ("smem_bytes", ctypes.c_size_t), ("packed", ctypes.c_int), ("biased", ctypes.c_int)]
+                ("smem_bytes", ctypes.c_size_t), ("packed", ctypes.c_int), ("biased", ctypes.c_int),
+                ("pruned", ctypes.c_int)]
 
 
 # qubo_result record as a numpy dtype (status, reserved, min_energy, argmin_rank, tie_count)

@@ -269,6 +269,8 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   // minimum passes (each launched, the ones that do not apply exiting at once) would cost more
   // than they save, so small problems run the int32 pass alone.
   const bool narrow_passes = n >= kNarrowPassesMinN;
+  // Block-bounded minimum passes: fast variant with at least one iteration of two blocks.
+  p.prune = p.variant == kFast && p.w >= kFastR + 1 && p.C >= 5;
   p.biased = narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
   // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
   // shared rows are 2 bytes per column.
@@ -670,6 +672,7 @@ int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* ou
   out->smem_bytes = p.smem_bytes;
   out->packed = p.packed ? 1 : 0;
   out->biased = p.biased ? 1 : 0;
+  out->pruned = p.prune ? 1 : 0;
   return QUBO_OK;
 }
 

@@ -13,9 +13,11 @@ namespace qgb {
 //          2^s times its energy by at most (#selected terms)/2 <= n(n+1)/4, so every fp64
 //          minimiser lies within band = n(n+1)/2 image units of the image minimum.
 // ------------------------------------------------------------------------------------------------
+// gthr (optional, ngroups entries): the pruned minimum passes' per-group best, started at
+// sum |U_ij| of the int32 image, which no energy exceeds.
 __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void* __restrict__ Qv, DevHeader* hdr,
                                                    int32_t* U, double* U64, uint64_t* gbase0,
-                                                   uint64_t gbase0_value) {
+                                                   uint64_t gbase0_value, int32_t* gthr, int ngroups) {
   __shared__ unsigned long long s_sum;
   __shared__ int s_bad;
   __shared__ double s_part[256];
@@ -47,6 +49,10 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
       hdr->band = 0;
       hdr->tied_count = 0;
       hdr->status = (s_sum > (unsigned long long)kMaxAbsSum) ? QUBO_ERR_RANGE : QUBO_OK;
+    }
+    if (gthr) {
+      const int32_t top = (int32_t)(s_sum < (unsigned long long)kMaxAbsSum ? s_sum : (unsigned long long)kMaxAbsSum);
+      for (int g = tid; g < ngroups; g += nt) gthr[g] = top;
     }
     return;
   }
@@ -115,6 +121,10 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
     hdr->tied_count = 0;
     hdr->status = s_bad ? QUBO_ERR_NONFINITE : (s_sum <= (unsigned long long)kMaxAbsSum ? QUBO_OK : QUBO_ERR_RANGE);
   }
+  if (gthr) {
+    const int32_t top = (int32_t)(s_sum < (unsigned long long)kMaxAbsSum ? s_sum : (unsigned long long)kMaxAbsSum);
+    for (int g = tid; g < ngroups; g += nt) gthr[g] = top;
+  }
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -123,10 +133,12 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
 //   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
 //   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
 //   T2[i]    = (T[i] mod 2^16) in both 16-bit halves (packed pass; optional)
+//   Tmin[m]  = min of T over steps [2^kFastR m, 2^kFastR (m + 1)) (pruned minimum passes; optional,
+//              needs w > kFastR and C >= 5: then every warp of the loop lies inside the T range)
 // ------------------------------------------------------------------------------------------------
 __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __restrict__ hdr,
                               const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint32_t* T2,
-                              uint64_t nTpad) {
+                              int32_t* Tmin, uint64_t nTpad) {
   if (hdr->status != QUBO_OK) return;
   const int ncols = 1 << C;
   const uint64_t nM = (uint64_t)(n - C) << C;
@@ -169,6 +181,13 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
       }
       T[i] = acc;
       if (T2) T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
+      if (Tmin) {
+        // the 2^kFastR consecutive steps of a block are consecutive lanes of this warp
+        int m = acc;
+#pragma unroll
+        for (int off = 1; off < (1 << kFastR); off <<= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, off));
+        if ((i & ((1u << kFastR) - 1)) == 0) Tmin[i >> kFastR] = m;
+      }
     }
   }
 }
@@ -254,6 +273,10 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.Ec = reinterpret_cast<int32_t*>(take(ncols * 4 < 16 ? 16 : ncols * 4));
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));
   if (p.packed) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
+  if (p.prune) {
+    w.Tmin = reinterpret_cast<int32_t*>(take((nT >> kFastR) * 4 + 8));
+    w.gthr = reinterpret_cast<int32_t*>(take((size_t)p.ngroups * 4));
+  }
   w.unit_min = reinterpret_cast<int32_t*>(take(p.total_units * 4));
   w.tied = reinterpret_cast<uint32_t*>(take(p.total_units * 4));
   w.gbase = reinterpret_cast<uint64_t*>(take((size_t)p.ngroups * 8));
@@ -283,14 +306,14 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   // gbase: uploaded by the host for slices and ranges; otherwise one group starting at unit 0,
   // written by the prep kernel.
   prep_kernel<<<1, 256, 0, stream>>>(p.n, p.dtype, d_Q, w.hdr, w.U, w.U64, p.host_gbase ? nullptr : w.gbase,
-                                     p.gbase0);
+                                     p.gbase0, w.gthr, p.ngroups);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   const uint64_t nTpad = ((uint64_t)1 << p.w) < 4 ? 4 : ((uint64_t)1 << p.w);
   const uint64_t tab_work = ((uint64_t)(p.n - p.C) << p.C) + ((uint64_t)1 << p.C) + nTpad;
   const int tab_blocks = (int)((tab_work + 255) / 256 < 4096 ? (tab_work + 255) / 256 : 4096);
-  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, nTpad);
+  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, w.Tmin, nTpad);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -312,6 +335,8 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   kp.Ec = w.Ec;
   kp.T = w.T;
   kp.T2 = w.T2;
+  kp.Tmin = w.Tmin;
+  kp.gthr = w.gthr;
   kp.gbase = w.gbase;
   kp.unit_min = w.unit_min;
   kp.tied = w.tied;
@@ -347,11 +372,15 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     }
     if (p.biased) {
       // biased-binade CUDA-core pass (exits at once unless it owns the minimum pass) ...
-      if ((e = launch_search_biased(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
+      e = p.prune ? launch_search_pruned(true, kp, blocks, p.threads, p.smem_bytes, stream)
+                  : launch_search_biased(kp, blocks, p.threads, p.smem_bytes, stream);
+      if (e != cudaSuccess) return e;
       ++nl;
     }
     // ... and the int32 CUDA-core pass (exits at once when another pass ran)
-    if (p.variant == kFast && p.w >= kIntMinR + 1) {
+    if (p.prune) {
+      if ((e = launch_search_pruned(false, kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
+    } else if (p.variant == kFast && p.w >= kIntMinR + 1) {
       if ((e = launch_search_int_min5(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
     } else if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) {
       return e;

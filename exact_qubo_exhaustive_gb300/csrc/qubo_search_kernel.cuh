@@ -24,6 +24,8 @@ struct KParams {
   const int32_t* Ec;
   const int32_t* T;
   const uint32_t* T2;       // packed pass: T's low 16 bits in both halves
+  const int32_t* Tmin;      // pruned minimum passes: block minima of T
+  int32_t* gthr;            // pruned minimum passes: best energy published so far, per group
   const uint64_t* gbase;
   int32_t* unit_min;
   uint32_t* tied;
@@ -80,9 +82,12 @@ __device__ __forceinline__ int min_walk(const WalkCtx& c, const KParams& p, int 
 
 // BIASED: the minimum pass with column energies in the biased fp32 binade (VOps<float>). Which
 // minimum pass of a launch sequence runs is decided on the device by min_pass_owner.
-template <int CPT, int R, int MODE, bool BIASED = false>
+// PRUNE: the minimum pass with block bounds (PrunedMinWalker); unit minima above the group's
+// best are then only upper bounds of the true ones (see PrunedMinWalker).
+template <int CPT, int R, int MODE, bool BIASED = false, bool PRUNE = false>
 __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const KParams p) {
   static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
+  static_assert(!PRUNE || (MODE == kModeMin && CPT >= 4), "pruned walk: fast layout, minimum pass");
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
   __shared__ int s_red[32];
@@ -170,7 +175,13 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 
     if constexpr (MODE == kModeMin) {
       int best;
-      if (niter == 0) {
+      if constexpr (PRUNE) {
+        using VT = typename std::conditional<BIASED, float, int>::type;
+        PrunedMinWalker<CPT, R, VT> W;
+        W.init(c, p.Ec, p.M, cP);
+        W.walk(c, niter, p.Tmin, p.gthr + g, p.hdr->band);
+        best = W.aux - VOps<VT>::kBiasBits + W.s;
+      } else if (niter == 0) {
         // no walked variable (generic variant only): the single walked assignment is 0
         Walker<CPT, R, MODE> W;
         W.init(c, p.Ec, p.M, cP);
@@ -188,6 +199,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
         int b = s_red[0];
         for (int k = 1; k < (nthreads >> 5); ++k) b = min(b, s_red[k]);
         p.unit_min[u] = b;
+        if constexpr (PRUNE) atomicMin(p.gthr + g, b);
       }
     } else {
       Walker<CPT, R, MODE> W;
@@ -233,6 +245,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_int_min5(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_search_pruned(bool biased, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_packed(int threads, size_t smem, int* blocks_per_sm);
 size_t packed_smem_bytes(int C, int w);

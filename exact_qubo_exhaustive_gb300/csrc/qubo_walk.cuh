@@ -617,6 +617,153 @@ struct Walker {
   }
 };
 
+// ------------------------------------------------------------------------------------------------
+// Minimum walk with block bounds (kModeMin, fast layout).
+//
+// Every state still costs its one add (eq. 9): each Gray step adds a walked row to all of the
+// thread's column energies. What a block bound saves is the minimum over the columns. A block is
+// the 2^R steps between two shared-memory flips; inside it only the register rows flip, so s is
+// constant and, for every step d of block m and column j,
+//     E(d, j) - s = T[2^R m + d] + V_d[j] >= Tmin[m] + min_j V_0[j] + D_par,
+// where Tmin[m] is the smallest walked energy of the block (a table), V_0 the columns at the
+// block's first state and D_par <= 0 the most negative change of any of the thread's columns over
+// a block of that parity (the register rows alone fix it, so it is computed once per unit). When
+// that bound is above the threshold for every lane of the warp, no state of the block can be at
+// or below the threshold, and the block's per-step minima are not formed; otherwise the block is
+// walked with them, exactly as the plain minimum walk does.
+//
+// The threshold is min(this thread's best, G) + band. G is the best energy any block of the grid
+// has published for this group so far (or sum |U_ij|, which bounds every energy from above).
+// Every value involved is an energy some state of the group attains, so the threshold is never
+// below the group's minimum E*: a state with E <= E* + band is never in a skipped block. Hence a
+// unit holding such a state reports its minimum exactly, every other unit reports the energy of
+// a state it evaluated (above E* + band), the group minimum and the list of units within the
+// band are exactly those of the plain walk, and the resolution passes are unchanged.
+// ------------------------------------------------------------------------------------------------
+template <int CPT, int R, typename VT>
+struct PrunedMinWalker : Walker<CPT, R, kModeMin, VT> {
+  using B = Walker<CPT, R, kModeMin, VT>;
+  using O = typename B::O;
+  using RowBuf = typename B::RowBuf;
+  static constexpr int kMid = B::kMid;       // steps per block
+  static constexpr int kSteps = B::kSteps;   // steps per iteration: two blocks
+  static_assert(CPT >= 4 && R >= 2 && kMid % 4 == 0, "fast layout, whole quads of walked energies per block");
+  static constexpr int kRefreshMask = 15;    // iterations between two exchanges of the group's best
+
+  int dmin[2];   // D_par of the two block parities
+  int g_best;    // G: the group's best energy known to this warp (absolute, image units)
+
+  // Register-row flip of step L -> L + 1 of an iteration, L < kSteps - 1 and L + 1 != kMid.
+  template <int L>
+  __device__ __forceinline__ void reg_flip(VT* v) {
+    constexpr int a = ctz_c(L + 1);
+    constexpr int bit = ((L >> a) ^ (L >> (a + 1))) & 1;  // bit a of gray(L): 1 -> the flip clears it
+#pragma unroll
+    for (int jj = 0; jj < CPT; ++jj) v[jj] = bit ? O::sub(v[jj], this->Row[a][jj]) : O::add(v[jj], this->Row[a][jj]);
+  }
+
+  // Most negative change of any column from a block's first state to any of its states.
+  template <int H, int D>
+  __device__ __forceinline__ void block_drop(VT* delta, VT& lo) {
+    if constexpr (D + 1 < kMid) {
+      reg_flip<H * kMid + D>(delta);
+#pragma unroll
+      for (int jj = 0; jj < CPT; ++jj) lo = delta[jj] < lo ? delta[jj] : lo;
+      block_drop<H, D + 1>(delta, lo);
+    }
+  }
+
+  __device__ __forceinline__ void init_bounds() {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      VT delta[CPT];
+#pragma unroll
+      for (int jj = 0; jj < CPT; ++jj) delta[jj] = O::row(0);
+      VT lo = O::row(0);
+      if (h == 0) block_drop<0, 0>(delta, lo);
+      else block_drop<1, 0>(delta, lo);
+      dmin[h] = static_cast<int>(lo);  // exact: an integer-valued fp32 number for the biased walk
+    }
+  }
+
+  // Steps of one block: the register flips, and (EXACT) the per-step minima of steps 1..kMid-1.
+  template <int H, int D, bool EXACT>
+  __device__ __forceinline__ void block_steps(const int4* tq) {
+    if constexpr (D + 1 < kMid) {
+      reg_flip<H * kMid + D>(this->V);
+      if constexpr (EXACT)
+        this->aux = __viaddmin_s32(vmin_bits<VT, CPT>(this->V), B::template comp<(D + 1) & 3>(tq[(D + 1) >> 2]), this->aux);
+      block_steps<H, D + 1, EXACT>(tq);
+    }
+  }
+
+  // One block: bound test, then the walk with or without per-step minima. On return V holds the
+  // block's last state; `rb` holds the row of the flip that follows (position a_next).
+  template <int H>
+  __device__ __forceinline__ void block(const WalkCtx& c, uint64_t m, int tmin, int a_next, int band, RowBuf& rb) {
+    this->load_dyn_row(c, a_next, rb);
+    const int m0 = vmin_bits<VT, CPT>(this->V);
+    bool skip;
+    if constexpr (O::kInt) {
+      // int32 image of up to 2^30: the bound can leave int32, so compare in 64 bits
+      const long long lb = (long long)m0 + tmin + dmin[H];
+      const long long th = (long long)min(this->aux, g_best - this->s) + band;
+      skip = lb > th;
+    } else {
+      // biased binade: |every term| <= 4 sum|U| < 2^24, far inside int32 around the bias
+      const int lb = m0 + tmin + dmin[H];
+      const int th = min(this->aux, O::kBiasBits + g_best - this->s) + band;
+      skip = lb > th;
+    }
+    if (__all_sync(0xffffffffu, skip)) {
+      block_steps<H, 0, false>(nullptr);
+    } else {
+      const int4* T4 = reinterpret_cast<const int4*>(c.T) + (m << (R - 2));
+      int4 tq[kMid / 4];
+#pragma unroll
+      for (int q = 0; q < kMid / 4; ++q) tq[q] = __ldg(T4 + q);
+      this->aux = __viaddmin_s32(m0, tq[0].x, this->aux);
+      block_steps<H, 0, true>(tq);
+    }
+  }
+
+  // The group's best: publish this warp's, take the grid's.
+  __device__ __forceinline__ void exchange_best(int* gbest) {
+    int v = __reduce_min_sync(0xffffffffu, this->aux - O::kBiasBits + this->s);
+    if ((threadIdx.x & 31) == 0) {
+      const int old = atomicMin(gbest, v);
+      v = old < v ? old : v;
+    }
+    v = __shfl_sync(0xffffffffu, v, 0);
+    g_best = v < g_best ? v : g_best;
+  }
+
+  // Whole unit: niter iterations of two blocks. Tmin: block minima of T (2 per iteration);
+  // gbest: the group's published best (absolute image units); band: resolution band.
+  __device__ __forceinline__ void walk(const WalkCtx& c, int64_t niter, const int* __restrict__ Tmin, int* gbest,
+                                       int band) {
+    init_bounds();
+    g_best = __ldcg(gbest);
+    // a real best from the first state's columns, so the running best never leaves its range
+    this->aux = __viaddmin_s32(vmin_bits<VT, CPT>(this->V), __ldg(c.T), kIntInf);
+    const int2* Tm2 = reinterpret_cast<const int2*>(Tmin);
+    int2 tm = __ldg(Tm2);
+    for (int64_t iter = 0; iter < niter; ++iter) {
+      const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
+      const bool flip_end = iter + 1 < niter;
+      const int a_end = flip_end ? R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1 : R;
+      const int2 tm_next = __ldg(Tm2 + (flip_end ? iter + 1 : iter));
+      RowBuf rb;
+      block<0>(c, static_cast<uint64_t>(iter) << 1, tm.x, R, band, rb);
+      this->apply_dyn_row(c, R, rb, (iter & 1) == 0);
+      block<1>(c, (static_cast<uint64_t>(iter) << 1) | 1, tm.y, a_end, band, rb);
+      if (flip_end) this->apply_dyn_row(c, a_end, rb, ((gray_code(base + kSteps - 1) >> a_end) & 1u) == 0);
+      tm = tm_next;
+      if ((iter & kRefreshMask) == kRefreshMask) exchange_best(gbest);
+    }
+  }
+};
+
 // Iterations of 2^(R+1) steps in a walk over w bits (generic variant: R = 0, w may be 0).
 template <int R>
 __host__ __device__ inline int64_t walk_iterations(int w) {

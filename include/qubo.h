@@ -95,6 +95,9 @@ typedef struct qubo_plan_desc {
                           16-bit energies per 32-bit word (§IV-B.5's narrow path); 0: not available */
   int biased;          /* 1: int32 input whose sum |U_ij| <= 2^22 - 1 (and not narrower) runs the
                           minimum pass with fp32 column adds in the exact binade [2^23, 2^24) */
+  int pruned;          /* 1: the biased and int32 minimum passes skip the per-step minima of blocks of
+                          16 Gray steps whose lower bound is above the best energy found so far
+                          (every state is still added; results are unchanged) */
 } qubo_plan_desc;
 
 /* Minimise one QUBO. Q is a HOST pointer to n*n int32, fp32 or fp64 values (row-major).

@@ -1,0 +1,106 @@
+"""The block-bounded minimum passes against the oracle where the bound is tightest.
+
+The biased and int32 minimum passes skip the per-step minima of a block of 16 Gray steps when a
+lower bound of every state in it lies above the group's best energy found so far (the states are
+still added, eq. 9). A block holding a state at the minimum (or inside the fp32 band) always has
+its bound at or below the threshold, so it is walked exactly. These cases put minimisers in many
+work units and many blocks at once: the results must still be bit-exact.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import qubo_instances as qi
+
+pytestmark = pytest.mark.gpu
+
+O = oracle.get()
+
+
+@pytest.fixture(scope="module")
+def q():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import exact_qubo_exhaustive_gb300 as lib
+    return lib
+
+
+def with_free_prefix(Q_sub, free: int):
+    """Q over free + m variables: the first `free` variables have no coupling and no diagonal, so
+    every minimiser of Q_sub appears once for each of their 2^free assignments."""
+    m = Q_sub.shape[0]
+    Q = np.zeros((free + m, free + m), dtype=Q_sub.dtype)
+    Q[free:, free:] = Q_sub
+    return Q
+
+
+def test_plans_use_the_bounded_passes(q):
+    assert q.plan(40)["pruned"] == 1 and q.plan(32)["pruned"] == 1
+    assert q.plan(36, q.FP32)["pruned"] == 1
+    assert q.plan(8)["pruned"] == 0  # generic kernel
+
+
+@pytest.mark.parametrize("lo,hi,seed", [(-1000, 1000, 901), (-(1 << 17), 1 << 17, 902), (-2, 2, 903)])
+def test_minimisers_repeated_in_every_unit(q, lo, hi, seed):
+    # 2^7 copies of the 27-variable landscape: one minimiser set per assignment of x_0..x_6, in
+    # many units; biased pass (entries to 1000), int32 pass (2^17) and packed pass (2)
+    sub = qi.random_upper_int(27, lo, hi, seed)
+    e, x, t = O.solve(sub)
+    Q = with_free_prefix(sub, 7)
+    ge, gx, gt = q.solve(Q)
+    assert (ge, gt) == (e, t << 7)
+    assert not gx[:7].any() and (gx[7:] == x).all()
+
+
+def test_minimisers_repeated_fp32(q):
+    sub = qi.random_symmetric_normal_f32(26, 904)
+    e, x, t = O.solve(sub)
+    Q = with_free_prefix(sub, 6)
+    ge, gx, gt = q.solve(Q)
+    tol = 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+    assert abs(ge - e) <= tol and gt == t << 6
+    assert not gx[:6].any() and (gx[6:] == x).all()
+
+
+def test_many_near_minimum_states(q):
+    # entries in {-1, 0, 1}: huge numbers of states within a few units of the minimum, so many
+    # blocks are walked exactly and the threshold meets the bounds often
+    Q = qi.random_upper_int(32, -1, 1, 905)
+    want = O.solve(Q)
+    e, x, t = q.solve(Q)
+    assert (e, t) == (want[0], want[2]) and (x == want[1]).all()
+
+
+def test_small_units_and_explicit_splits(q):
+    # many small units (most of them report only an upper bound of their minimum)
+    Q = qi.random_upper_int(31, -1000, 1000, 906)
+    want = O.solve(Q)
+    for k, c in ((14, 12), (10, 9), (16, 10)):
+        e, x, t = q.solve(Q, k_prefix=k, cache_bits=c)
+        assert (e, t) == (want[0], want[2]) and (x == want[1]).all(), (k, c)
+
+
+def test_slices_keep_their_own_thresholds(q):
+    # slices whose minima differ by a lot: each group's threshold must come from its own units
+    n, k = 30, 3
+    Q = qi.random_upper_int(n, -500, 500, 907)
+    Q[0, 0] = -200000  # slices with x_0 = 1 lie far below those with x_0 = 0
+    ids = np.arange(1 << k, dtype=np.uint64)
+    e, x, t = q.solve_slices(Q, k, ids)
+    for s in range(1 << k):
+        want = O.solve_slice(Q, k, s)
+        assert (int(e[s]), int(t[s])) == (want[0], want[2]) and (x[s] == want[1]).all(), s
+
+
+def test_slice_range_starting_above_zero(q):
+    # a range that does not hold the zero state: no threshold below its own minimum is used
+    n, k = 30, 4
+    Q = qi.random_upper_int(n, 0, 9, 908)  # non-negative: every minimum is 0 ... except the range's
+    Q[np.diag_indices(n)] += 1               # all diagonals >= 1: E(x) > 0 for every x != 0
+    e, x, t = q.solve_slice_range(Q, k, 5, 7)
+    recs = [O.solve_slice(Q, k, s) for s in range(5, 12)]
+    best = min(r[0] for r in recs)
+    ties = sum(r[2] for r in recs if r[0] == best)
+    first = min(oracle.rank_of_bits(r[1]) for r in recs if r[0] == best)
+    assert (e, t, oracle.rank_of_bits(x)) == (best, ties, first) and best > 0
