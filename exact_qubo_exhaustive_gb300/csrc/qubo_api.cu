@@ -173,6 +173,14 @@ bool generic_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
   return true;
 }
 
+// The biased-binade minimum pass: int32 input, fast variant, at least one iteration of
+// 2^(kBiasedR+1) Gray steps. Below 2^30 states a search takes tens of microseconds, mostly kernel
+// launches: the alternative minimum passes (each launched, the ones that do not apply exiting at
+// once) would cost more than they save, so small problems run the int32 pass alone.
+bool biased_pass_applies(const Plan& p) {
+  return p.n >= kNarrowPassesMinN && p.variant == kFast && p.dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
+}
+
 // kind: 0 = whole problem (fixed_lo = 0), 1 = slices/range (fixed bits >= K).
 // units_base: number of groups (slices) or range length; unit bits F = K + s.
 int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t units_base, bool explicit_F,
@@ -263,15 +271,14 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   const int want_seg = ceil_log2_u64((uint64_t)p.blocks);
   while (seg < want_seg && (niter >> (seg + 1)) >= 1) ++seg;
   p.seg_bits = (niter > 0) ? seg : 0;
-  // Biased-binade minimum pass (int32 input; it needs at least one iteration of 2^(kBiasedR+1)
-  // Gray steps and stages fewer shared rows than the int32 pass, so the same launch shape fits).
-  // Below 2^30 states a search takes tens of microseconds, mostly kernel launches: the alternative
-  // minimum passes (each launched, the ones that do not apply exiting at once) would cost more
-  // than they save, so small problems run the int32 pass alone.
+  // Small problems run the int32 pass alone (see biased_pass_applies).
   const bool narrow_passes = n >= kNarrowPassesMinN;
   // Block-bounded minimum passes: fast variant with at least one iteration of two blocks.
   p.prune = p.variant == kFast && p.w >= kFastR + 1 && p.C >= 5;
-  p.biased = narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
+  // With block bounds the column minima are mostly skipped and the walk is the adds alone; int32
+  // adds then issue to the ALU and the FMA pipe's integer multiply-add both, which outruns the fp32
+  // adds of the biased pass, so the biased pass only runs where the bounds are off.
+  p.biased = biased_pass_applies(p) && !p.prune;
   // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
   // shared rows are 2 bytes per column.
   if (narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.C >= 10 && p.w >= kPackedR + 1) {
@@ -350,6 +357,11 @@ int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p) 
   p->upg = (uint64_t)1 << p->F;
   p->total_units = p->upg;
   return QUBO_OK;
+}
+
+void plan_without_bounds(Plan* p) {
+  p->prune = false;
+  p->biased = biased_pass_applies(*p);
 }
 
 int record_launch_count(int launches) {

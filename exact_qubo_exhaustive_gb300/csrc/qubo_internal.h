@@ -140,6 +140,7 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
 bool valid_dtype(int dtype);
 size_t dtype_bytes(int dtype);
 int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p);
+void plan_without_bounds(Plan* p);  // minimum passes that report every unit's exact minimum
 int record_launch_count(int launches);
 int record_cuda_error(cudaError_t e, const char* where);  // returns QUBO_ERR_CUDA
 std::mutex& api_mutex();      // serialises the host entry points

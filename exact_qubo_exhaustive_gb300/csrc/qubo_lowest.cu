@@ -77,7 +77,7 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
     }
   }
   // theta and the collect pass need every unit's exact minimum: no block bounds here
-  p.prune = false;
+  plan_without_bounds(&p);
   const uint64_t cap = std::max<uint64_t>(2 * want, (uint64_t)1 << 18);
 
   // one allocation: workspace | Q | candidates | counter

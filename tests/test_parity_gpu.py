@@ -81,7 +81,7 @@ def test_infeasible_explicit_plan_is_an_error(q):
 def test_plans_pick_fast_kernel_for_large_n(q):
     p = q.plan(40)
     assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
-    assert p["biased"] == 1 and p["packed"] == 1
+    assert p["pruned"] == 1 and p["biased"] == 0 and p["packed"] == 1  # block bounds: the int32 pass
     assert q.plan(8)["variant"] == 0
     assert q.plan(36, q.FP32)["biased"] == 0 and q.plan(36, q.FP32)["packed"] == 0
 
@@ -106,9 +106,10 @@ def _with_abs_sum(Q, total):
 
 @pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
 def test_biased_walk_range_limit_is_exact(q, sign):
-    # The CUDA-core minimum walk keeps column energies in the fp32 binade [2^23, 2^24) for
-    # sum |U| <= 2^22 - 1 and in int32 above. Both sides of the limit, with running values pushed
-    # to the extremes: all-negative entries reach E = -sum |U| at x = 1, all-positive ones +sum |U|.
+    # The minimum walk without block bounds (the k-lowest driver's) keeps column energies in the
+    # fp32 binade [2^23, 2^24) for sum |U| <= 2^22 - 1 and in int32 above; the bounded walk of
+    # solve() runs int32. Both sides of the limit through both, with running values pushed to the
+    # extremes: all-negative entries reach E = -sum |U| at x = 1, all-positive ones +sum |U|.
     n = 30
     lo, hi = {"mixed": (-15000, 15000), "negative": (-15000, -1), "positive": (1, 15000)}[sign]
     for total in ((1 << 22) - 1, 1 << 22):
@@ -123,6 +124,8 @@ def test_biased_walk_range_limit_is_exact(q, sign):
         e, x, t = check_int(q, Q)
         if sign == "negative":
             assert e == -total and x.all()
+        le, lx = q.solve_lowest(Q, 1)
+        assert int(le[0]) == e and (lx[0] == x).all()
 
 
 def test_int32_walk_large_values(q):
@@ -172,6 +175,8 @@ def test_packed_range_limit_is_exact(q, sign):
         e, x, t = check_int(q, Q)
         if sign == "negative":
             assert e == -total and x.all()
+        le, lx = q.solve_lowest(Q, 1)
+        assert int(le[0]) == e and (lx[0] == x).all()
 
 
 def test_packed_pass_all_ties(q):

@@ -61,9 +61,9 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(env):
 
 
 def test_interleaved_problems_of_every_minimum_pass(env):
-    # every minimum pass works in the shared array: packed 16x2 (narrow int32, n >= 30), biased
-    # fp32 binade (wide int32, n >= 30) and int32 (fp32 input's fixed-point image, n >= 30), plus
-    # a small problem; two rounds, so every call follows another problem's leftovers
+    # every minimum pass works in the shared array: packed 16x2 (narrow int32, n >= 30), the
+    # block-bounded int32 pass on wide int32 input and on fp32 input's fixed-point image (n >= 30),
+    # plus a small problem; two rounds, so every call follows another problem's leftovers
     q, torch = env
     cases = [(32, qi.random_upper_int(32, -3, 3, 81), q.INT32),
              (31, qi.random_symmetric_normal_f32(31, 82), q.FP32),
@@ -71,7 +71,7 @@ def test_interleaved_problems_of_every_minimum_pass(env):
              (20, qi.random_upper_int(20, -1, 1, 84), q.INT32),
              (30, qi.random_upper_int(30, -2, 2, 85), q.INT32)]
     plans = [q.plan(n, dt) for n, _, dt in cases]
-    assert plans[0]["packed"] == 1 and plans[2]["biased"] == 1 and plans[4]["packed"] == 1
+    assert plans[0]["packed"] == 1 and plans[2]["pruned"] == 1 and plans[4]["packed"] == 1
     wants = [with_workspace(q, torch, n, Q, dt) for n, Q, dt in cases]
     for _ in range(2):
         for (n, Q, dt), want in zip(cases, wants):
