@@ -12,6 +12,13 @@ constexpr int kChains = 16;
 template <int KIND>
 __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int* out, unsigned long long* clk) {
   const unsigned one = (unsigned)(seed > 0 ? 1 : 2);  // 1 at run time (seed is 1), unknown to the compiler
+  const int big = seed > 0 ? 0x7fffffff : 0;          // INT_MAX at run time, unknown to the compiler
+  // kinds 10..15: adds in forms the compiler cannot merge or cancel (a fused add-min against an
+  // opaque bound on the ALU, an integer multiply-add by an opaque one on the FMA pipe, fp32 adds),
+  // alone and mixed; the first kFp chains are fp32 adds, the next kMad multiply-adds, the rest
+  // add-mins
+  constexpr int kFp = KIND == 12 ? 11 : (KIND == 14 ? 10 : (KIND == 15 ? 12 : 0));
+  constexpr int kMad = KIND == 11 ? kChains : (KIND == 13 ? 8 : 0);
   int a[kChains];
   float f[kChains];
   unsigned long long f2[kChains];  // kind 9: pairs of fp32 in one 64-bit register
@@ -42,6 +49,15 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
       if (KIND == 6) a[k] = (int)__vimin3_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 7) a[k] = (int)__viaddmin_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 9) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(f2[k]) : "l"(f2[(k + 1) % kChains]));
+      if constexpr (KIND >= 10) {
+        if (k < kFp) {
+          f[k] = __fadd_rn(f[k], f[(k + 1) % kFp]);
+        } else if (k < kFp + kMad) {
+          asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(a[k]) : "r"(x), "r"((int)one));
+        } else {
+          a[k] = __viaddmin_s32(a[k], x, big);
+        }
+      }
       if (KIND == 8) {
         // int32 adds, half of them as multiply-adds by a run-time one, so that the ALU and the
         // FMA pipe's integer multiply-add unit share them
@@ -103,7 +119,13 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       case 6: return launch<6>(blocks, it, out, clk);
       case 7: return launch<7>(blocks, it, out, clk);
       case 8: return launch<8>(blocks, it, out, clk);
-      default: return launch<9>(blocks, it, out, clk);
+      case 9: return launch<9>(blocks, it, out, clk);
+      case 10: return launch<10>(blocks, it, out, clk);
+      case 11: return launch<11>(blocks, it, out, clk);
+      case 12: return launch<12>(blocks, it, out, clk);
+      case 13: return launch<13>(blocks, it, out, clk);
+      case 14: return launch<14>(blocks, it, out, clk);
+      default: return launch<15>(blocks, it, out, clk);
     }
   };
   cudaEvent_t e0 = nullptr, e1 = nullptr;

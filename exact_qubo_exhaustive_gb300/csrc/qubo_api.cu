@@ -173,12 +173,14 @@ bool generic_fits(int n, int C, int F, size_t smem_optin, size_t* smem) {
   return true;
 }
 
-// The biased-binade minimum pass: int32 input, fast variant, at least one iteration of
-// 2^(kBiasedR+1) Gray steps. Below 2^30 states a search takes tens of microseconds, mostly kernel
-// launches: the alternative minimum passes (each launched, the ones that do not apply exiting at
-// once) would cost more than they save, so small problems run the int32 pass alone.
+// The biased-binade minimum pass: fast variant, at least one iteration of 2^(kBiasedR+1) Gray
+// steps; int32 input whose sum |U| turns out below 2^22 on the device, and every fp32/fp64 input
+// (its fixed-point image is scaled to that range). Below 2^30 states a search takes tens of
+// microseconds, mostly kernel launches: the alternative minimum passes (each launched, the ones
+// that do not apply exiting at once) would cost more than they save, so small problems run the
+// int32 pass alone.
 bool biased_pass_applies(const Plan& p) {
-  return p.n >= kNarrowPassesMinN && p.variant == kFast && p.dtype == QUBO_INT32 && p.w >= kBiasedR + 1;
+  return p.n >= kNarrowPassesMinN && p.variant == kFast && p.w >= kBiasedR + 1;
 }
 
 // kind: 0 = whole problem (fixed_lo = 0), 1 = slices/range (fixed bits >= K).
@@ -273,12 +275,10 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   p.seg_bits = (niter > 0) ? seg : 0;
   // Small problems run the int32 pass alone (see biased_pass_applies).
   const bool narrow_passes = n >= kNarrowPassesMinN;
-  // Block-bounded minimum passes: fast variant with at least one iteration of two blocks.
-  p.prune = p.variant == kFast && p.w >= kFastR + 1 && p.C >= 5;
-  // With block bounds the column minima are mostly skipped and the walk is the adds alone; int32
-  // adds then issue to the ALU and the FMA pipe's integer multiply-add both, which outruns the fp32
-  // adds of the biased pass, so the biased pass only runs where the bounds are off.
-  p.biased = biased_pass_applies(p) && !p.prune;
+  p.biased = biased_pass_applies(p);
+  // The biased pass with block bounds: 2^12 columns (256 threads of 16) and at least two blocks
+  // of 2^kPruneR steps per unit.
+  p.prune = p.biased && p.C == 12 && p.threads == 256 && p.w >= kPruneR + 1;
   // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
   // shared rows are 2 bytes per column.
   if (narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.C >= 10 && p.w >= kPackedR + 1) {
@@ -359,10 +359,7 @@ int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p) 
   return QUBO_OK;
 }
 
-void plan_without_bounds(Plan* p) {
-  p->prune = false;
-  p->biased = biased_pass_applies(*p);
-}
+void plan_without_bounds(Plan* p) { p->prune = false; }
 
 int record_launch_count(int launches) {
   g_last_launches = launches;
@@ -712,7 +709,7 @@ void qubo_request_abort(void) { g_abort = 1; }
 void qubo_clear_abort(void) { g_abort = 0; }
 
 int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz) {
-  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 9) return QUBO_ERR_ARG;
+  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 15) return QUBO_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   int dev, st;
   if ((st = current_device(&dev))) return st;

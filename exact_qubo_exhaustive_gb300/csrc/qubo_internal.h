@@ -29,6 +29,7 @@ constexpr int kFastR = 4;
 constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
 constexpr int kPackedR = 5;  // register rows of the packed 16x2 minimum pass
 constexpr int kIntMinR = 5;  // register rows of the int32 minimum pass (the resolve passes keep kFastR)
+constexpr int kPruneR = 5;   // register rows of the block-bounded minimum pass: blocks of 2^kPruneR steps
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 
@@ -75,7 +76,7 @@ struct Plan {
   size_t smem_bytes = 0;   // dynamic shared memory of the enumeration kernels
   bool host_gbase = false; // group bases uploaded by the host (else one group, written on device)
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
-  bool prune = false;      // minimum passes skip the per-step minima of blocks bounded above the threshold
+  bool prune = false;      // the biased minimum pass skips the per-step minima of blocks bounded above the threshold
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
   int packed_threads = 0;  // 2^C / 32
@@ -92,7 +93,7 @@ struct Work {
   int32_t* Ec = nullptr;    // 2^C: energy of the cached variables alone
   int32_t* T = nullptr;     // 2^w (padded): walked-variable energy, in Gray order
   uint32_t* T2 = nullptr;   // packed pass: T's low 16 bits in both halves
-  int32_t* Tmin = nullptr;  // pruned minimum passes: minimum of T over each block of 2^kFastR steps
+  int32_t* Tmin = nullptr;  // block-bounded minimum pass: minimum of T over each block of 2^kPruneR steps
   int32_t* gthr = nullptr;  // pruned minimum passes: best energy published so far, per group
   int32_t* unit_min = nullptr;
   uint32_t* tied = nullptr;

@@ -9,9 +9,10 @@ namespace qgb {
 // A1: fold Q to the upper triangle and validate (one block).
 //   int32: U_ii = Q_ii, U_ij = Q_ij + Q_ji (i < j) in int64; S = sum |U_ij| must be <= 2^30 - 1.
 //   fp32/fp64: every entry finite; U64 folded in fp64; the int32 image is round(U64 * 2^s) with the
-//          largest s keeping sum |image| <= 2^30 - 1. A state's image energy then differs from
-//          2^s times its energy by at most (#selected terms)/2 <= n(n+1)/4, so every fp64
-//          minimiser lies within band = n(n+1)/2 image units of the image minimum.
+//          largest s keeping sum |image| <= 2^22 - 1 (the range of the biased fp32 minimum pass).
+//          A state's image energy then differs from 2^s times its energy by at most
+//          (#selected terms)/2 <= n(n+1)/4, so every fp64 minimiser lies within
+//          band = n(n+1)/2 image units of the image minimum.
 // ------------------------------------------------------------------------------------------------
 // gthr (optional, ngroups entries): the pruned minimum passes' per-group best, started at
 // sum |U_ij| of the int32 image, which no energy exceeds.
@@ -86,7 +87,7 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
     int sc = 0;
     if (S64 > 0.0) {
       int e;
-      frexp((double)(kMaxAbsSum - npairs) / S64, &e);  // ratio = m * 2^e, m in [0.5, 1)
+      frexp((double)(kBiasedWalkMaxAbsSum - npairs) / S64, &e);  // ratio = m * 2^e, m in [0.5, 1)
       sc = e - 1;
       sc = sc > 1074 ? 1074 : (sc < -1074 ? -1074 : sc);
     }
@@ -105,7 +106,7 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
     __syncthreads();
     atomicAdd(&s_sum, q);
     __syncthreads();
-    const bool fits = s_sum <= (unsigned long long)kMaxAbsSum;
+    const bool fits = s_sum <= (unsigned long long)kBiasedWalkMaxAbsSum;
     __syncthreads();
     if (fits) break;
     if (tid == 0) s_scale = sc - 1;
@@ -119,7 +120,8 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
     hdr->scale_exp = sc;
     hdr->band = npairs;
     hdr->tied_count = 0;
-    hdr->status = s_bad ? QUBO_ERR_NONFINITE : (s_sum <= (unsigned long long)kMaxAbsSum ? QUBO_OK : QUBO_ERR_RANGE);
+    hdr->status = s_bad ? QUBO_ERR_NONFINITE
+                        : (s_sum <= (unsigned long long)kBiasedWalkMaxAbsSum ? QUBO_OK : QUBO_ERR_RANGE);
   }
   if (gthr) {
     const int32_t top = (int32_t)(s_sum < (unsigned long long)kMaxAbsSum ? s_sum : (unsigned long long)kMaxAbsSum);
@@ -133,8 +135,9 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
 //   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
 //   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
 //   T2[i]    = (T[i] mod 2^16) in both 16-bit halves (packed pass; optional)
-//   Tmin[m]  = min of T over steps [2^kFastR m, 2^kFastR (m + 1)) (pruned minimum passes; optional,
-//              needs w > kFastR and C >= 5: then every warp of the loop lies inside the T range)
+//   Tmin[m]  = min of T over steps [32 m, 32 (m + 1)) (block-bounded minimum pass, blocks of
+//              2^kPruneR = 32 steps; optional, needs w > kPruneR and C >= 5: then every warp of the
+//              loop lies inside the T range and its 32 lanes hold one block)
 // ------------------------------------------------------------------------------------------------
 __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __restrict__ hdr,
                               const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint32_t* T2,
@@ -182,11 +185,9 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
       T[i] = acc;
       if (T2) T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
       if (Tmin) {
-        // the 2^kFastR consecutive steps of a block are consecutive lanes of this warp
-        int m = acc;
-#pragma unroll
-        for (int off = 1; off < (1 << kFastR); off <<= 1) m = min(m, __shfl_xor_sync(0xffffffffu, m, off));
-        if ((i & ((1u << kFastR) - 1)) == 0) Tmin[i >> kFastR] = m;
+        static_assert(kPruneR == 5, "one warp holds one block of walked energies");
+        const int m = __reduce_min_sync(0xffffffffu, acc);
+        if ((i & 31u) == 0) Tmin[i >> 5] = m;
       }
     }
   }
@@ -274,7 +275,7 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));
   if (p.packed) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
   if (p.prune) {
-    w.Tmin = reinterpret_cast<int32_t*>(take((nT >> kFastR) * 4 + 8));
+    w.Tmin = reinterpret_cast<int32_t*>(take((nT >> kPruneR) * 4 + 8));
     w.gthr = reinterpret_cast<int32_t*>(take((size_t)p.ngroups * 4));
   }
   w.unit_min = reinterpret_cast<int32_t*>(take(p.total_units * 4));
@@ -371,16 +372,15 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
       ++nl;
     }
     if (p.biased) {
-      // biased-binade CUDA-core pass (exits at once unless it owns the minimum pass) ...
-      e = p.prune ? launch_search_pruned(true, kp, blocks, p.threads, p.smem_bytes, stream)
+      // biased-binade CUDA-core pass, with block bounds where planned (exits at once unless it
+      // owns the minimum pass) ...
+      e = p.prune ? launch_search_biased_pruned(kp, blocks, p.threads, p.smem_bytes, stream)
                   : launch_search_biased(kp, blocks, p.threads, p.smem_bytes, stream);
       if (e != cudaSuccess) return e;
       ++nl;
     }
     // ... and the int32 CUDA-core pass (exits at once when another pass ran)
-    if (p.prune) {
-      if ((e = launch_search_pruned(false, kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
-    } else if (p.variant == kFast && p.w >= kIntMinR + 1) {
+    if (p.variant == kFast && p.w >= kIntMinR + 1) {
       if ((e = launch_search_int_min5(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
     } else if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) {
       return e;

@@ -87,7 +87,7 @@ __device__ __forceinline__ int min_walk(const WalkCtx& c, const KParams& p, int 
 template <int CPT, int R, int MODE, bool BIASED = false, bool PRUNE = false>
 __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const KParams p) {
   static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
-  static_assert(!PRUNE || (MODE == kModeMin && CPT >= 4), "pruned walk: fast layout, minimum pass");
+  static_assert(!PRUNE || (MODE == kModeMin && BIASED && CPT == 16), "pruned walk: biased minimum pass, fast layout");
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[64];
   __shared__ int s_red[32];
@@ -176,11 +176,10 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
     if constexpr (MODE == kModeMin) {
       int best;
       if constexpr (PRUNE) {
-        using VT = typename std::conditional<BIASED, float, int>::type;
-        PrunedMinWalker<CPT, R, VT> W;
+        PrunedMinWalker<R> W;
         W.init(c, p.Ec, p.M, cP);
-        W.walk(c, niter, p.Tmin, p.gthr + g, p.hdr->band);
-        best = W.aux - VOps<VT>::kBiasBits + W.s;
+        W.walk(c, niter << 1, p.Tmin, p.gthr + g, p.hdr->band);  // two blocks of 2^R steps per iteration
+        best = W.aux - VOps<float>::kBiasBits + W.s;
       } else if (niter == 0) {
         // no walked variable (generic variant only): the single walked assignment is 0
         Walker<CPT, R, MODE> W;
@@ -245,7 +244,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_int_min5(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
-cudaError_t launch_search_pruned(bool biased, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_search_biased_pruned(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_packed(int threads, size_t smem, int* blocks_per_sm);
 size_t packed_smem_bytes(int C, int w);

@@ -618,18 +618,21 @@ struct Walker {
 };
 
 // ------------------------------------------------------------------------------------------------
-// Minimum walk with block bounds (kModeMin, fast layout).
+// Minimum walk with block bounds (kModeMin, biased fp32 binade, 16 columns x 256 threads).
 //
 // Every state still costs its one add (eq. 9): each Gray step adds a walked row to all of the
-// thread's column energies. What a block bound saves is the minimum over the columns. A block is
-// the 2^R steps between two shared-memory flips; inside it only the register rows flip, so s is
-// constant and, for every step d of block m and column j,
+// thread's column energies with an fp32 add (an fp32 add is never merged or reordered by the
+// compiler, so every intermediate column energy is formed). What a block bound saves is the
+// minimum over the columns. A block is the 2^R steps between two shared-memory flips; inside it
+// only the register rows flip, so s is constant and, for every step d of block m and column j,
 //     E(d, j) - s = T[2^R m + d] + V_d[j] >= Tmin[m] + min_j V_0[j] + D_par,
-// where Tmin[m] is the smallest walked energy of the block (a table), V_0 the columns at the
-// block's first state and D_par <= 0 the most negative change of any of the thread's columns over
-// a block of that parity (the register rows alone fix it, so it is computed once per unit). When
-// that bound is above the threshold for every lane of the warp, no state of the block can be at
-// or below the threshold, and the block's per-step minima are not formed; otherwise the block is
+// where Tmin[m] is the least walked energy of the block (a table), V_0 the columns at the
+// block's first state and D_par <= 0 the most negative change of any of the thread's columns
+// over a block of that parity. A block visits every pattern of the R register bits once, so the
+// most negative change of column j is the sum of the negative parts of its signed register rows
+// (row R-1 enters added in even blocks, removed in odd ones): D_par is fixed per unit. When the
+// bound is above the threshold for every lane of the warp, no state of the block can be at or
+// below the threshold, and the block's per-step minima are not formed; otherwise the block is
 // walked with them, exactly as the plain minimum walk does.
 //
 // The threshold is min(this thread's best, G) + band. G is the best energy any block of the grid
@@ -637,93 +640,87 @@ struct Walker {
 // Every value involved is an energy some state of the group attains, so the threshold is never
 // below the group's minimum E*: a state with E <= E* + band is never in a skipped block. Hence a
 // unit holding such a state reports its minimum exactly, every other unit reports the energy of
-// a state it evaluated (above E* + band), the group minimum and the list of units within the
-// band are exactly those of the plain walk, and the resolution passes are unchanged.
+// a state it evaluated (above E* + band), and the group minimum and the list of units within the
+// band are exactly those of the plain walk; the resolution passes are unchanged.
 // ------------------------------------------------------------------------------------------------
-template <int CPT, int R, typename VT>
-struct PrunedMinWalker : Walker<CPT, R, kModeMin, VT> {
-  using B = Walker<CPT, R, kModeMin, VT>;
-  using O = typename B::O;
+template <int R>
+struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
+  using B = Walker<16, R, kModeMin, float>;
+  using O = VOps<float>;
   using RowBuf = typename B::RowBuf;
-  static constexpr int kMid = B::kMid;       // steps per block
-  static constexpr int kSteps = B::kSteps;   // steps per iteration: two blocks
-  static_assert(CPT >= 4 && R >= 2 && kMid % 4 == 0, "fast layout, whole quads of walked energies per block");
-  static constexpr int kRefreshMask = 15;    // iterations between two exchanges of the group's best
+  static constexpr int kCPT = 16;
+  static constexpr int kThreads = 256;      // 2^12 columns: the quad stride is a constant
+  static constexpr int kBlock = 1 << R;     // steps per block
+  static constexpr int kQuadsPerRow = 1024; // 2^12 / 4
+  static constexpr int kRefreshMask = 31;   // blocks between two exchanges of the group's best
+  static_assert(R >= 3, "whole quads of walked energies per block");
 
-  int dmin[2];   // D_par of the two block parities
-  int g_best;    // G: the group's best energy known to this warp (absolute, image units)
+  int dmin0, dmin1;  // D_par of even and odd blocks
+  int g_best;        // G: the group's best energy known to this warp (absolute, image units)
 
-  // Register-row flip of step L -> L + 1 of an iteration, L < kSteps - 1 and L + 1 != kMid.
-  template <int L>
-  __device__ __forceinline__ void reg_flip(VT* v) {
-    constexpr int a = ctz_c(L + 1);
-    constexpr int bit = ((L >> a) ^ (L >> (a + 1))) & 1;  // bit a of gray(L): 1 -> the flip clears it
+  // Flips of steps 0..kBlock-2 of a block; position R-1 flips once, with sign sgn (+1 in even
+  // blocks, -1 in odd ones); the others with the sign their Gray bit fixes. EXACT also forms the
+  // minimum of every step after the first.
+  template <int D, bool EXACT>
+  __device__ __forceinline__ void body(float sgn, const int4* tq) {
+    if constexpr (D + 1 < kBlock) {
+      constexpr int a = ctz_c(D + 1);
+      if constexpr (a == R - 1) {
 #pragma unroll
-    for (int jj = 0; jj < CPT; ++jj) v[jj] = bit ? O::sub(v[jj], this->Row[a][jj]) : O::add(v[jj], this->Row[a][jj]);
-  }
-
-  // Most negative change of any column from a block's first state to any of its states.
-  template <int H, int D>
-  __device__ __forceinline__ void block_drop(VT* delta, VT& lo) {
-    if constexpr (D + 1 < kMid) {
-      reg_flip<H * kMid + D>(delta);
+        for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = __fmaf_rn(this->Row[a][jj], sgn, this->V[jj]);
+      } else {
+        constexpr int bit = ((D >> a) ^ (D >> (a + 1))) & 1;  // bit a of gray(D): 1 -> the flip clears it
 #pragma unroll
-      for (int jj = 0; jj < CPT; ++jj) lo = delta[jj] < lo ? delta[jj] : lo;
-      block_drop<H, D + 1>(delta, lo);
+        for (int jj = 0; jj < kCPT; ++jj)
+          this->V[jj] = bit ? O::sub(this->V[jj], this->Row[a][jj]) : O::add(this->V[jj], this->Row[a][jj]);
+      }
+      if constexpr (EXACT)
+        this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), B::template comp<(D + 1) & 3>(tq[(D + 1) >> 2]),
+                                   this->aux);
+      body<D + 1, EXACT>(sgn, tq);
     }
   }
 
   __device__ __forceinline__ void init_bounds() {
+    float lo0 = 0.f, lo1 = 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      VT delta[CPT];
+    for (int jj = 0; jj < kCPT; ++jj) {
+      float neg = 0.f;  // sum of the negative parts of rows 0..R-2 (exact: integer-valued)
 #pragma unroll
-      for (int jj = 0; jj < CPT; ++jj) delta[jj] = O::row(0);
-      VT lo = O::row(0);
-      if (h == 0) block_drop<0, 0>(delta, lo);
-      else block_drop<1, 0>(delta, lo);
-      dmin[h] = static_cast<int>(lo);  // exact: an integer-valued fp32 number for the biased walk
+      for (int a = 0; a < R - 1; ++a) neg = __fadd_rn(neg, fminf(this->Row[a][jj], 0.f));
+      const float r = this->Row[R - 1][jj];
+      lo0 = fminf(lo0, __fadd_rn(neg, fminf(r, 0.f)));
+      lo1 = fminf(lo1, __fadd_rn(neg, fminf(-r, 0.f)));
     }
+    dmin0 = static_cast<int>(lo0);
+    dmin1 = static_cast<int>(lo1);
   }
 
-  // Steps of one block: the register flips, and (EXACT) the per-step minima of steps 1..kMid-1.
-  template <int H, int D, bool EXACT>
-  __device__ __forceinline__ void block_steps(const int4* tq) {
-    if constexpr (D + 1 < kMid) {
-      reg_flip<H * kMid + D>(this->V);
-      if constexpr (EXACT)
-        this->aux = __viaddmin_s32(vmin_bits<VT, CPT>(this->V), B::template comp<(D + 1) & 3>(tq[(D + 1) >> 2]), this->aux);
-      block_steps<H, D + 1, EXACT>(tq);
-    }
+  // The shared-memory row of position R + rr into rb.
+  __device__ __forceinline__ void load_row(const WalkCtx& c, int rr, RowBuf& rb) const {
+    const float4* rp = reinterpret_cast<const float4*>(c.rows4) + rr * kQuadsPerRow + c.thread;
+#pragma unroll
+    for (int k = 0; k < kCPT / 4; ++k) rb.q[k] = rp[k * kThreads];
   }
 
   // One block: bound test, then the walk with or without per-step minima. On return V holds the
-  // block's last state; `rb` holds the row of the flip that follows (position a_next).
-  template <int H>
-  __device__ __forceinline__ void block(const WalkCtx& c, uint64_t m, int tmin, int a_next, int band, RowBuf& rb) {
-    this->load_dyn_row(c, a_next, rb);
-    const int m0 = vmin_bits<VT, CPT>(this->V);
-    bool skip;
-    if constexpr (O::kInt) {
-      // int32 image of up to 2^30: the bound can leave int32, so compare in 64 bits
-      const long long lb = (long long)m0 + tmin + dmin[H];
-      const long long th = (long long)min(this->aux, g_best - this->s) + band;
-      skip = lb > th;
-    } else {
-      // biased binade: |every term| <= 4 sum|U| < 2^24, far inside int32 around the bias
-      const int lb = m0 + tmin + dmin[H];
-      const int th = min(this->aux, O::kBiasBits + g_best - this->s) + band;
-      skip = lb > th;
-    }
-    if (__all_sync(0xffffffffu, skip)) {
-      block_steps<H, 0, false>(nullptr);
+  // block's last state.
+  __device__ __forceinline__ void block(const WalkCtx& c, uint64_t m, int tmin, int band) {
+    const int par = static_cast<int>(m & 1);
+    const float sgn = par ? -1.f : 1.f;
+    const int m0 = vmin_bits<float, kCPT>(this->V);
+    // biased binade: |every term| <= 4 sum|U| < 2^24, far inside int32 around the bias
+    const int lb = m0 + tmin + (par ? dmin1 : dmin0);
+    const int th = min(this->aux, O::kBiasBits + g_best - this->s) + band;
+    if (__all_sync(0xffffffffu, lb > th)) {
+      body<0, false>(sgn, nullptr);
     } else {
       const int4* T4 = reinterpret_cast<const int4*>(c.T) + (m << (R - 2));
-      int4 tq[kMid / 4];
+      int4 tq[kBlock / 4];
 #pragma unroll
-      for (int q = 0; q < kMid / 4; ++q) tq[q] = __ldg(T4 + q);
+      for (int q = 0; q < kBlock / 4; ++q) tq[q] = __ldg(T4 + q);
       this->aux = __viaddmin_s32(m0, tq[0].x, this->aux);
-      block_steps<H, 0, true>(tq);
+      body<0, true>(sgn, tq);
     }
   }
 
@@ -738,28 +735,41 @@ struct PrunedMinWalker : Walker<CPT, R, kModeMin, VT> {
     g_best = v < g_best ? v : g_best;
   }
 
-  // Whole unit: niter iterations of two blocks. Tmin: block minima of T (2 per iteration);
-  // gbest: the group's published best (absolute image units); band: resolution band.
-  __device__ __forceinline__ void walk(const WalkCtx& c, int64_t niter, const int* __restrict__ Tmin, int* gbest,
+  // Whole unit: nblocks blocks of 2^R steps, each but the last followed by the flip of shared row
+  // ctz(m + 1). Tmin: block minima of T; gbest: the group's published best (absolute image
+  // units); band: resolution band.
+  __device__ __forceinline__ void walk(const WalkCtx& c, int64_t nblocks, const int* __restrict__ Tmin, int* gbest,
                                        int band) {
     init_bounds();
     g_best = __ldcg(gbest);
     // a real best from the first state's columns, so the running best never leaves its range
-    this->aux = __viaddmin_s32(vmin_bits<VT, CPT>(this->V), __ldg(c.T), kIntInf);
-    const int2* Tm2 = reinterpret_cast<const int2*>(Tmin);
-    int2 tm = __ldg(Tm2);
-    for (int64_t iter = 0; iter < niter; ++iter) {
-      const uint64_t base = static_cast<uint64_t>(iter) << (R + 1);
-      const bool flip_end = iter + 1 < niter;
-      const int a_end = flip_end ? R + 1 + __ffsll(static_cast<long long>(iter + 1)) - 1 : R;
-      const int2 tm_next = __ldg(Tm2 + (flip_end ? iter + 1 : iter));
+    this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), __ldg(c.T), kIntInf);
+    int tm = __ldg(Tmin);
+    for (int64_t m = 0; m < nblocks; ++m) {
+      const bool more = m + 1 < nblocks;
+      const int tm_next = __ldg(Tmin + (more ? m + 1 : m));
+      const int rr = more ? __ffsll(static_cast<long long>(m + 1)) - 1 : 0;  // row of the next flip
       RowBuf rb;
-      block<0>(c, static_cast<uint64_t>(iter) << 1, tm.x, R, band, rb);
-      this->apply_dyn_row(c, R, rb, (iter & 1) == 0);
-      block<1>(c, (static_cast<uint64_t>(iter) << 1) | 1, tm.y, a_end, band, rb);
-      if (flip_end) this->apply_dyn_row(c, a_end, rb, ((gray_code(base + kSteps - 1) >> a_end) & 1u) == 0);
+      load_row(c, rr, rb);  // in flight while the block is walked
+      block(c, static_cast<uint64_t>(m), tm, band);
+      if (more) {
+        // position R + rr becomes set unless the next bit of m + 1 is set (reflected Gray code)
+        const bool up = !((static_cast<uint64_t>(m + 1) >> (rr + 1)) & 1u);
+        const float dsgn = up ? 1.f : -1.f;
+#pragma unroll
+        for (int k = 0; k < kCPT / 4; ++k) {
+          this->V[4 * k + 0] = __fmaf_rn(rb.q[k].x, dsgn, this->V[4 * k + 0]);
+          this->V[4 * k + 1] = __fmaf_rn(rb.q[k].y, dsgn, this->V[4 * k + 1]);
+          this->V[4 * k + 2] = __fmaf_rn(rb.q[k].z, dsgn, this->V[4 * k + 2]);
+          this->V[4 * k + 3] = __fmaf_rn(rb.q[k].w, dsgn, this->V[4 * k + 3]);
+        }
+        const int Lv = c.sL[c.n - c.C - 1 - (R + rr)];
+        const int dl = up ? Lv : -Lv;
+        this->s += dl;
+        this->aux -= dl;
+      }
       tm = tm_next;
-      if ((iter & kRefreshMask) == kRefreshMask) exchange_best(gbest);
+      if ((m & kRefreshMask) == kRefreshMask) exchange_best(gbest);
     }
   }
 };

@@ -274,7 +274,11 @@ QUBO_API void qubo_clear_abort(void);
  * kind: 0 int32 add, 1 int32 min, 2 int32 3-input min, 3 int32 add-then-min (fused),
  *       4 fp32 add, 5 fp32 min, 6 packed 16x2 3-input min, 7 packed 16x2 add-then-min,
  *       8 int32 add with half of the adds issued as integer multiply-adds by one (FMA pipe),
- *       9 packed fp32x2 add (two adds per instruction; counted as two operations). */
+ *       9 packed fp32x2 add (two adds per instruction; counted as two operations),
+ *       10 int32 add as a fused add-min against an opaque INT_MAX (ALU; cannot be merged),
+ *       11 int32 add as a multiply-add by an opaque one (FMA pipe; cannot be merged),
+ *       12 / 14 / 15: 11 / 10 / 12 of the 16 chains fp32 adds, the rest kind-10 adds,
+ *       13: 8 chains kind 11, 8 chains kind 10. */
 QUBO_API int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz);
 
 #ifdef __cplusplus

@@ -81,7 +81,7 @@ def test_infeasible_explicit_plan_is_an_error(q):
 def test_plans_pick_fast_kernel_for_large_n(q):
     p = q.plan(40)
     assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
-    assert p["pruned"] == 1 and p["biased"] == 0 and p["packed"] == 1  # block bounds: the int32 pass
+    assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 1
     assert q.plan(8)["variant"] == 0
     assert q.plan(36, q.FP32)["biased"] == 0 and q.plan(36, q.FP32)["packed"] == 0
 
