@@ -83,7 +83,8 @@ def test_plans_pick_fast_kernel_for_large_n(q):
     assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
     assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 1
     assert q.plan(8)["variant"] == 0
-    assert q.plan(36, q.FP32)["biased"] == 0 and q.plan(36, q.FP32)["packed"] == 0
+    # fp32 input: its fixed-point image is scaled into the biased pass's range; never packed
+    assert q.plan(36, q.FP32)["biased"] == 1 and q.plan(36, q.FP32)["packed"] == 0
 
 
 @pytest.mark.parametrize("n,seed", [(16, 1), (17, 2), (19, 3), (23, 4), (27, 5)])
