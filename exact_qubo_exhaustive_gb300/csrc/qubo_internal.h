@@ -40,6 +40,18 @@ constexpr int64_t kBiasedWalkMaxAbsSum = (int64_t(1) << 22) - 1;
 // stay inside (-2^15, 2^15) when sum |U| < 2^14.
 constexpr int64_t kPackedMaxAbsSum = (int64_t(1) << 14) - 1;
 
+// Per block of 2^kPruneR Gray steps (block-bounded minimum pass): the block's least walked
+// energy and the shared-row flip that follows it, precomputed once per launch (the same for every
+// unit): the row's float4 offset in shared memory, its sign (+1 sets the variable, -1 clears it,
+// 0 after the last block: no flip) and the index of its signed linear term in the walker's
+// table of +L, -L and a zero.
+struct alignas(16) BlockCtl {
+  int32_t tmin;
+  int32_t row;
+  float dsgn;
+  int32_t lvx;
+};
+
 // Written by the device, read back by the host (lives at the start of the workspace).
 struct DevHeader {
   int32_t status;      // QUBO_OK or an error code found on the device
@@ -93,7 +105,7 @@ struct Work {
   int32_t* Ec = nullptr;    // 2^C: energy of the cached variables alone
   int32_t* T = nullptr;     // 2^w (padded): walked-variable energy, in Gray order
   uint32_t* T2 = nullptr;   // packed pass: T's low 16 bits in both halves
-  int32_t* Tmin = nullptr;  // block-bounded minimum pass: minimum of T over each block of 2^kPruneR steps
+  BlockCtl* blk = nullptr;  // block-bounded minimum pass: one entry per block of 2^kPruneR steps (+ 1)
   int32_t* gthr = nullptr;  // pruned minimum passes: best energy published so far, per group
   int32_t* unit_min = nullptr;
   uint32_t* tied = nullptr;

@@ -135,13 +135,15 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
 //   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
 //   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
 //   T2[i]    = (T[i] mod 2^16) in both 16-bit halves (packed pass; optional)
-//   Tmin[m]  = min of T over steps [32 m, 32 (m + 1)) (block-bounded minimum pass, blocks of
-//              2^kPruneR = 32 steps; optional, needs w > kPruneR and C >= 5: then every warp of the
-//              loop lies inside the T range and its 32 lanes hold one block)
+//   blk[m]   = block m of 2^kPruneR = 32 steps (block-bounded minimum pass; optional, needs
+//              w > kPruneR and C >= 5: then every warp of the loop lies inside the T range and its
+//              32 lanes hold one block): the least T of the block and the flip that follows it,
+//              position kPruneR + ctz(m + 1), set unless bit ctz(m + 1) + 1 of m + 1 is set
+//              (reflected Gray code); blk[2^(w-5) - 1] and the padding entry after it: no flip
 // ------------------------------------------------------------------------------------------------
 __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __restrict__ hdr,
                               const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint32_t* T2,
-                              int32_t* Tmin, uint64_t nTpad) {
+                              BlockCtl* blk, uint64_t nTpad) {
   if (hdr->status != QUBO_OK) return;
   const int ncols = 1 << C;
   const uint64_t nM = (uint64_t)(n - C) << C;
@@ -184,10 +186,27 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
       }
       T[i] = acc;
       if (T2) T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
-      if (Tmin) {
+      if (blk) {
         static_assert(kPruneR == 5, "one warp holds one block of walked energies");
-        const int m = __reduce_min_sync(0xffffffffu, acc);
-        if ((i & 31u) == 0) Tmin[i >> 5] = m;
+        const int tmin = __reduce_min_sync(0xffffffffu, acc);
+        if ((i & 31u) == 0) {
+          const uint32_t m = (uint32_t)(i >> 5), nb = 1u << (w - kPruneR);
+          BlockCtl b;
+          b.tmin = tmin;
+          if (m + 1 < nb) {
+            const int rr = __ffs((int)(m + 1)) - 1;
+            const bool up = !(((m + 1) >> (rr + 1)) & 1u);
+            b.row = rr << (C - 2);
+            b.dsgn = up ? 1.f : -1.f;
+            b.lvx = (up ? 0 : 64) + (n - C - 1 - (kPruneR + rr));
+          } else {
+            b.row = 0;
+            b.dsgn = 0.f;
+            b.lvx = 128;
+          }
+          blk[m] = b;
+          if (m + 1 == nb) blk[nb] = b;  // padding: the walk reads one entry ahead
+        }
       }
     }
   }
@@ -275,7 +294,7 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));
   if (p.packed) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
   if (p.prune) {
-    w.Tmin = reinterpret_cast<int32_t*>(take((nT >> kPruneR) * 4 + 8));
+    w.blk = reinterpret_cast<BlockCtl*>(take(((nT >> kPruneR) + 1) * sizeof(BlockCtl)));
     w.gthr = reinterpret_cast<int32_t*>(take((size_t)p.ngroups * 4));
   }
   w.unit_min = reinterpret_cast<int32_t*>(take(p.total_units * 4));
@@ -314,7 +333,7 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   const uint64_t nTpad = ((uint64_t)1 << p.w) < 4 ? 4 : ((uint64_t)1 << p.w);
   const uint64_t tab_work = ((uint64_t)(p.n - p.C) << p.C) + ((uint64_t)1 << p.C) + nTpad;
   const int tab_blocks = (int)((tab_work + 255) / 256 < 4096 ? (tab_work + 255) / 256 : 4096);
-  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, w.Tmin, nTpad);
+  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, w.blk, nTpad);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
@@ -336,7 +355,7 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   kp.Ec = w.Ec;
   kp.T = w.T;
   kp.T2 = w.T2;
-  kp.Tmin = w.Tmin;
+  kp.blk = w.blk;
   kp.gthr = w.gthr;
   kp.gbase = w.gbase;
   kp.unit_min = w.unit_min;

@@ -24,7 +24,7 @@ struct KParams {
   const int32_t* Ec;
   const int32_t* T;
   const uint32_t* T2;       // packed pass: T's low 16 bits in both halves
-  const int32_t* Tmin;      // pruned minimum passes: block minima of T
+  const BlockCtl* blk;      // block-bounded minimum pass: per-block minimum of T and following flip
   int32_t* gthr;            // pruned minimum passes: best energy published so far, per group
   const uint64_t* gbase;
   int32_t* unit_min;
@@ -89,7 +89,8 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
   static_assert(!PRUNE || (MODE == kModeMin && BIASED && CPT == 16), "pruned walk: biased minimum pass, fast layout");
   extern __shared__ __align__(16) int4 s_rows4[];
-  __shared__ int sL[64];
+  // linear terms; the block-bounded pass also keeps -L at 64 + v and a zero at 128
+  __shared__ int sL[PRUNE ? 129 : 64];
   __shared__ int s_red[32];
   // resolve modes: per-thread slots for the out-of-line candidate scan
   __shared__ __align__(16) int s_slot[(MODE != kModeMin && CPT >= 4) ? kFastThreadsMax * CPT : 4];
@@ -169,6 +170,10 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 
     __syncthreads();  // previous item is done with sL; staged rows are visible
     unit_linear_terms(p.U, n, F, P, sL, tid, nthreads);
+    if constexpr (PRUNE) {
+      __syncthreads();
+      for (int v = tid; v <= 64; v += nthreads) sL[64 + v] = v < n ? -sL[v] : 0;
+    }
     __syncthreads();
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
@@ -178,7 +183,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
       if constexpr (PRUNE) {
         PrunedMinWalker<R> W;
         W.init(c, p.Ec, p.M, cP);
-        W.walk(c, niter << 1, p.Tmin, p.gthr + g, p.hdr->band);  // two blocks of 2^R steps per iteration
+        W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band);  // two blocks per iteration
         best = W.aux - VOps<float>::kBiasBits + W.s;
       } else if (niter == 0) {
         // no walked variable (generic variant only): the single walked assignment is 0

@@ -625,8 +625,8 @@ struct Walker {
 // compiler, so every intermediate column energy is formed). What a block bound saves is the
 // minimum over the columns. A block is the 2^R steps between two shared-memory flips; inside it
 // only the register rows flip, so s is constant and, for every step d of block m and column j,
-//     E(d, j) - s = T[2^R m + d] + V_d[j] >= Tmin[m] + min_j V_0[j] + D_par,
-// where Tmin[m] is the least walked energy of the block (a table), V_0 the columns at the
+//     E(d, j) - s = T[2^R m + d] + V_d[j] >= Tmin_m + min_j V_0[j] + D_par,
+// where Tmin_m is the least walked energy of the block (a table), V_0 the columns at the
 // block's first state and D_par <= 0 the most negative change of any of the thread's columns
 // over a block of that parity. A block visits every pattern of the R register bits once, so the
 // most negative change of column j is the sum of the negative parts of its signed register rows
@@ -651,7 +651,6 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   static constexpr int kCPT = 16;
   static constexpr int kThreads = 256;      // 2^12 columns: the quad stride is a constant
   static constexpr int kBlock = 1 << R;     // steps per block
-  static constexpr int kQuadsPerRow = 1024; // 2^12 / 4
   static constexpr int kRefreshMask = 31;   // blocks between two exchanges of the group's best
   static_assert(R >= 3, "whole quads of walked energies per block");
 
@@ -659,10 +658,9 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   int g_best;        // G: the group's best energy known to this warp (absolute, image units)
 
   // Flips of steps 0..kBlock-2 of a block; position R-1 flips once, with sign sgn (+1 in even
-  // blocks, -1 in odd ones); the others with the sign their Gray bit fixes. EXACT also forms the
-  // minimum of every step after the first.
-  template <int D, bool EXACT>
-  __device__ __forceinline__ void body(float sgn, const int4* tq) {
+  // blocks, -1 in odd ones); the others with the sign their Gray bit fixes.
+  template <int D>
+  __device__ __forceinline__ void body(float sgn) {
     if constexpr (D + 1 < kBlock) {
       constexpr int a = ctz_c(D + 1);
       if constexpr (a == R - 1) {
@@ -674,10 +672,7 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
         for (int jj = 0; jj < kCPT; ++jj)
           this->V[jj] = bit ? O::sub(this->V[jj], this->Row[a][jj]) : O::add(this->V[jj], this->Row[a][jj]);
       }
-      if constexpr (EXACT)
-        this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), B::template comp<(D + 1) & 3>(tq[(D + 1) >> 2]),
-                                   this->aux);
-      body<D + 1, EXACT>(sgn, tq);
+      body<D + 1>(sgn);
     }
   }
 
@@ -696,31 +691,52 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
     dmin1 = static_cast<int>(lo1);
   }
 
-  // The shared-memory row of position R + rr into rb.
-  __device__ __forceinline__ void load_row(const WalkCtx& c, int rr, RowBuf& rb) const {
-    const float4* rp = reinterpret_cast<const float4*>(c.rows4) + rr * kQuadsPerRow + c.thread;
-#pragma unroll
-    for (int k = 0; k < kCPT / 4; ++k) rb.q[k] = rp[k * kThreads];
-  }
-
   // One block: bound test, then the walk with or without per-step minima. On return V holds the
-  // block's last state.
-  __device__ __forceinline__ void block(const WalkCtx& c, uint64_t m, int tmin, int band) {
-    const int par = static_cast<int>(m & 1);
-    const float sgn = par ? -1.f : 1.f;
+  // block's last state. lbo = the block's least walked energy + D_par - band; thr = min(this
+  // thread's best, G) relative to s, both in the biased bit image.
+  __device__ __forceinline__ void block(const WalkCtx& c, int m, int lbo, int thr, float sgn) {
     const int m0 = vmin_bits<float, kCPT>(this->V);
     // biased binade: |every term| <= 4 sum|U| < 2^24, far inside int32 around the bias
-    const int lb = m0 + tmin + (par ? dmin1 : dmin0);
-    const int th = min(this->aux, O::kBiasBits + g_best - this->s) + band;
-    if (__all_sync(0xffffffffu, lb > th)) {
-      body<0, false>(sgn, nullptr);
+    if (__all_sync(0xffffffffu, m0 + lbo > thr)) {
+      body<0>(sgn);
     } else {
-      const int4* T4 = reinterpret_cast<const int4*>(c.T) + (m << (R - 2));
-      int4 tq[kBlock / 4];
+      exact_block(c, m, m0, sgn);
+    }
+  }
+
+  // Flip of a register row whose position and sign are known at run time.
+  __device__ __forceinline__ void flip_rt(const float* row, float sg) {
 #pragma unroll
-      for (int q = 0; q < kBlock / 4; ++q) tq[q] = __ldg(T4 + q);
-      this->aux = __viaddmin_s32(m0, tq[0].x, this->aux);
-      body<0, true>(sgn, tq);
+    for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = __fmaf_rn(row[jj], sg, this->V[jj]);
+  }
+
+  // The block walked with every per-step minimum (rare: the bound did not clear it). A loop over
+  // groups of four steps keeps the code small: in group k the flips of steps 4k and 4k + 2 are
+  // row 0 (+, -), of step 4k + 1 row 1 (- when k is odd), of step 4k + 3 row 2 + ctz(k + 1).
+  __device__ __forceinline__ void exact_block(const WalkCtx& c, int m, int m0, float sgn) {
+    static_assert(R == 5, "groups of four steps: rows 0 and 1 inside, rows 2..4 between");
+    const int4* T4 = reinterpret_cast<const int4*>(c.T) + (static_cast<uint32_t>(m) << (R - 2));
+    int4 tq = __ldg(T4);
+    this->aux = __viaddmin_s32(m0, tq.x, this->aux);
+#pragma unroll 1
+    for (int k = 0; k < kBlock / 4; ++k) {
+#pragma unroll
+      for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = O::add(this->V[jj], this->Row[0][jj]);
+      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.y, this->aux);
+      flip_rt(this->Row[1], (k & 1) ? -1.f : 1.f);
+      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.z, this->aux);
+#pragma unroll
+      for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = O::sub(this->V[jj], this->Row[0][jj]);
+      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.w, this->aux);
+      if (k + 1 == kBlock / 4) break;  // the block's last state
+      const int a = 2 + __ffs(k + 1) - 1;
+      const int d = 4 * k + 3;
+      const float sg = (a == R - 1) ? sgn : ((((d >> a) ^ (d >> (a + 1))) & 1) ? -1.f : 1.f);
+      if (a == 2) flip_rt(this->Row[2], sg);
+      else if (a == 3) flip_rt(this->Row[3], sg);
+      else flip_rt(this->Row[4], sg);
+      tq = __ldg(T4 + k + 1);
+      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.x, this->aux);
     }
   }
 
@@ -735,40 +751,44 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
     g_best = v < g_best ? v : g_best;
   }
 
-  // Whole unit: nblocks blocks of 2^R steps, each but the last followed by the flip of shared row
-  // ctz(m + 1). Tmin: block minima of T; gbest: the group's published best (absolute image
-  // units); band: resolution band.
-  __device__ __forceinline__ void walk(const WalkCtx& c, int64_t nblocks, const int* __restrict__ Tmin, int* gbest,
+  // Whole unit: nblocks (even, < 2^31) blocks of 2^R steps, each but the last followed by a
+  // shared-row flip; blk: per-block control (least T, the flip that follows; one padding entry);
+  // c.sL holds L, -L at 64 + v and a zero at 128. gbest: the group's published best (absolute
+  // image units); band: resolution band.
+  __device__ __forceinline__ void walk(const WalkCtx& c, int nblocks, const BlockCtl* __restrict__ blk, int* gbest,
                                        int band) {
     init_bounds();
+    const int dmb0 = dmin0 - band, dmb1 = dmin1 - band;
     g_best = __ldcg(gbest);
     // a real best from the first state's columns, so the running best never leaves its range
     this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), __ldg(c.T), kIntInf);
-    int tm = __ldg(Tmin);
-    for (int64_t m = 0; m < nblocks; ++m) {
-      const bool more = m + 1 < nblocks;
-      const int tm_next = __ldg(Tmin + (more ? m + 1 : m));
-      const int rr = more ? __ffsll(static_cast<long long>(m + 1)) - 1 : 0;  // row of the next flip
+    const int4* ctl4 = reinterpret_cast<const int4*>(blk);
+    const float4* rows = reinterpret_cast<const float4*>(c.rows4) + c.thread;
+    int4 ctl = __ldg(ctl4);
+    for (int m = 0; m < nblocks; ++m) {
+      const int4 next = __ldg(ctl4 + m + 1);  // one block ahead (the table has a padding entry)
       RowBuf rb;
-      load_row(c, rr, rb);  // in flight while the block is walked
-      block(c, static_cast<uint64_t>(m), tm, band);
-      if (more) {
-        // position R + rr becomes set unless the next bit of m + 1 is set (reflected Gray code)
-        const bool up = !((static_cast<uint64_t>(m + 1) >> (rr + 1)) & 1u);
-        const float dsgn = up ? 1.f : -1.f;
+      {
+        const float4* rp = rows + ctl.y;  // in flight while the block is walked
 #pragma unroll
-        for (int k = 0; k < kCPT / 4; ++k) {
-          this->V[4 * k + 0] = __fmaf_rn(rb.q[k].x, dsgn, this->V[4 * k + 0]);
-          this->V[4 * k + 1] = __fmaf_rn(rb.q[k].y, dsgn, this->V[4 * k + 1]);
-          this->V[4 * k + 2] = __fmaf_rn(rb.q[k].z, dsgn, this->V[4 * k + 2]);
-          this->V[4 * k + 3] = __fmaf_rn(rb.q[k].w, dsgn, this->V[4 * k + 3]);
-        }
-        const int Lv = c.sL[c.n - c.C - 1 - (R + rr)];
-        const int dl = up ? Lv : -Lv;
-        this->s += dl;
-        this->aux -= dl;
+        for (int k = 0; k < kCPT / 4; ++k) rb.q[k] = rp[k * kThreads];
       }
-      tm = tm_next;
+      const bool odd = m & 1;
+      const int thr = min(this->aux, O::kBiasBits + g_best - this->s);
+      block(c, m, ctl.x + (odd ? dmb1 : dmb0), thr, odd ? -1.f : 1.f);
+      // the flip that follows (a no-op after the last block: sign 0, linear term 0)
+      const float dsgn = __int_as_float(ctl.z);
+#pragma unroll
+      for (int k = 0; k < kCPT / 4; ++k) {
+        this->V[4 * k + 0] = __fmaf_rn(rb.q[k].x, dsgn, this->V[4 * k + 0]);
+        this->V[4 * k + 1] = __fmaf_rn(rb.q[k].y, dsgn, this->V[4 * k + 1]);
+        this->V[4 * k + 2] = __fmaf_rn(rb.q[k].z, dsgn, this->V[4 * k + 2]);
+        this->V[4 * k + 3] = __fmaf_rn(rb.q[k].w, dsgn, this->V[4 * k + 3]);
+      }
+      const int dl = c.sL[ctl.w];
+      this->s += dl;
+      this->aux -= dl;
+      ctl = next;
       if ((m & kRefreshMask) == kRefreshMask) exchange_best(gbest);
     }
   }
