@@ -10,8 +10,8 @@ record) through the library's C ABI.
   e2e   : the host API (qubo_solve) from pinned host memory: H2D of Q and D2H of the result are
           inside the timed region (wall clock, synchronised).
   roofline: the enumeration kernel's own duration (CUDA events the library records around its
-          launches), one int32 add per state, against the INT32 issue roofline of the part:
-          152 SMs x 128 lanes/clk x 2.07 GHz.
+          launches), one add per state (an exact fp32 add), against the issue roofline of the part:
+          152 SMs x 128 lanes/clk x 2.07 GHz; also against the measured fp32-add and int32-add rates.
   cpu_baseline / --impl reference: the CPU oracle (test infrastructure, plain C + OpenMP) on a
           bounded sample of the same workload, on the host's cores.
 
@@ -52,7 +52,7 @@ SMS = 152
 LANES_PER_CLK = 128          # issue-limited int32 lanes per SM per clock (ALU + FMA-heavy pipes)
 MAX_SM_MHZ = 2070.0
 PROFILE = os.path.join(ROOT, "profiles", "search_kernel_n40.md")
-KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_pruned.cu", "qubo_internal.h"]
+KERNEL_SOURCES = ["qubo_walk.cuh", "qubo_search_kernel.cuh", "qubo_search_pruned.cu", "qubo_internal.h", "qubo_search.cu"]
 
 
 SHARD_K = 12                 # slices of the multi-GPU split: 2^12, divisible by 1, 2, 4 and 8 ranks
@@ -357,6 +357,10 @@ def run_gb300(args):
     probes = [q.probe_alu(kind, 20000) for kind in (0, 8)]
     best_ops, probe_mhz = max(probes, key=lambda t: t[0])
     r_int = best_ops / 1e12
+    # the add the kernel issues is an fp32 add (exact integers in the binade [2^23, 2^24)): its
+    # measured rate is the roofline of the pipe the kernel runs on
+    fadd_ops, fadd_mhz = q.probe_alu(4, 20000)
+    r_fadd = fadd_ops / 1e12
     traffic, traffic_src = profiled_traffic()
 
     extra = {}
@@ -375,14 +379,20 @@ def run_gb300(args):
                    "tie_count": int(r["tie_count"]), "checks": checks},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "search_kernel<16,4,min,biased,pruned> (enumeration, biased fp32-binade minimum pass with block bounds)", "kernel_ms": kern,
+                     "kernel": "search_kernel<16,5,min,biased,bounded> (enumeration, biased fp32-binade minimum pass with block bounds)", "kernel_ms": kern,
                      "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
                                    "add per state) x 2.07 GHz max SM clock",
                      "traffic_source": traffic_src,
+                     "measured_fp32_add_peak": r_fadd,
+                     "frac_of_measured_fp32_add": achieved / r_fadd,
+                     "measured_fp32_add_basis": (f"qubo_probe_alu fp32 add chains: {fadd_ops / (SMS * fadd_mhz * 1e6):.1f} "
+                                                 f"lanes/clk/SM at {fadd_mhz:.0f} MHz x {SMS} SMs; the kernel's one add "
+                                                 "per state is an fp32 add (ncu: 2^n fp32 add lane-ops per launch)"),
                      "measured_int32_add_peak": r_int,
                      "frac_of_measured_int32_add": achieved / r_int,
                      "measured_int32_add_basis": (f"qubo_probe_alu int32 add chains: {best_ops / (SMS * probe_mhz * 1e6):.1f} "
-                                                  f"lanes/clk/SM at {probe_mhz:.0f} MHz x {SMS} SMs"),
+                                                  f"lanes/clk/SM at {probe_mhz:.0f} MHz x {SMS} SMs; above 1 because the "
+                                                  "kernel's adds are fp32 adds, which this part issues faster than int32 adds"),
                      "frac_at_measured_clock": (achieved / (SMS * LANES_PER_CLK * clocks["sm_mhz"] * 1e-6)
                                                 if clocks.get("sm_mhz") else None)},
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": N * N * 4,
@@ -481,7 +491,7 @@ def run_gb300_sharded(args):
                        "checks": checks},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                          "frac": achieved / peak, "traffic": None,
-                         "kernel": "search_kernel<16,4,min,biased,pruned> on rank 0's shard", "kernel_ms": kern,
+                         "kernel": "search_kernel<16,5,min,biased,bounded> on rank 0's shard", "kernel_ms": kern,
                          "kernel_ms_max_over_ranks": kern_max,
                          "peak_basis": "152 SMs x 128 lanes/clk x 2.07 GHz max SM clock"},
             "e2e": {"value": STATES / (e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": world * N * N * 4,
