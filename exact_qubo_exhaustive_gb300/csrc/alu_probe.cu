@@ -21,11 +21,13 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
   constexpr int kMad = KIND == 11 ? kChains : (KIND == 13 ? 8 : 0);
   int a[kChains];
   float f[kChains];
+  float rinv[kChains];  // kind 16: loop-invariant addends
   unsigned long long f2[kChains];  // kind 9: pairs of fp32 in one 64-bit register
 #pragma unroll
   for (int k = 0; k < kChains; ++k) {
     a[k] = (threadIdx.x * 7 + k * 13 + seed) & 1023;
     f[k] = (float)a[k] * 0.5f;
+    rinv[k] = (float)((k * 37 + seed) & 63);
     f2[k] = 0;
     if constexpr (KIND == 9) {  // only kind 9 carries the packed pairs (the other kinds' code stays as it was)
       const float lo = f[k], hi = f[k] + 1.0f;
@@ -49,7 +51,11 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
       if (KIND == 6) a[k] = (int)__vimin3_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 7) a[k] = (int)__viaddmin_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 9) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(f2[k]) : "l"(f2[(k + 1) % kChains]));
-      if constexpr (KIND >= 10) {
+      if constexpr (KIND == 16) {
+        // fp32 adds of loop-invariant addends into 16 accumulators, alternating add and subtract:
+        // the pattern of the walk's column updates (V[j] +-= Row[a][j])
+        f[k] = (k & 1) ? __fsub_rn(f[k], rinv[k]) : __fadd_rn(f[k], rinv[k]);
+      } else if constexpr (KIND >= 10) {
         if (k < kFp) {
           f[k] = __fadd_rn(f[k], f[(k + 1) % kFp]);
         } else if (k < kFp + kMad) {
@@ -125,7 +131,8 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       case 12: return launch<12>(blocks, it, out, clk);
       case 13: return launch<13>(blocks, it, out, clk);
       case 14: return launch<14>(blocks, it, out, clk);
-      default: return launch<15>(blocks, it, out, clk);
+      case 15: return launch<15>(blocks, it, out, clk);
+      default: return launch<16>(blocks, it, out, clk);
     }
   };
   cudaEvent_t e0 = nullptr, e1 = nullptr;

@@ -709,7 +709,7 @@ void qubo_request_abort(void) { g_abort = 1; }
 void qubo_clear_abort(void) { g_abort = 0; }
 
 int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz) {
-  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 15) return QUBO_ERR_ARG;
+  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 16) return QUBO_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   int dev, st;
   if ((st = current_device(&dev))) return st;

@@ -29,7 +29,7 @@ constexpr int kFastR = 4;
 constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
 constexpr int kPackedR = 5;  // register rows of the packed 16x2 minimum pass
 constexpr int kIntMinR = 5;  // register rows of the int32 minimum pass (the resolve passes keep kFastR)
-constexpr int kPruneR = 5;   // register rows of the block-bounded minimum pass: blocks of 2^kPruneR steps
+constexpr int kPruneR = 6;   // register rows of the block-bounded minimum pass: blocks of 2^kPruneR steps
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 

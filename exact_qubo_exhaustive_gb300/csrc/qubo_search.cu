@@ -135,15 +135,11 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
 //   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
 //   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
 //   T2[i]    = (T[i] mod 2^16) in both 16-bit halves (packed pass; optional)
-//   blk[m]   = block m of 2^kPruneR = 32 steps (block-bounded minimum pass; optional, needs
-//              w > kPruneR and C >= 5: then every warp of the loop lies inside the T range and its
-//              32 lanes hold one block): the least T of the block and the flip that follows it,
-//              position kPruneR + ctz(m + 1), set unless bit ctz(m + 1) + 1 of m + 1 is set
-//              (reflected Gray code); blk[2^(w-5) - 1] and the padding entry after it: no flip
+
 // ------------------------------------------------------------------------------------------------
 __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __restrict__ hdr,
                               const int32_t* __restrict__ U, int32_t* M, int32_t* Ec, int32_t* T, uint32_t* T2,
-                              BlockCtl* blk, uint64_t nTpad) {
+                              uint64_t nTpad) {
   if (hdr->status != QUBO_OK) return;
   const int ncols = 1 << C;
   const uint64_t nM = (uint64_t)(n - C) << C;
@@ -186,29 +182,43 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
       }
       T[i] = acc;
       if (T2) T2[i] = ((uint32_t)acc & 0xffffu) * 0x10001u;
-      if (blk) {
-        static_assert(kPruneR == 5, "one warp holds one block of walked energies");
-        const int tmin = __reduce_min_sync(0xffffffffu, acc);
-        if ((i & 31u) == 0) {
-          const uint32_t m = (uint32_t)(i >> 5), nb = 1u << (w - kPruneR);
-          BlockCtl b;
-          b.tmin = tmin;
-          if (m + 1 < nb) {
-            const int rr = __ffs((int)(m + 1)) - 1;
-            const bool up = !(((m + 1) >> (rr + 1)) & 1u);
-            b.row = rr << (C - 2);
-            b.dsgn = up ? 1.f : -1.f;
-            b.lvx = (up ? 0 : 64) + (n - C - 1 - (kPruneR + rr));
-          } else {
-            b.row = 0;
-            b.dsgn = 0.f;
-            b.lvx = 128;
-          }
-          blk[m] = b;
-          if (m + 1 == nb) blk[nb] = b;  // padding: the walk reads one entry ahead
-        }
-      }
     }
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// Block table of the block-bounded minimum pass (one thread per block of 2^kPruneR Gray steps):
+//   blk[m] = the least T of block m, and the flip that follows it: position kPruneR + ctz(m + 1),
+//            which becomes set unless bit ctz(m + 1) + 1 of m + 1 is set (reflected Gray code);
+//            its shared row's float4 offset, sign, and the index of +L or -L of its variable in
+//            the walker's linear-term table. blk[nb - 1] and the padding entry blk[nb]: no flip.
+// ------------------------------------------------------------------------------------------------
+__global__ void block_table_kernel(int n, int C, int w, const DevHeader* __restrict__ hdr,
+                                   const int32_t* __restrict__ T, BlockCtl* blk) {
+  if (hdr->status != QUBO_OK) return;
+  const uint32_t nb = 1u << (w - kPruneR);
+  for (uint32_t m = blockIdx.x * blockDim.x + threadIdx.x; m <= nb; m += gridDim.x * blockDim.x) {
+    const uint32_t mm = m < nb ? m : nb - 1;
+    const int4* T4 = reinterpret_cast<const int4*>(T + ((size_t)mm << kPruneR));
+    int tmin = kIntInf;
+    for (int q = 0; q < (1 << kPruneR) / 4; ++q) {
+      const int4 t = T4[q];
+      tmin = min(tmin, __vimin3_s32(t.x, t.y, min(t.z, t.w)));
+    }
+    BlockCtl b;
+    b.tmin = tmin;
+    if (m + 1 < nb) {
+      const int rr = __ffs((int)(m + 1)) - 1;
+      const bool up = !(((m + 1) >> (rr + 1)) & 1u);
+      b.row = rr << (C - 2);
+      b.dsgn = up ? 1.f : -1.f;
+      b.lvx = (up ? 0 : 64) + (n - C - 1 - (kPruneR + rr));
+    } else {
+      b.row = 0;
+      b.dsgn = 0.f;
+      b.lvx = 128;
+    }
+    blk[m] = b;
   }
 }
 
@@ -333,9 +343,15 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   const uint64_t nTpad = ((uint64_t)1 << p.w) < 4 ? 4 : ((uint64_t)1 << p.w);
   const uint64_t tab_work = ((uint64_t)(p.n - p.C) << p.C) + ((uint64_t)1 << p.C) + nTpad;
   const int tab_blocks = (int)((tab_work + 255) / 256 < 4096 ? (tab_work + 255) / 256 : 4096);
-  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, w.blk, nTpad);
+  tables_kernel<<<tab_blocks, 256, 0, stream>>>(p.n, p.C, p.F, p.w, w.hdr, w.U, w.M, w.Ec, w.T, w.T2, nTpad);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if (p.prune) {
+    const uint32_t nb = 1u << (p.w - kPruneR);
+    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, w.hdr, w.T, w.blk);
+    ++nl;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
 
   memset(&kp, 0, sizeof(kp));
   kp.n = p.n;

@@ -651,8 +651,9 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   static constexpr int kCPT = 16;
   static constexpr int kThreads = 256;      // 2^12 columns: the quad stride is a constant
   static constexpr int kBlock = 1 << R;     // steps per block
-  static constexpr int kRefreshMask = 31;   // blocks between two exchanges of the group's best
+  static constexpr int kRefreshMask = 15;   // blocks between two exchanges of the group's best
   static_assert(R >= 3, "whole quads of walked energies per block");
+  static_assert(kThreads * kCPT == 4096, "the control table's row offsets assume 2^12 columns");
 
   int dmin0, dmin1;  // D_par of even and odd blocks
   int g_best;        // G: the group's best energy known to this warp (absolute, image units)
@@ -710,11 +711,20 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
     for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = __fmaf_rn(row[jj], sg, this->V[jj]);
   }
 
+  // Register row a (2 <= a < R) added with sign sg.
+  template <int A = 2>
+  __device__ __forceinline__ void flip_row_rt(int a, float sg) {
+    if constexpr (A < R) {
+      if (a == A) flip_rt(this->Row[A], sg);
+      else flip_row_rt<A + 1>(a, sg);
+    }
+  }
+
   // The block walked with every per-step minimum (rare: the bound did not clear it). A loop over
   // groups of four steps keeps the code small: in group k the flips of steps 4k and 4k + 2 are
   // row 0 (+, -), of step 4k + 1 row 1 (- when k is odd), of step 4k + 3 row 2 + ctz(k + 1).
   __device__ __forceinline__ void exact_block(const WalkCtx& c, int m, int m0, float sgn) {
-    static_assert(R == 5, "groups of four steps: rows 0 and 1 inside, rows 2..4 between");
+    static_assert(R >= 3, "groups of four steps: rows 0 and 1 inside, rows 2..R-1 between");
     const int4* T4 = reinterpret_cast<const int4*>(c.T) + (static_cast<uint32_t>(m) << (R - 2));
     int4 tq = __ldg(T4);
     this->aux = __viaddmin_s32(m0, tq.x, this->aux);
@@ -732,9 +742,7 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
       const int a = 2 + __ffs(k + 1) - 1;
       const int d = 4 * k + 3;
       const float sg = (a == R - 1) ? sgn : ((((d >> a) ^ (d >> (a + 1))) & 1) ? -1.f : 1.f);
-      if (a == 2) flip_rt(this->Row[2], sg);
-      else if (a == 3) flip_rt(this->Row[3], sg);
-      else flip_rt(this->Row[4], sg);
+      flip_row_rt(a, sg);
       tq = __ldg(T4 + k + 1);
       this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.x, this->aux);
     }

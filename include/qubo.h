@@ -95,8 +95,8 @@ typedef struct qubo_plan_desc {
                           16-bit energies per 32-bit word (§IV-B.5's narrow path); 0: not available */
   int biased;          /* 1: int32 input whose sum |U_ij| <= 2^22 - 1 (and not narrower) runs the
                           minimum pass with fp32 column adds in the exact binade [2^23, 2^24) */
-  int pruned;          /* 1: the biased and int32 minimum passes skip the per-step minima of blocks of
-                          16 Gray steps whose lower bound is above the best energy found so far
+  int pruned;          /* 1: the biased minimum pass forms its per-step minima only in blocks of 64
+                          Gray steps whose lower bound does not clear the best energy found so far
                           (every state is still added; results are unchanged) */
 } qubo_plan_desc;
 
@@ -278,7 +278,9 @@ QUBO_API void qubo_clear_abort(void);
  *       10 int32 add as a fused add-min against an opaque INT_MAX (ALU; cannot be merged),
  *       11 int32 add as a multiply-add by an opaque one (FMA pipe; cannot be merged),
  *       12 / 14 / 15: 11 / 10 / 12 of the 16 chains fp32 adds, the rest kind-10 adds,
- *       13: 8 chains kind 11, 8 chains kind 10. */
+ *       13: 8 chains kind 11, 8 chains kind 10,
+ *       16 fp32 add / subtract of loop-invariant addends into 16 accumulators (the column-update
+ *          pattern of the enumeration walk). */
 QUBO_API int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz);
 
 #ifdef __cplusplus
