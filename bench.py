@@ -354,13 +354,13 @@ def run_gb300(args):
     # the measured INT32-add roofline: the best int32 add throughput of the add microbenchmark
     # (kind 0: the compiler's own split of the adds; kind 8: half of them forced onto the FMA
     # pipe's multiply-add) times the SM count, at the clock the probe saw
-    probes = [q.probe_alu(kind, 20000) for kind in (0, 8)]
+    probes = [q.probe_alu(kind, 4000) for kind in (0, 8)]
     best_ops, probe_mhz = max(probes, key=lambda t: t[0])
     r_int = best_ops / 1e12
     # the add the kernel issues is an fp32 add (exact integers in the binade [2^23, 2^24)): its
     # measured rate is the roofline of the pipe the kernel runs on (the better of two patterns:
     # kind 4, chains that read a neighbour's sum; kind 16, loop-invariant addends as in the walk)
-    fadd_ops, fadd_mhz = max((q.probe_alu(kind, 20000) for kind in (4, 16)), key=lambda t: t[0])
+    fadd_ops, fadd_mhz = max((q.probe_alu(kind, 4000) for kind in (4, 16)), key=lambda t: t[0])
     r_fadd = fadd_ops / 1e12
     traffic, traffic_src = profiled_traffic()
 

@@ -658,6 +658,18 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   int dmin0, dmin1;  // D_par of even and odd blocks
   int g_best;        // G: the group's best energy known to this warp (absolute, image units)
 
+  // Column pairs: one fp32x2 instruction adds (or adds with a sign) the rows of two columns.
+  __device__ __forceinline__ void pair_add(int jj, float r0, float r1) {
+    const float2 t = __fadd2_rn(make_float2(this->V[jj], this->V[jj + 1]), make_float2(r0, r1));
+    this->V[jj] = t.x;
+    this->V[jj + 1] = t.y;
+  }
+  __device__ __forceinline__ void pair_fma(int jj, float r0, float r1, float2 sg) {
+    const float2 t = __ffma2_rn(make_float2(r0, r1), sg, make_float2(this->V[jj], this->V[jj + 1]));
+    this->V[jj] = t.x;
+    this->V[jj + 1] = t.y;
+  }
+
   // Flips of steps 0..kBlock-2 of a block; position R-1 flips once, with sign sgn (+1 in even
   // blocks, -1 in odd ones); the others with the sign their Gray bit fixes.
   template <int D>
@@ -666,12 +678,14 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
       constexpr int a = ctz_c(D + 1);
       if constexpr (a == R - 1) {
 #pragma unroll
-        for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = __fmaf_rn(this->Row[a][jj], sgn, this->V[jj]);
+        for (int jj = 0; jj < kCPT; jj += 2) pair_fma(jj, this->Row[a][jj], this->Row[a][jj + 1], make_float2(sgn, sgn));
       } else {
         constexpr int bit = ((D >> a) ^ (D >> (a + 1))) & 1;  // bit a of gray(D): 1 -> the flip clears it
 #pragma unroll
-        for (int jj = 0; jj < kCPT; ++jj)
-          this->V[jj] = bit ? O::sub(this->V[jj], this->Row[a][jj]) : O::add(this->V[jj], this->Row[a][jj]);
+        for (int jj = 0; jj < kCPT; jj += 2) {
+          if (bit) pair_fma(jj, this->Row[a][jj], this->Row[a][jj + 1], make_float2(-1.f, -1.f));
+          else pair_add(jj, this->Row[a][jj], this->Row[a][jj + 1]);
+        }
       }
       body<D + 1>(sgn);
     }
@@ -708,7 +722,7 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   // Flip of a register row whose position and sign are known at run time.
   __device__ __forceinline__ void flip_rt(const float* row, float sg) {
 #pragma unroll
-    for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = __fmaf_rn(row[jj], sg, this->V[jj]);
+    for (int jj = 0; jj < kCPT; jj += 2) pair_fma(jj, row[jj], row[jj + 1], make_float2(sg, sg));
   }
 
   // Register row a (2 <= a < R) added with sign sg.
@@ -731,12 +745,12 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
 #pragma unroll 1
     for (int k = 0; k < kBlock / 4; ++k) {
 #pragma unroll
-      for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = O::add(this->V[jj], this->Row[0][jj]);
+      for (int jj = 0; jj < kCPT; jj += 2) pair_add(jj, this->Row[0][jj], this->Row[0][jj + 1]);
       this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.y, this->aux);
       flip_rt(this->Row[1], (k & 1) ? -1.f : 1.f);
       this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.z, this->aux);
 #pragma unroll
-      for (int jj = 0; jj < kCPT; ++jj) this->V[jj] = O::sub(this->V[jj], this->Row[0][jj]);
+      for (int jj = 0; jj < kCPT; jj += 2) pair_fma(jj, this->Row[0][jj], this->Row[0][jj + 1], make_float2(-1.f, -1.f));
       this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.w, this->aux);
       if (k + 1 == kBlock / 4) break;  // the block's last state
       const int a = 2 + __ffs(k + 1) - 1;
@@ -786,12 +800,11 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
       block(c, m, ctl.x + (odd ? dmb1 : dmb0), thr, odd ? -1.f : 1.f);
       // the flip that follows (a no-op after the last block: sign 0, linear term 0)
       const float dsgn = __int_as_float(ctl.z);
+      const float2 dsgn2 = make_float2(dsgn, dsgn);
 #pragma unroll
       for (int k = 0; k < kCPT / 4; ++k) {
-        this->V[4 * k + 0] = __fmaf_rn(rb.q[k].x, dsgn, this->V[4 * k + 0]);
-        this->V[4 * k + 1] = __fmaf_rn(rb.q[k].y, dsgn, this->V[4 * k + 1]);
-        this->V[4 * k + 2] = __fmaf_rn(rb.q[k].z, dsgn, this->V[4 * k + 2]);
-        this->V[4 * k + 3] = __fmaf_rn(rb.q[k].w, dsgn, this->V[4 * k + 3]);
+        pair_fma(4 * k + 0, rb.q[k].x, rb.q[k].y, dsgn2);
+        pair_fma(4 * k + 2, rb.q[k].z, rb.q[k].w, dsgn2);
       }
       const int dl = c.sL[ctl.w];
       this->s += dl;
