@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
     f[k] = (float)a[k] * 0.5f;
     rinv[k] = (float)((k * 37 + seed) & 63);
     f2[k] = 0;
-    if constexpr (KIND == 9) {  // only kind 9 carries the packed pairs (the other kinds' code stays as it was)
+    if constexpr (KIND == 9 || KIND >= 17) {  // only these kinds carry packed pairs
       const float lo = f[k], hi = f[k] + 1.0f;
       asm("mov.b64 %0, {%1, %2};" : "=l"(f2[k]) : "f"(lo), "f"(hi));
     }
@@ -56,7 +56,16 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
       if (KIND == 6) a[k] = (int)__vimin3_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 7) a[k] = (int)__viaddmin_u16x2((unsigned)a[k], (unsigned)x, (unsigned)y);
       if (KIND == 9) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(f2[k]) : "l"(f2[(k + 1) % kChains]));
-      if constexpr (KIND == 16) {
+      if constexpr (KIND == 17 || KIND == 18) {
+        // fp32x2 adds on the first kPairChains chains (two adds per instruction, FMA pipes) and
+        // fused add-mins against an opaque INT_MAX on the rest (ALU): the mix a walk could use
+        constexpr int kPairChains = KIND == 17 ? 12 : 10;
+        if (k < kPairChains) {
+          if ((k & 1) == 0) asm("add.rn.f32x2 %0, %0, %1;" : "+l"(f2[k >> 1]) : "l"(f2[8 + (k >> 1)]));
+        } else {
+          a[k] = __viaddmin_s32(a[k], x, big);
+        }
+      } else if constexpr (KIND == 16) {
         // fp32 adds of loop-invariant addends into 16 accumulators, alternating add and subtract:
         // the pattern of the walk's column updates (V[j] +-= Row[a][j])
         f[k] = (k & 1) ? __fsub_rn(f[k], rinv[k]) : __fadd_rn(f[k], rinv[k]);
@@ -87,7 +96,7 @@ __global__ void __launch_bounds__(256) alu_probe_kernel(int iters, int seed, int
 #pragma unroll
   for (int k = 0; k < kChains; ++k) {
     s += a[k] + (int)f[k];
-    if constexpr (KIND == 9) {
+    if constexpr (KIND == 9 || KIND >= 17) {
       float lo, hi;
       asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(f2[k]));
       s += (int)lo + (int)hi;
@@ -137,7 +146,9 @@ cudaError_t run_alu_probe(int kind, int iters, double* ops_per_s, double* sm_mhz
       case 13: return launch<13>(blocks, it, out, clk);
       case 14: return launch<14>(blocks, it, out, clk);
       case 15: return launch<15>(blocks, it, out, clk);
-      default: return launch<16>(blocks, it, out, clk);
+      case 16: return launch<16>(blocks, it, out, clk);
+      case 17: return launch<17>(blocks, it, out, clk);
+      default: return launch<18>(blocks, it, out, clk);
     }
   };
   cudaEvent_t e0 = nullptr, e1 = nullptr;

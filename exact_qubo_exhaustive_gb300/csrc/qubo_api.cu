@@ -277,8 +277,9 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   const bool narrow_passes = n >= kNarrowPassesMinN;
   p.biased = biased_pass_applies(p);
   // The biased pass with block bounds: 2^12 columns (256 threads of 16) and at least two blocks
-  // of 2^kPruneR steps per unit.
-  p.prune = p.biased && p.C == 12 && p.threads == 256 && p.w >= kPruneR + 1;
+  // of 2^prune_r steps per unit.
+  p.prune_r = p.w >= kPruneLongW ? kPruneRLong : kPruneRShort;
+  p.prune = p.biased && p.C == 12 && p.threads == 256 && p.w >= p.prune_r + 1;
   // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
   // shared rows are 2 bytes per column.
   if (narrow_passes && p.variant == kFast && dtype == QUBO_INT32 && p.C >= 10 && p.w >= kPackedR + 1) {
@@ -709,7 +710,7 @@ void qubo_request_abort(void) { g_abort = 1; }
 void qubo_clear_abort(void) { g_abort = 0; }
 
 int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz) {
-  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 16) return QUBO_ERR_ARG;
+  if (!out_ops_per_s || !out_sm_mhz || iters < 1 || kind < 0 || kind > 18) return QUBO_ERR_ARG;
   std::lock_guard<std::mutex> lk(g_mu);
   int dev, st;
   if ((st = current_device(&dev))) return st;

@@ -29,7 +29,12 @@ constexpr int kFastR = 4;
 constexpr int kBiasedR = 5;  // register rows of the biased-binade minimum pass
 constexpr int kPackedR = 5;  // register rows of the packed 16x2 minimum pass
 constexpr int kIntMinR = 5;  // register rows of the int32 minimum pass (the resolve passes keep kFastR)
-constexpr int kPruneR = 6;   // register rows of the block-bounded minimum pass: blocks of 2^kPruneR steps
+// Register rows of the block-bounded minimum pass, which walks blocks of 2^R Gray steps: R = 7
+// for units of at least kPruneLongW walked bits, R = 6 below (the longer block body pays off
+// only when a unit has many blocks).
+constexpr int kPruneRShort = 6;
+constexpr int kPruneRLong = 7;
+constexpr int kPruneLongW = 14;
 constexpr int kGenericMaxC = 10;  // 2^C threads per block
 constexpr int kMaxWalkedBits = 24;
 
@@ -40,7 +45,7 @@ constexpr int64_t kBiasedWalkMaxAbsSum = (int64_t(1) << 22) - 1;
 // stay inside (-2^15, 2^15) when sum |U| < 2^14.
 constexpr int64_t kPackedMaxAbsSum = (int64_t(1) << 14) - 1;
 
-// Per block of 2^kPruneR Gray steps (block-bounded minimum pass): the block's least walked
+// Per block of 2^R Gray steps (block-bounded minimum pass): the block's least walked
 // energy and the shared-row flip that follows it, precomputed once per launch (the same for every
 // unit): the row's float4 offset in shared memory, its sign (+1 sets the variable, -1 clears it,
 // 0 after the last block: no flip) and the index of its signed linear term in the walker's
@@ -89,6 +94,7 @@ struct Plan {
   bool host_gbase = false; // group bases uploaded by the host (else one group, written on device)
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
   bool prune = false;      // the biased minimum pass skips the per-step minima of blocks bounded above the threshold
+  int prune_r = 0;         // its register rows: blocks of 2^prune_r steps
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
   int packed_threads = 0;  // 2^C / 32
@@ -105,7 +111,7 @@ struct Work {
   int32_t* Ec = nullptr;    // 2^C: energy of the cached variables alone
   int32_t* T = nullptr;     // 2^w (padded): walked-variable energy, in Gray order
   uint32_t* T2 = nullptr;   // packed pass: T's low 16 bits in both halves
-  BlockCtl* blk = nullptr;  // block-bounded minimum pass: one entry per block of 2^kPruneR steps (+ 1)
+  BlockCtl* blk = nullptr;  // block-bounded minimum pass: one entry per block of 2^prune_r steps (+ 1)
   int32_t* gthr = nullptr;  // pruned minimum passes: best energy published so far, per group
   int32_t* unit_min = nullptr;
   uint32_t* tied = nullptr;

@@ -187,21 +187,21 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
 }
 
 // ------------------------------------------------------------------------------------------------
-// Block table of the block-bounded minimum pass (one thread per block of 2^kPruneR Gray steps):
-//   blk[m] = the least T of block m, and the flip that follows it: position kPruneR + ctz(m + 1),
+// Block table of the block-bounded minimum pass (one thread per block of 2^R Gray steps):
+//   blk[m] = the least T of block m, and the flip that follows it: position R + ctz(m + 1),
 //            which becomes set unless bit ctz(m + 1) + 1 of m + 1 is set (reflected Gray code);
 //            its shared row's float4 offset, sign, and the index of +L or -L of its variable in
 //            the walker's linear-term table. blk[nb - 1] and the padding entry blk[nb]: no flip.
 // ------------------------------------------------------------------------------------------------
-__global__ void block_table_kernel(int n, int C, int w, const DevHeader* __restrict__ hdr,
+__global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* __restrict__ hdr,
                                    const int32_t* __restrict__ T, BlockCtl* blk) {
   if (hdr->status != QUBO_OK) return;
-  const uint32_t nb = 1u << (w - kPruneR);
+  const uint32_t nb = 1u << (w - R);
   for (uint32_t m = blockIdx.x * blockDim.x + threadIdx.x; m <= nb; m += gridDim.x * blockDim.x) {
     const uint32_t mm = m < nb ? m : nb - 1;
-    const int4* T4 = reinterpret_cast<const int4*>(T + ((size_t)mm << kPruneR));
+    const int4* T4 = reinterpret_cast<const int4*>(T + ((size_t)mm << R));
     int tmin = kIntInf;
-    for (int q = 0; q < (1 << kPruneR) / 4; ++q) {
+    for (int q = 0; q < (1 << R) / 4; ++q) {
       const int4 t = T4[q];
       tmin = min(tmin, __vimin3_s32(t.x, t.y, min(t.z, t.w)));
     }
@@ -212,7 +212,7 @@ __global__ void block_table_kernel(int n, int C, int w, const DevHeader* __restr
       const bool up = !(((m + 1) >> (rr + 1)) & 1u);
       b.row = rr << (C - 2);
       b.dsgn = up ? 1.f : -1.f;
-      b.lvx = (up ? 0 : 64) + (n - C - 1 - (kPruneR + rr));
+      b.lvx = (up ? 0 : 64) + (n - C - 1 - (R + rr));
     } else {
       b.row = 0;
       b.dsgn = 0.f;
@@ -304,7 +304,7 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));
   if (p.packed) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
   if (p.prune) {
-    w.blk = reinterpret_cast<BlockCtl*>(take(((nT >> kPruneR) + 1) * sizeof(BlockCtl)));
+    w.blk = reinterpret_cast<BlockCtl*>(take(((nT >> p.prune_r) + 1) * sizeof(BlockCtl)));
     w.gthr = reinterpret_cast<int32_t*>(take((size_t)p.ngroups * 4));
   }
   w.unit_min = reinterpret_cast<int32_t*>(take(p.total_units * 4));
@@ -347,8 +347,8 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.prune) {
-    const uint32_t nb = 1u << (p.w - kPruneR);
-    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, w.hdr, w.T, w.blk);
+    const uint32_t nb = 1u << (p.w - p.prune_r);
+    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk);
     ++nl;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -409,7 +409,7 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     if (p.biased) {
       // biased-binade CUDA-core pass, with block bounds where planned (exits at once unless it
       // owns the minimum pass) ...
-      e = p.prune ? launch_search_biased_pruned(kp, blocks, p.threads, p.smem_bytes, stream)
+      e = p.prune ? launch_search_biased_pruned(p.prune_r, kp, blocks, p.threads, p.smem_bytes, stream)
                   : launch_search_biased(kp, blocks, p.threads, p.smem_bytes, stream);
       if (e != cudaSuccess) return e;
       ++nl;

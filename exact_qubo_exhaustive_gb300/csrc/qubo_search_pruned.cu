@@ -1,17 +1,25 @@
 // Biased-binade minimum pass with block bounds: 16 columns per thread, 256 threads (2^12 cached
-// columns), the kPruneR lowest walked rows in registers; blocks of 2^kPruneR steps whose lower
-// bound is above the group's best skip their per-step minima (PrunedMinWalker).
+// columns), the R lowest walked rows in registers (R = kPruneRShort or kPruneRLong, as planned);
+// blocks of 2^R steps whose lower bound is above the group's best skip their per-step minima
+// (PrunedMinWalker).
 #include "qubo_search_kernel.cuh"
 
 namespace qgb {
 
-cudaError_t launch_search_biased_pruned(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
-  if (threads != PrunedMinWalker<kPruneR>::kThreads) return cudaErrorInvalidConfiguration;
-  auto k = search_kernel<kFastCPT, kPruneR, kModeMin, true, true>;
+template <int R>
+static cudaError_t launch_one(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
+  if (threads != PrunedMinWalker<R>::kThreads) return cudaErrorInvalidConfiguration;
+  auto k = search_kernel<kFastCPT, R, kModeMin, true, true>;
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   k<<<blocks, threads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+cudaError_t launch_search_biased_pruned(int R, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
+  if (R == kPruneRLong) return launch_one<kPruneRLong>(p, blocks, threads, smem, s);
+  if (R == kPruneRShort) return launch_one<kPruneRShort>(p, blocks, threads, smem, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace qgb

@@ -280,7 +280,9 @@ QUBO_API void qubo_clear_abort(void);
  *       12 / 14 / 15: 11 / 10 / 12 of the 16 chains fp32 adds, the rest kind-10 adds,
  *       13: 8 chains kind 11, 8 chains kind 10,
  *       16 fp32 add / subtract of loop-invariant addends into 16 accumulators (the column-update
- *          pattern of the enumeration walk). */
+ *          pattern of the enumeration walk),
+ *       17 / 18: 12 / 10 of the 16 chains as fp32x2 adds (two adds per instruction), the rest
+ *          kind-10 adds (counted per add). */
 QUBO_API int qubo_probe_alu(int kind, int iters, double* out_ops_per_s, double* out_sm_mhz);
 
 #ifdef __cplusplus
