@@ -97,6 +97,7 @@ struct Plan {
   int prune_r = 0;         // its register rows: blocks of 2^prune_r steps
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
+  bool packed_ok = false;  //   the packed pass fits this plan (it runs when the bounded pass does not)
   int packed_threads = 0;  // 2^C / 32
   int packed_blocks = 0;
   size_t packed_smem = 0;

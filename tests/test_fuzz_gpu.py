@@ -89,3 +89,35 @@ def test_random_lowest_spectra(q, seed):
         e, x = q.solve_lowest(Q, k)
         we, wx = O.lowest(Q, k)
         assert np.array_equal(e, we) and np.array_equal(x, wx), (n, k)
+
+
+@pytest.mark.parametrize("seed", [5, 6])
+def test_random_problems_of_the_bounded_pass(q, seed):
+    # n >= 30 with 2^12 columns: the block-bounded biased pass (every range that fits the fp32
+    # binade, and fp32 input) or the int32 pass (wide); decoupled variables put minimisers in
+    # many units and blocks at once; slices give each group its own threshold
+    rng = np.random.default_rng(seed)
+    for _ in range(3):
+        n = int(rng.integers(30, 32))
+        kind = str(rng.choice(["narrow", "mid", "wide", "pos", "fp32"]))
+        Q = _instance(rng, n, kind, int(rng.integers(0, 1 << 30)))
+        e, x, t = q.solve(Q)
+        want = O.solve(Q)
+        if kind == "fp32":
+            assert abs(e - want[0]) <= 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+            assert (x == want[1]).all() and t == want[2], (n, kind)
+        else:
+            assert (e, t) == (want[0], want[2]) and (x == want[1]).all(), (n, kind)
+    for _ in range(2):
+        n, k = int(rng.integers(34, 38)), int(rng.integers(6, 9))
+        kind = str(rng.choice(["narrow", "mid", "pos", "fp32"]))
+        Q = _instance(rng, n, kind, int(rng.integers(0, 1 << 30)))
+        ids = np.unique(rng.integers(0, 1 << k, 3)).astype(np.uint64)
+        e, x, t = q.solve_slices(Q, k, ids)
+        for i, sid in enumerate(ids):
+            want = O.solve_slice(Q, k, int(sid))
+            if kind == "fp32":
+                assert abs(float(e[i]) - want[0]) <= 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+                assert (x[i] == want[1]).all() and int(t[i]) == want[2], (n, k, int(sid))
+            else:
+                assert (int(e[i]), int(t[i])) == (want[0], want[2]) and (x[i] == want[1]).all(), (n, k, int(sid))

@@ -81,7 +81,8 @@ def test_infeasible_explicit_plan_is_an_error(q):
 def test_plans_pick_fast_kernel_for_large_n(q):
     p = q.plan(40)
     assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
-    assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 1
+    # the bounded biased pass; the packed pass runs only without bounds (the k-lowest driver)
+    assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 0
     assert q.plan(8)["variant"] == 0
     # fp32 input: its fixed-point image is scaled into the biased pass's range; never packed
     assert q.plan(36, q.FP32)["biased"] == 1 and q.plan(36, q.FP32)["packed"] == 0
@@ -150,18 +151,23 @@ def test_fewer_threads_than_variables(q):
 
 
 # ---------------------------------------------------------------- packed 16x2 minimum pass
+# Narrow inputs (sum |U| < 2^14) take the bounded biased pass in solve() and the packed pass in
+# the k-lowest driver, whose minimum pass runs without bounds: both are checked.
 
 @pytest.mark.parametrize("n,lo,hi,seed", [(30, -30, 30, 1), (30, -9, 9, 3), (31, -3, 3, 4), (31, 0, 2, 5)])
 def test_packed_pass_small_range(q, n, lo, hi, seed):
     Q = qi.random_upper_int(n, lo, hi, 2400 + seed)
     assert int(np.abs(Q.astype(np.int64)).sum()) <= (1 << 14) - 1
-    assert q.plan(n)["packed"] == 1
-    check_int(q, Q)
+    assert q.plan(n)["packed"] == 0 and q.plan(n)["pruned"] == 1
+    e, x, t = check_int(q, Q)
+    le, lx = q.solve_lowest(Q, 1)  # the packed pass
+    assert int(le[0]) == e and (lx[0] == x).all()
 
 
 @pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
 def test_packed_range_limit_is_exact(q, sign):
-    # sum |U| = 2^14 - 1 runs the packed pass (values pushed to +-sum |U|), 2^14 the biased one
+    # without bounds (solve_lowest) sum |U| = 2^14 - 1 runs the packed pass (values pushed to
+    # +-sum |U|), 2^14 the biased one; solve() runs the bounded biased pass on both
     n = 30
     lo, hi = {"mixed": (-50, 50), "negative": (-50, -1), "positive": (1, 50)}[sign]
     for total in ((1 << 14) - 1, 1 << 14):
@@ -181,10 +187,13 @@ def test_packed_range_limit_is_exact(q, sign):
 
 
 def test_packed_pass_all_ties(q):
-    # Q = 0: every state ties; the packed minimum is 0 and the resolve pass counts 2^n
-    assert q.plan(30)["packed"] == 1
-    e, x, t = q.solve(np.zeros((30, 30), np.int32))
+    # Q = 0: every state ties; every block's bound equals the threshold, so the bounded pass walks
+    # every block exactly, and the resolve pass counts 2^n; the packed pass (k lowest) sees 0 too
+    Z = np.zeros((30, 30), np.int32)
+    e, x, t = q.solve(Z)
     assert (e, t) == (0, 1 << 30) and not x.any()
+    le, lx = q.solve_lowest(Z, 3)
+    assert list(le) == [0, 0, 0] and [oracle.rank_of_bits(v) for v in lx] == [0, 1, 2]
 
 
 def test_small_problems_run_the_int32_pass_alone(q):
@@ -196,7 +205,7 @@ def test_small_problems_run_the_int32_pass_alone(q):
 
 def test_n40_narrow_slices_against_oracle(q):
     Q = qi.workload_n40_narrow()
-    assert q.plan(40)["packed"] == 1
+    assert q.plan(40)["pruned"] == 1
     k = 16
     ids = qi.Stream(4041).integers(0, (1 << k) - 1, 4).astype(np.uint64)
     e, x, t = q.solve_slices(Q, k, ids)

@@ -61,17 +61,19 @@ def test_two_calls_in_a_row_match_the_workspace_entry_point(env):
 
 
 def test_interleaved_problems_of_every_minimum_pass(env):
-    # every minimum pass works in the shared array: packed 16x2 (narrow int32, n >= 30), the
-    # block-bounded int32 pass on wide int32 input and on fp32 input's fixed-point image (n >= 30),
-    # plus a small problem; two rounds, so every call follows another problem's leftovers
+    # every minimum pass works in the shared array: the block-bounded biased pass (narrow and
+    # wide-but-below-2^22 int32 input, fp32 input's fixed-point image; its block table and group
+    # words live in the array too), the int32 pass on int32 input beyond 2^22 (n >= 30) and on a
+    # small problem; two rounds, so every call follows another problem's leftovers
     q, torch = env
     cases = [(32, qi.random_upper_int(32, -3, 3, 81), q.INT32),
              (31, qi.random_symmetric_normal_f32(31, 82), q.FP32),
              (33, qi.random_upper_int(33, -1000, 1000, 83), q.INT32),
              (20, qi.random_upper_int(20, -1, 1, 84), q.INT32),
-             (30, qi.random_upper_int(30, -2, 2, 85), q.INT32)]
+             (30, qi.random_upper_int(30, -(1 << 17), 1 << 17, 85), q.INT32)]
     plans = [q.plan(n, dt) for n, _, dt in cases]
-    assert plans[0]["packed"] == 1 and plans[2]["pruned"] == 1 and plans[4]["packed"] == 1
+    assert plans[0]["pruned"] == 1 and plans[1]["pruned"] == 1 and plans[2]["pruned"] == 1
+    assert int(np.abs(cases[4][1].astype(np.int64)).sum()) > (1 << 22)  # the int32 pass owns it
     wants = [with_workspace(q, torch, n, Q, dt) for n, Q, dt in cases]
     for _ in range(2):
         for (n, Q, dt), want in zip(cases, wants):
