@@ -192,9 +192,11 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
 //            which becomes set unless bit ctz(m + 1) + 1 of m + 1 is set (reflected Gray code);
 //            its shared row's float4 offset, sign, and the index of +L or -L of its variable in
 //            the walker's linear-term table. blk[nb - 1] and the padding entry blk[nb]: no flip.
+// seed (optional): the best energy of a group that holds the unit with prefix 0; every T[i] is
+// the energy of a state of that unit (prefix 0, cached variables 0), so min T may start it.
 // ------------------------------------------------------------------------------------------------
 __global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* __restrict__ hdr,
-                                   const int32_t* __restrict__ T, BlockCtl* blk) {
+                                   const int32_t* __restrict__ T, BlockCtl* blk, int32_t* seed) {
   if (hdr->status != QUBO_OK) return;
   const uint32_t nb = 1u << (w - R);
   for (uint32_t m = blockIdx.x * blockDim.x + threadIdx.x; m <= nb; m += gridDim.x * blockDim.x) {
@@ -205,6 +207,7 @@ __global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* 
       const int4 t = T4[q];
       tmin = min(tmin, __vimin3_s32(t.x, t.y, min(t.z, t.w)));
     }
+    if (seed && m < nb) atomicMin(seed, tmin);
     BlockCtl b;
     b.tmin = tmin;
     if (m + 1 < nb) {
@@ -348,7 +351,9 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.prune) {
     const uint32_t nb = 1u << (p.w - p.prune_r);
-    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk);
+    // a whole problem (one group from unit 0) seeds its best with the least walked energy
+    int32_t* seed = (!p.host_gbase && p.gbase0 == 0 && p.ngroups == 1) ? w.gthr : nullptr;
+    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk, seed);
     ++nl;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -651,7 +651,8 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   static constexpr int kCPT = 16;
   static constexpr int kThreads = 256;      // 2^12 columns: the quad stride is a constant
   static constexpr int kBlock = 1 << R;     // steps per block
-  static constexpr int kRefreshMask = 15;   // blocks between two exchanges of the group's best
+  static constexpr int kRefreshMask = 3;    // blocks between two publications of the warp's best
+  static constexpr int kReadMask = 7;       // blocks between two reads of the group's best
   static_assert(R >= 3, "whole quads of walked energies per block");
   static_assert(kThreads * kCPT == 4096, "the control table's row offsets assume 2^12 columns");
 
@@ -762,15 +763,17 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
     }
   }
 
-  // The group's best: publish this warp's, take the grid's.
-  __device__ __forceinline__ void exchange_best(int* gbest) {
-    int v = __reduce_min_sync(0xffffffffu, this->aux - O::kBiasBits + this->s);
-    if ((threadIdx.x & 31) == 0) {
-      const int old = atomicMin(gbest, v);
-      v = old < v ? old : v;
+  // The group's best. Every kRefreshMask + 1 blocks the warp publishes its best if it improved on
+  // what it last published (a reduction whose result nobody waits for: after the first blocks
+  // almost no warp improves, so the shared word sees few updates); every kReadMask + 1 blocks it
+  // also takes the grid's value with a plain load, first used a block later.
+  __device__ __forceinline__ void exchange_best(int* gbest, bool read) {
+    const int v = __reduce_min_sync(0xffffffffu, this->aux - O::kBiasBits + this->s);
+    if (v < g_best) {
+      if ((threadIdx.x & 31) == 0) atomicMin(gbest, v);
+      g_best = v;
     }
-    v = __shfl_sync(0xffffffffu, v, 0);
-    g_best = v < g_best ? v : g_best;
+    if (read) g_best = min(g_best, __ldcg(gbest));
   }
 
   // Whole unit: nblocks (even, < 2^31) blocks of 2^R steps, each but the last followed by a
@@ -810,7 +813,7 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
       this->s += dl;
       this->aux -= dl;
       ctl = next;
-      if ((m & kRefreshMask) == kRefreshMask) exchange_best(gbest);
+      if ((m & kRefreshMask) == kRefreshMask) exchange_best(gbest, (m & kReadMask) == kReadMask);
     }
   }
 };
