@@ -27,7 +27,7 @@ __all__ = [
     "solve_lowest", "LOWEST_MAX_K", "solve_ising", "ising_to_qubo",
     "solve_checkpointed", "checkpoint_read", "fnv1a64", "INCOMPLETE",
     # planner, measurement, status, cancellation
-    "plan", "probe_alu", "enable_kernel_timing", "kernel_time_ms", "last_launch_count",
+    "plan", "probe_alu", "enable_kernel_timing", "enable_block_bounds", "kernel_time_ms", "last_launch_count",
     "status_string", "last_error", "request_abort", "clear_abort", "rank_to_bits",
 ]
 
@@ -89,6 +89,7 @@ _sig = {
                                                   ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]),
     "qubo_enable_kernel_timing": (None, [ctypes.c_int]),
     "qubo_kernel_time_ms": (ctypes.c_double, []),
+    "qubo_enable_block_bounds": (None, [ctypes.c_int]),
     "qubo_solve_batched_device": (ctypes.c_int, [ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_int,
                                                  ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p,
                                                  ctypes.c_void_p]),
@@ -353,6 +354,13 @@ def solve_slice_range_device(n: int, d_Q, dtype: int, k_prefix: int, first_slice
 
 def enable_kernel_timing(enable: bool = True) -> None:
     _lib.qubo_enable_kernel_timing(1 if enable else 0)
+
+
+def enable_block_bounds(enable: bool = True) -> None:
+    """Block bounds in the single-problem minimum pass (on by default). Off, calls planned from
+    then on form every step's minimum (the packed pass for narrow int32 input, the biased pass
+    without bounds otherwise); results are identical either way."""
+    _lib.qubo_enable_block_bounds(1 if enable else 0)
 
 
 def kernel_time_ms() -> float:

@@ -5,6 +5,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <cmath>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -25,6 +26,7 @@ bool g_timing_enabled = false;
 int g_timing_device = -1;
 KernelTiming g_timing;
 bool g_timing_recorded = false;
+std::atomic<int> g_block_bounds{1};  // qubo_enable_block_bounds
 
 // Events around the min-pass launches of the next calls, when kernel timing is enabled.
 const KernelTiming* timing_for_call(int dev) {
@@ -279,7 +281,7 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   // The biased pass with block bounds: 2^12 columns (256 threads of 16) and at least two blocks
   // of 2^prune_r steps per unit.
   p.prune_r = p.w >= kPruneLongW ? kPruneRLong : kPruneRShort;
-  p.prune = p.biased && p.C == 12 && p.threads == 256 && p.w >= p.prune_r + 1;
+  p.prune = g_block_bounds.load() && p.biased && p.C == 12 && p.threads == 256 && p.w >= p.prune_r + 1;
   // Packed 16x2 minimum pass: 32 columns per thread, so at least one warp needs C >= 10; its
   // shared rows are 2 bytes per column. It runs where the bounded biased pass does not: narrow
   // inputs (sum |U| < 2^14) fit the binade too, and there the bounded pass is the faster one
@@ -653,6 +655,8 @@ void qubo_enable_kernel_timing(int enable) {
   g_timing_enabled = enable != 0;
   g_timing_recorded = false;
 }
+
+void qubo_enable_block_bounds(int enable) { g_block_bounds.store(enable != 0 ? 1 : 0); }
 
 double qubo_kernel_time_ms(void) {
   std::lock_guard<std::mutex> lk(g_mu);

@@ -95,6 +95,7 @@ struct Plan {
   uint64_t gbase0 = 0;     // first unit prefix of the single group when !host_gbase
   bool prune = false;      // the biased minimum pass skips the per-step minima of blocks bounded above the threshold
   int prune_r = 0;         // its register rows: blocks of 2^prune_r steps
+  int bound_margin = 0;    // extra margin of its bound test: unit minima up to E* + margin stay exact
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
   bool packed_ok = false;  //   the packed pass fits this plan (it runs when the bounded pass does not)

@@ -6,10 +6,15 @@
 // ascending, equal energies by rank, so the answer is unique whatever the decomposition.
 //
 // Driver (host), over the enumeration kernel's passes:
-//  1. the usual fold, tables and minimum pass give every work unit's minimum;
+//  1. the usual fold, tables and minimum pass give every work unit's minimum (with block bounds
+//     whose test keeps a margin: every unit whose minimum lies within E* + margin reports it
+//     exactly, every other unit a value above E* + margin);
 //  2. theta = the k-th smallest unit minimum (each of those units holds a state <= theta, so at
-//     least k states have E <= theta); with fewer than k units, theta grows from the largest
-//     unit minimum until the count reaches k;
+//     least k states have E <= theta) when it lies within the margin; otherwise theta =
+//     E* + margin, whose collect pass counts the states at or below it exactly, and the margin
+//     is widened fourfold (and the minimum pass rerun) while fewer than k states lie within it;
+//     with fewer than k units (no bounds then), theta grows from the largest unit minimum until
+//     the count reaches k;
 //  3. one collect pass re-walks only the units whose minimum is <= theta and appends every state
 //     with E <= theta; if they fit the candidate buffer, selecting the k smallest keys on the
 //     host finishes;
@@ -76,8 +81,19 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
       }
     }
   }
-  // theta and the collect pass need every unit's exact minimum: no block bounds here
-  plan_without_bounds(&p);
+  // theta and the collect pass need the exact minimum of every unit at or below theta: the block
+  // bounds keep a margin (below); without enough units for theta to be one of them, no bounds
+  const bool bounded = p.prune && p.total_units >= want;
+  if (!bounded) plan_without_bounds(&p);
+  int64_t abs_sum = 0;  // sum |U_ij| of the folded triangle: every energy lies in [-S, S]
+  {
+    const int32_t* Qi = static_cast<const int32_t*>(Q);
+    for (int i = 0; i < n; ++i)
+      for (int j = i; j < n; ++j) {
+        const int64_t u = (j == i) ? (int64_t)Qi[i * n + i] : (int64_t)Qi[i * n + j] + Qi[j * n + i];
+        abs_sum += u < 0 ? -u : u;
+      }
+  }
   const uint64_t cap = std::max<uint64_t>(2 * want, (uint64_t)1 << 18);
 
   // one allocation: workspace | Q | candidates | counter
@@ -97,18 +113,26 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
   if ((e = cudaMemcpyAsync(dQ, Q, (size_t)n * n * 4, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return record_cuda_error(e, "cudaMemcpyAsync(Q)");
   KParams kp;
-  int nl = 0;
-  if ((e = run_min_stage(p, dQ, w, s, &nl, &kp)) != cudaSuccess) return record_cuda_error(e, "kernel launch");
-  launches += nl;
   DevHeader hdr;
   std::vector<int32_t> um(p.total_units);
-  if ((e = cudaMemcpyAsync(&hdr, w.hdr, sizeof(hdr), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(um.data(), w.unit_min, um.size() * 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
-      (e = cudaStreamSynchronize(s)) != cudaSuccess)
-    return record_cuda_error(e, "unit minima");
-  if (hdr.status != QUBO_OK) return hdr.status;
+  // The margin starts at S / 64; from 2S on no block is skipped at all.
+  int64_t margin = bounded ? std::max<int64_t>(64, abs_sum / 64) : 0;
+  auto min_stage = [&]() -> int {
+    if (abort_requested()) return QUBO_ERR_ABORTED;
+    p.bound_margin = (int)std::min<int64_t>(margin, 4 * abs_sum + 64);
+    int nl = 0;
+    cudaError_t ee;
+    if ((ee = run_min_stage(p, dQ, w, s, &nl, &kp)) != cudaSuccess) return record_cuda_error(ee, "kernel launch");
+    launches += nl;
+    if ((ee = cudaMemcpyAsync(&hdr, w.hdr, sizeof(hdr), cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (ee = cudaMemcpyAsync(um.data(), w.unit_min, um.size() * 4, cudaMemcpyDeviceToHost, s)) != cudaSuccess ||
+        (ee = cudaStreamSynchronize(s)) != cudaSuccess)
+      return record_cuda_error(ee, "unit minima");
+    return hdr.status;
+  };
+  if ((st = min_stage())) return st;
 
-  const int64_t E0 = *std::min_element(um.begin(), um.end());
+  int64_t E0 = *std::min_element(um.begin(), um.end());
   const int64_t Smax = hdr.abs_sum;  // every energy lies in [-S, S]
 
   // One pass: count (or collect) the states with key (E, rank) < (theta, rho) over the units
@@ -146,15 +170,26 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
 
   // 2. an upper threshold with at least `want` states at or below it
   int64_t theta;
+  uint64_t c = 0;
   if (p.total_units >= want) {  // the want-th smallest unit minimum (linear-time selection)
-    std::vector<int32_t> sel(um);
-    std::nth_element(sel.begin(), sel.begin() + (want - 1), sel.end());
-    theta = sel[want - 1];
+    for (;;) {
+      std::vector<int32_t> sel(um);
+      std::nth_element(sel.begin(), sel.begin() + (want - 1), sel.end());
+      theta = sel[want - 1];
+      if (!bounded || margin >= 2 * abs_sum || theta <= E0 + margin) break;
+      // beyond the margin: count the states within it exactly; enough of them make E0 + margin
+      // the threshold, otherwise widen the margin and walk again
+      theta = E0 + margin;
+      if ((st = pass(kModeCollectKey, theta, kAllRanks, &c))) return st;
+      if (c >= want) break;
+      margin *= 4;
+      if ((st = min_stage())) return st;
+      E0 = *std::min_element(um.begin(), um.end());
+    }
   } else {
     theta = *std::max_element(um.begin(), um.end());
   }
-  uint64_t c = 0;
-  if ((st = pass(kModeCollectKey, theta, kAllRanks, &c))) return st;
+  if (c < want && (st = pass(kModeCollectKey, theta, kAllRanks, &c))) return st;
   int64_t lo = E0 - 1;  // count(E <= lo) = 0 < want
   while (c < want) {
     lo = theta;

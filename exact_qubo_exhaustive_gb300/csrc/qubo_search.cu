@@ -377,6 +377,7 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   kp.T = w.T;
   kp.T2 = w.T2;
   kp.blk = w.blk;
+  kp.margin = p.bound_margin;
   kp.gthr = w.gthr;
   kp.gbase = w.gbase;
   kp.unit_min = w.unit_min;

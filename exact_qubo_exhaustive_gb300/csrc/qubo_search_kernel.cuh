@@ -26,6 +26,7 @@ struct KParams {
   const uint32_t* T2;       // packed pass: T's low 16 bits in both halves
   const BlockCtl* blk;      // block-bounded minimum pass: per-block minimum of T and following flip
   int32_t* gthr;            // pruned minimum passes: best energy published so far, per group
+  int margin;               // extra margin of the block bound test (image units)
   const uint64_t* gbase;
   int32_t* unit_min;
   uint32_t* tied;
@@ -183,7 +184,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
       if constexpr (PRUNE) {
         PrunedMinWalker<R> W;
         W.init(c, p.Ec, p.M, cP);
-        W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band);  // two blocks per iteration
+        W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band + p.margin);  // two blocks per iteration
         best = W.aux - VOps<float>::kBiasBits + W.s;
       } else if (niter == 0) {
         // no walked variable (generic variant only): the single walked assignment is 0

@@ -635,8 +635,10 @@ struct Walker {
 // below the threshold, and the block's per-step minima are not formed; otherwise the block is
 // walked with them, exactly as the plain minimum walk does.
 //
-// The threshold is min(this thread's best, G) + band. G is the best energy any block of the grid
-// has published for this group so far (or sum |U_ij|, which bounds every energy from above).
+// The threshold is min(this thread's best, G) + band (the fp32 resolution band, plus any margin a
+// driver asks for so that unit minima up to E* + margin stay exact). G is the best energy any
+// block of the grid has published for this group so far (or sum |U_ij|, which bounds every energy
+// from above).
 // Every value involved is an energy some state of the group attains, so the threshold is never
 // below the group's minimum E*: a state with E <= E* + band is never in a skipped block. Hence a
 // unit holding such a state reports its minimum exactly, every other unit reports the energy of

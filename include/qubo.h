@@ -92,12 +92,15 @@ typedef struct qubo_plan_desc {
   size_t workspace_bytes;
   size_t smem_bytes;
   int packed;          /* 1: int32 input whose sum |U_ij| <= 2^14 - 1 runs the minimum pass with two
-                          16-bit energies per 32-bit word (§IV-B.5's narrow path); 0: not available */
-  int biased;          /* 1: int32 input whose sum |U_ij| <= 2^22 - 1 (and not narrower) runs the
-                          minimum pass with fp32 column adds in the exact binade [2^23, 2^24) */
-  int pruned;          /* 1: the biased minimum pass forms its per-step minima only in blocks of 64
-                          Gray steps whose lower bound does not clear the best energy found so far
-                          (every state is still added; results are unchanged) */
+                          16-bit energies per 32-bit word (§IV-B.5's narrow path); planned only
+                          where block bounds are off (qubo_enable_block_bounds) */
+  int biased;          /* 1: the minimum pass adds columns as fp32 numbers in the exact binade
+                          [2^23, 2^24): int32 input whose sum |U_ij| <= 2^22 - 1, and fp32 input
+                          (its fixed-point image is scaled into that range); n >= 30 */
+  int pruned;          /* 1: the biased minimum pass forms its per-step minima only in blocks of
+                          2^6 or 2^7 Gray steps (2^7 from 14 walked bits on) whose lower bound does
+                          not clear the best energy found so far (every state is still added;
+                          results are unchanged) */
 } qubo_plan_desc;
 
 /* Minimise one QUBO. Q is a HOST pointer to n*n int32, fp32 or fp64 values (row-major).
@@ -252,6 +255,17 @@ QUBO_API int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan
  * nothing was recorded). Not thread-safe with concurrent device-resident calls. */
 QUBO_API void qubo_enable_kernel_timing(int enable);
 QUBO_API double qubo_kernel_time_ms(void);
+
+/* Block bounds in the single-problem minimum pass (on by default). They are this library's
+ * addition to the paper's walk (Terastate-per-second QUBO Brute-Force on a Single GPU, Alg. 2 and
+ * eq. 9), which is otherwise unchanged: every state is still added, and blocks of Gray steps whose
+ * lower bound clears the best energy found so far skip their per-step minima. With 0, calls
+ * planned from then on take minimum passes that form every step's minimum: the packed 16x2 pass
+ * for int32 input with sum |U| < 2^14, the biased fp32-binade pass without bounds otherwise.
+ * Results are identical either way; the switch exists to test and measure each pass.
+ * Process-wide, read when a call is planned (qubo_plan reports it in `pruned`); calls already
+ * planned are not affected. The batched calls have no bounded pass and ignore it. */
+QUBO_API void qubo_enable_block_bounds(int enable);
 
 /* Number of kernel launches the last host or device call enqueued. */
 QUBO_API int qubo_last_launch_count(void);

@@ -1,4 +1,6 @@
 """GPU parity of the k-lowest-energies entry point (through the C ABI) against the oracle."""
+import itertools
+
 import numpy as np
 import pytest
 
@@ -75,3 +77,98 @@ def test_lowest_argument_errors(q):
     assert ei.value.status == -1
     with pytest.raises(q.QuboError):
         q.solve_lowest(np.zeros((8, 8), np.int32), 0)
+
+
+# ---------------------------------------------------------------- n >= 30: the bounded driver
+# From 30 variables the driver's minimum pass runs with block bounds and a margin that it widens
+# until k states lie within it. Two instance families whose k lowest keys are known exactly at
+# that size pin it.
+
+def _full_rank(bits_by_pos, n):
+    """Ranks of the rows of a (m, n) bit matrix whose column i is variable x_i."""
+    w = np.array([1 << (n - 1 - i) for i in range(n)], dtype=np.uint64)
+    return (bits_by_pos.astype(np.uint64) * w).sum(axis=1)
+
+
+@pytest.mark.parametrize("n,n0,k,seed", [(30, 18, 1000, 1), (31, 19, 4000, 2), (32, 20, 300, 3)])
+def test_lowest_bounded_separable_instances(q, n, n0, k, seed):
+    # n0 coupled variables at random positions and n - n0 variables with a diagonal term only:
+    # E(x) = E_core(x_core) + sum_i d_i x_i. If c lies beyond the core's k lowest (ties at the
+    # k-th energy included), k core states c' have E(c') < E(c), and every (c', y) lies strictly
+    # below (c, y); so the k lowest keys combine the core's k lowest (the oracle's) with all
+    # 2^(n - n0) diagonal parts
+    rng = qi.Stream(3100 + seed)
+    pos = np.sort(np.argsort(rng.raw(n))[:n0])
+    free = np.array([i for i in range(n) if i not in set(pos.tolist())])
+    core = qi.random_upper_int(n0, -1000, 1000, 3110 + seed)
+    d = rng.integers(-400, 400, n - n0)
+    Q = np.zeros((n, n), np.int32)
+    Q[np.ix_(pos, pos)] = core
+    Q[free, free] = d
+    assert q.plan(n)["pruned"] == 1
+    # the core's k lowest keys and every other core state at the k-th energy
+    kc = k + 1
+    ce, cx = O.lowest(core, kc)
+    while len(ce) == kc and ce[-1] == ce[k - 1]:
+        kc *= 2
+        ce, cx = O.lowest(core, kc)
+    keep = ce <= ce[k - 1]
+    ce, cx = ce[keep], cx[keep]
+    f = n - n0
+    fx = ((np.arange(1 << f)[:, None] >> np.arange(f - 1, -1, -1)[None, :]) & 1).astype(np.uint8)
+    fe = fx.astype(np.int64) @ d.astype(np.int64)
+    # energy and rank of (core state a, diagonal part b): each the sum of its two parts
+    wbit = np.array([1 << (n - 1 - i) for i in range(n)], dtype=np.uint64)
+    cr = (cx.astype(np.uint64) * wbit[pos]).sum(axis=1)
+    fr = (fx.astype(np.uint64) * wbit[free]).sum(axis=1)
+    E = (ce[:, None] + fe[None, :]).reshape(-1)
+    R = (cr[:, None] + fr[None, :]).reshape(-1)
+    order = np.lexsort((R, E))[:k]
+    e, x = q.solve_lowest(Q, k)
+    assert np.array_equal(e, E[order])
+    assert np.array_equal(_full_rank(x, n), R[order])
+    U = O.fold_i32(Q)
+    for i in (0, k // 2, k - 1):
+        assert O.energy_i64(U, x[i]) == int(e[i])
+
+
+@pytest.mark.parametrize("k", [1, 100, 1500, 6000])
+def test_lowest_bounded_equal_weight_mattis(q, k):
+    # J_ij = -s*_i s*_j (i < j), h = 0, as a QUBO: Q_ij = 4 J_ij, Q_ii = -2 sum_j J_ij. With
+    # m = n - 2 L the overlap of the spins with s* at Hamming distance L, H = -(m^2 - n) / 2, so
+    # the k lowest keys are the states at distance L = 0, 1, 2, ... from x* or from its
+    # complement, by level and then by rank. The level gaps (62, 58, 54 at n = 32) exceed
+    # sum |U| / 64, so the driver's first margin holds only the two ground states
+    n = 32
+    s = qi.Stream(3200).signs(n).astype(np.int64)
+    J = -np.outer(s, s)
+    Q = np.zeros((n, n), np.int64)
+    for i in range(n):
+        for j in range(i + 1, n):
+            Q[i, j] = 4 * J[i, j]
+        Q[i, i] = -2 * (J[i].sum() - J[i, i])
+    Q = Q.astype(np.int32)
+    xs = ((s + 1) // 2).astype(np.uint8)
+    states, levels = [], []
+    for L in range(4):
+        for c in itertools.combinations(range(n), L):
+            y = xs.copy()
+            y[list(c)] ^= 1
+            states += [y, 1 - y]
+            levels += [L, L]
+    states = np.array(states, np.uint8)
+    levels = np.array(levels)
+    R = _full_rank(states, n)
+    order = np.lexsort((R, levels))[:k]
+    assert k <= len(order)
+    e, x = q.solve_lowest(Q, k)
+    assert np.array_equal(_full_rank(x, n), R[order])
+    U = O.fold_i32(Q)
+    E0 = O.energy_i64(U, xs)
+    assert int(e[0]) == E0
+    m0 = n
+    for i in range(k):
+        m = n - 2 * int(levels[order[i]])
+        assert int(e[i]) == E0 + (m0 * m0 - m * m) // 2
+    for i in sorted({0, k // 3, k - 1}):
+        assert O.energy_i64(U, x[i]) == int(e[i])

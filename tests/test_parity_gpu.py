@@ -4,6 +4,8 @@ int32: bit-exact (minimum energy, lowest-rank argmin, tie count).
 fp32:  the returned energy is the fixed-order fp64 energy of the returned state, and it lies
        within 1e-3 * sum|Q_ij| * 2^-20 of the oracle's fp64 minimum.
 """
+import contextlib
+
 import numpy as np
 import pytest
 
@@ -34,6 +36,16 @@ def check_int(q, Q, **kw):
     assert (e, t) == (want[0], want[2]), (e, t, want)
     assert (x == want[1]).all()
     return e, x, t
+
+
+@contextlib.contextmanager
+def no_bounds(q):
+    """Calls planned inside take the minimum passes without block bounds (packed or biased)."""
+    q.enable_block_bounds(False)
+    try:
+        yield
+    finally:
+        q.enable_block_bounds(True)
 
 
 # ---------------------------------------------------------------- exhaustive small sweeps
@@ -81,8 +93,15 @@ def test_infeasible_explicit_plan_is_an_error(q):
 def test_plans_pick_fast_kernel_for_large_n(q):
     p = q.plan(40)
     assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
-    # the bounded biased pass; the packed pass runs only without bounds (the k-lowest driver)
+    # the bounded biased pass; the packed pass runs only without bounds
     assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 0
+    with no_bounds(q):
+        # the packed pass is planned (it checks sum |U| < 2^14 on the device and exits at once
+        # otherwise, leaving the biased pass to run)
+        p = q.plan(40)
+        assert p["pruned"] == 0 and p["biased"] == 1 and p["packed"] == 1
+        assert q.plan(40, q.FP32)["pruned"] == 0
+    assert q.plan(40)["pruned"] == 1
     assert q.plan(8)["variant"] == 0
     # fp32 input: its fixed-point image is scaled into the biased pass's range; never packed
     assert q.plan(36, q.FP32)["biased"] == 1 and q.plan(36, q.FP32)["packed"] == 0
@@ -108,9 +127,9 @@ def _with_abs_sum(Q, total):
 
 @pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
 def test_biased_walk_range_limit_is_exact(q, sign):
-    # The minimum walk without block bounds (the k-lowest driver's) keeps column energies in the
-    # fp32 binade [2^23, 2^24) for sum |U| <= 2^22 - 1 and in int32 above; the bounded walk of
-    # solve() runs int32. Both sides of the limit through both, with running values pushed to the
+    # The biased minimum walk, with and without block bounds, keeps column energies in the fp32
+    # binade [2^23, 2^24) for sum |U| <= 2^22 - 1; above, the int32 walk runs. Both sides of the
+    # limit through both passes and the k-lowest driver, with running values pushed to the
     # extremes: all-negative entries reach E = -sum |U| at x = 1, all-positive ones +sum |U|.
     n = 30
     lo, hi = {"mixed": (-15000, 15000), "negative": (-15000, -1), "positive": (1, 15000)}[sign]
@@ -123,9 +142,13 @@ def test_biased_walk_range_limit_is_exact(q, sign):
         else:
             Q = _with_abs_sum(Q, total)
         assert int(np.abs(Q.astype(np.int64)).sum()) == total
+        assert q.plan(n)["pruned"] == 1
         e, x, t = check_int(q, Q)
         if sign == "negative":
             assert e == -total and x.all()
+        with no_bounds(q):
+            assert q.plan(n)["pruned"] == 0
+            check_int(q, Q)
         le, lx = q.solve_lowest(Q, 1)
         assert int(le[0]) == e and (lx[0] == x).all()
 
@@ -151,8 +174,8 @@ def test_fewer_threads_than_variables(q):
 
 
 # ---------------------------------------------------------------- packed 16x2 minimum pass
-# Narrow inputs (sum |U| < 2^14) take the bounded biased pass in solve() and the packed pass in
-# the k-lowest driver, whose minimum pass runs without bounds: both are checked.
+# Narrow inputs (sum |U| < 2^14) take the bounded biased pass by default and the packed pass
+# without block bounds: both are checked, and the k-lowest driver on the same inputs.
 
 @pytest.mark.parametrize("n,lo,hi,seed", [(30, -30, 30, 1), (30, -9, 9, 3), (31, -3, 3, 4), (31, 0, 2, 5)])
 def test_packed_pass_small_range(q, n, lo, hi, seed):
@@ -160,14 +183,17 @@ def test_packed_pass_small_range(q, n, lo, hi, seed):
     assert int(np.abs(Q.astype(np.int64)).sum()) <= (1 << 14) - 1
     assert q.plan(n)["packed"] == 0 and q.plan(n)["pruned"] == 1
     e, x, t = check_int(q, Q)
-    le, lx = q.solve_lowest(Q, 1)  # the packed pass
+    with no_bounds(q):
+        assert q.plan(n)["packed"] == 1 and q.plan(n)["pruned"] == 0
+        check_int(q, Q)  # the packed pass: every unit minimum feeds the tie and argmin passes
+    le, lx = q.solve_lowest(Q, 1)
     assert int(le[0]) == e and (lx[0] == x).all()
 
 
 @pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
 def test_packed_range_limit_is_exact(q, sign):
-    # without bounds (solve_lowest) sum |U| = 2^14 - 1 runs the packed pass (values pushed to
-    # +-sum |U|), 2^14 the biased one; solve() runs the bounded biased pass on both
+    # without bounds sum |U| = 2^14 - 1 runs the packed pass (values pushed to +-sum |U|), 2^14
+    # the biased one; with bounds both run the bounded biased pass
     n = 30
     lo, hi = {"mixed": (-50, 50), "negative": (-50, -1), "positive": (1, 50)}[sign]
     for total in ((1 << 14) - 1, 1 << 14):
@@ -182,16 +208,21 @@ def test_packed_range_limit_is_exact(q, sign):
         e, x, t = check_int(q, Q)
         if sign == "negative":
             assert e == -total and x.all()
+        with no_bounds(q):
+            assert q.plan(n)["packed"] == 1  # planned; on the device it runs below 2^14 only
+            check_int(q, Q)
         le, lx = q.solve_lowest(Q, 1)
         assert int(le[0]) == e and (lx[0] == x).all()
 
 
 def test_packed_pass_all_ties(q):
     # Q = 0: every state ties; every block's bound equals the threshold, so the bounded pass walks
-    # every block exactly, and the resolve pass counts 2^n; the packed pass (k lowest) sees 0 too
+    # every block exactly, and the resolve pass counts 2^n; so does the packed pass
     Z = np.zeros((30, 30), np.int32)
     e, x, t = q.solve(Z)
     assert (e, t) == (0, 1 << 30) and not x.any()
+    with no_bounds(q):
+        assert q.solve(Z)[2] == 1 << 30
     le, lx = q.solve_lowest(Z, 3)
     assert list(le) == [0, 0, 0] and [oracle.rank_of_bits(v) for v in lx] == [0, 1, 2]
 
