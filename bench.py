@@ -380,7 +380,8 @@ def run_gb300(args):
                    "tie_count": int(r["tie_count"]), "checks": checks},
         "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "search_kernel<16,5,min,biased,bounded> (enumeration, biased fp32-binade minimum pass with block bounds)", "kernel_ms": kern,
+                     "kernel": ("search_kernel<16,R,min,biased,bounded> (enumeration, biased fp32-binade minimum pass "
+                                "with block bounds; R = 7 register rows at n=40)"), "kernel_ms": kern,
                      "peak_basis": "152 SMs x 128 lanes/clk (4 schedulers x 32 lanes: the issue limit of one "
                                    "add per state) x 2.07 GHz max SM clock",
                      "traffic_source": traffic_src,
@@ -492,7 +493,7 @@ def run_gb300_sharded(args):
                        "checks": checks},
             "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "Tops/s (int32 lane-ops)",
                          "frac": achieved / peak, "traffic": None,
-                         "kernel": "search_kernel<16,5,min,biased,bounded> on rank 0's shard", "kernel_ms": kern,
+                         "kernel": "search_kernel<16,R,min,biased,bounded> on rank 0's shard", "kernel_ms": kern,
                          "kernel_ms_max_over_ranks": kern_max,
                          "peak_basis": "152 SMs x 128 lanes/clk x 2.07 GHz max SM clock"},
             "e2e": {"value": STATES / (e2e * 1e-3), "unit": UNIT, "h2d_bytes_per_step": world * N * N * 4,
@@ -523,7 +524,9 @@ def other_configs(q, torch, dev, stream):
         return e0.elapsed_time(e1) / reps
 
     for name, n, Q, dt in (("n40_narrow_int32", 40, qi.workload_n40_narrow(), q.INT32),
-                           ("n36_fp32", 36, qi.workload_n36_f32(), q.FP32), ("n32_int32", 32, qi.workload_n32(), q.INT32),
+                           ("n36_fp32", 36, qi.workload_n36_f32(), q.FP32),
+                           ("n36_wide_int32", 36, qi.workload_n36_wide(), q.INT32),
+                           ("n32_int32", 32, qi.workload_n32(), q.INT32),
                            ("n32_mattis_int32", 32, qi.workload_n32_mattis()[0], q.INT32),
                            ("n20_int32", 20, qi.workload_n20(), q.INT32)):
         dq = torch.from_numpy(Q).to(dev)
@@ -534,14 +537,36 @@ def other_configs(q, torch, dev, stream):
         kern = q.kernel_time_ms()
         out[name] = {"ms": ms, "states_per_s": (1 << n) / (ms * 1e-3), "min_pass_ms": kern,
                      "min_pass_states_per_s": (1 << n) / (kern * 1e-3) if kern > 0 else None}
-        if name == "n36_fp32":
+        if name in ("n36_fp32", "n36_wide_int32", "n40_narrow_int32"):
             r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
-            tol = 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
-            out[name]["check"] = check_result("n36_fp32", float(r["min_energy"]), int(r["argmin_rank"]),
+            tol = 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20 if dt == q.FP32 else 0.0
+            out[name]["check"] = check_result(name, float(r["min_energy"]), int(r["argmin_rank"]),
                                               int(r["tie_count"]), tol)
         if name == "n40_narrow_int32":
             out[name]["workload"] = ("n=40 dense QUBO, int32 upper-triangular, entries uniform in [-4,4] "
-                                     "(sum |U| = 1822: the packed 16x2 minimum pass)")
+                                     "(sum |U| = 1822: the bounded biased pass; the packed 16x2 pass "
+                                     "runs without bounds, below)")
+        if name == "n36_wide_int32":
+            out[name]["workload"] = ("n=36 dense QUBO, int32 upper-triangular, entries uniform in "
+                                     "[-2^20, 2^20] (sum |U| ~ 3.5e8 > 2^22: the int32 minimum pass)")
+    # the minimum passes without block bounds, on the n=40 workloads (same results)
+    q.enable_block_bounds(False)
+    try:
+        for name, Q in (("n40_int32_without_bounds", qi.workload_n40()),
+                        ("n40_narrow_int32_without_bounds", qi.workload_n40_narrow())):
+            dq = torch.from_numpy(Q).to(dev)
+            nb = q.workspace_bytes(40, q.INT32)
+            ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+            res = torch.zeros(32, dtype=torch.uint8, device=dev)
+            ms = timed(lambda: q.solve_device(40, dq, q.INT32, ws, nb, stream.cuda_stream, res), reps=2)
+            kern = q.kernel_time_ms()
+            out[name] = {"ms": ms, "states_per_s": (1 << 40) / (ms * 1e-3), "min_pass_ms": kern,
+                         "pass": "biased fp32-binade pass" if "narrow" not in name else "packed 16x2 pass"}
+            r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
+            out[name]["check"] = check_result(name.replace("_without_bounds", ""), float(r["min_energy"]),
+                                              int(r["argmin_rank"]), int(r["tie_count"]))
+    finally:
+        q.enable_block_bounds(True)
     # k lowest energies of the n=40 workload through the host entry point (wall clock)
     Q40 = qi.workload_n40()
     q.solve_lowest(Q40, 1024)
@@ -603,6 +628,8 @@ def profile_case(n: int, dtype_name: str):
         Q, dt = qi.random_symmetric_normal_f32(n, qi.MASTER_SEED + 3), q.FP32
     elif dtype_name == "int32_narrow":
         Q, dt = qi.random_upper_int(n, -4, 4, qi.MASTER_SEED + 5), q.INT32
+    elif dtype_name == "int32_wide":
+        Q, dt = qi.random_upper_int(n, -(1 << 20), 1 << 20, qi.MASTER_SEED + 7), q.INT32
     else:
         Q, dt = qi.random_upper_int(n, -1000, 1000, qi.MASTER_SEED + 2), q.INT32
     dq = torch.from_numpy(Q).cuda()
@@ -629,7 +656,7 @@ def main(argv=None):
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="only run two searches of an N-variable instance (for ncu), print no JSON")
-    ap.add_argument("--profile-dtype", choices=["int32", "fp32", "int32_narrow"], default="int32")
+    ap.add_argument("--profile-dtype", choices=["int32", "fp32", "int32_narrow", "int32_wide"], default="int32")
     ap.add_argument("--oracle-configs", type=float, default=0.0, metavar="SECONDS",
                     help="time the CPU oracle on every workload (one core and all cores) and exit")
     ap.add_argument("--profile-batched", type=int, default=0, metavar="B",

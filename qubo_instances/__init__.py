@@ -190,6 +190,12 @@ def workload_n40_narrow():
     return random_upper_int(40, -4, 4, MASTER_SEED + 5)
 
 
+def workload_n36_wide():
+    """n=36 dense, entries uniform in [-2^20, 2^20]: sum |U| ~ 3.5e8, beyond the fp32 binade
+    (2^22), so the minimum pass adds in int32."""
+    return random_upper_int(36, -(1 << 20), 1 << 20, MASTER_SEED + 7)
+
+
 def workload_n36_f32():
     return random_symmetric_normal_f32(36, MASTER_SEED + 3)
 

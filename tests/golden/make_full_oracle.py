@@ -1,11 +1,11 @@
-"""Writes the full-search oracle results of the n=36 fp32 and n=40 int32 workloads.
+"""Writes the full-search oracle results of the n=36 and n=40 workloads that the bench checks.
 
 Every state of each workload is evaluated by the CPU oracle (oracle_gray: the O(n)-per-step Gray
 walk over all 2^n states, OpenMP over leading-bit slices); nothing here touches the CUDA path.
 The n=40 run takes hours on a few cores, so its result is stored and the GPU tests compare
 against the stored value.
 
-    python tests/golden/make_full_oracle.py [n36_fp32] [n40_int32]
+    python tests/golden/make_full_oracle.py [n36_fp32] [n40_int32] [n36_wide_int32] [n40_narrow_int32]
 """
 import os
 import sys
@@ -21,6 +21,10 @@ CASES = {
     "n36_fp32": ("n=36 fp32, entries N(0,1), symmetric (qubo_instances.workload_n36_f32)", qi.workload_n36_f32),
     "n40_int32": ("n=40 int32, upper-triangular, entries uniform in [-1000, 1000] (qubo_instances.workload_n40)",
                   qi.workload_n40),
+    "n36_wide_int32": ("n=36 int32, upper-triangular, entries uniform in [-2^20, 2^20] "
+                       "(qubo_instances.workload_n36_wide)", qi.workload_n36_wide),
+    "n40_narrow_int32": ("n=40 int32, upper-triangular, entries uniform in [-4, 4] "
+                         "(qubo_instances.workload_n40_narrow)", qi.workload_n40_narrow),
 }
 
 
