@@ -280,7 +280,7 @@ def max_over_ranks(values, device):
 def run_gb300(args):
     import torch
     rank, world, local = dist_env()
-    if world > 1:
+    if world > 1 or args.sharded:
         return run_gb300_sharded(args)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -658,6 +658,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-extra", action="store_true", help="skip the other workloads")
+    ap.add_argument("--sharded", action="store_true",
+                    help="time the slice-sharded search (the N > 1 path) even with one rank (run under torchrun)")
     ap.add_argument("--profile-case", type=int, default=0, metavar="N",
                     help="only run two searches of an N-variable instance (for ncu), print no JSON")
     ap.add_argument("--profile-dtype", choices=["int32", "fp32", "int32_narrow", "int32_wide"], default="int32")

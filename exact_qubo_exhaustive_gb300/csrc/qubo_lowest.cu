@@ -119,7 +119,7 @@ extern "C" int qubo_solve_lowest(int n, const void* Q, int dtype, int k_prefix, 
   int64_t margin = bounded ? std::max<int64_t>(64, abs_sum / 64) : 0;
   auto min_stage = [&]() -> int {
     if (abort_requested()) return QUBO_ERR_ABORTED;
-    p.bound_margin = (int)std::min<int64_t>(margin, 4 * abs_sum + 64);
+    p.bound_margin = (int)std::min<int64_t>(margin, 2 * abs_sum);  // 2S < 2^31: S < 2^30 for int32
     int nl = 0;
     cudaError_t ee;
     if ((ee = run_min_stage(p, dQ, w, s, &nl, &kp)) != cudaSuccess) return record_cuda_error(ee, "kernel launch");

@@ -378,6 +378,7 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   kp.T2 = w.T2;
   kp.blk = w.blk;
   kp.margin = p.bound_margin;
+  kp.one = 1;
   kp.gthr = w.gthr;
   kp.gbase = w.gbase;
   kp.unit_min = w.unit_min;
@@ -420,8 +421,12 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
       if (e != cudaSuccess) return e;
       ++nl;
     }
-    // ... and the int32 CUDA-core pass (exits at once when another pass ran)
-    if (p.variant == kFast && p.w >= kIntMinR + 1) {
+    // ... and the int32 CUDA-core pass, with block bounds where planned (exits at once when
+    // another pass ran)
+    if (p.prune) {
+      if ((e = launch_search_int_pruned(p.prune_r, kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess)
+        return e;
+    } else if (p.variant == kFast && p.w >= kIntMinR + 1) {
       if ((e = launch_search_int_min5(kp, blocks, p.threads, p.smem_bytes, stream)) != cudaSuccess) return e;
     } else if ((e = launch_search(p, kModeMin, kp, blocks, stream)) != cudaSuccess) {
       return e;

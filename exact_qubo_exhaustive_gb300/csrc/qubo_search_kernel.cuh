@@ -27,6 +27,7 @@ struct KParams {
   const BlockCtl* blk;      // block-bounded minimum pass: per-block minimum of T and following flip
   int32_t* gthr;            // pruned minimum passes: best energy published so far, per group
   int margin;               // extra margin of the block bound test (image units)
+  int one;                  // 1: the int32 bounded walk derives its opaque constants from it
   const uint64_t* gbase;
   int32_t* unit_min;
   uint32_t* tied;
@@ -83,12 +84,13 @@ __device__ __forceinline__ int min_walk(const WalkCtx& c, const KParams& p, int 
 
 // BIASED: the minimum pass with column energies in the biased fp32 binade (VOps<float>). Which
 // minimum pass of a launch sequence runs is decided on the device by min_pass_owner.
-// PRUNE: the minimum pass with block bounds (PrunedMinWalker); unit minima above the group's
-// best are then only upper bounds of the true ones (see PrunedMinWalker).
+// PRUNE: the minimum pass with block bounds (PrunedMinWalker, biased fp32 or int32 columns);
+// unit minima above the group's best are then only upper bounds of the true ones (see
+// PrunedMinWalker).
 template <int CPT, int R, int MODE, bool BIASED = false, bool PRUNE = false>
 __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const KParams p) {
   static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
-  static_assert(!PRUNE || (MODE == kModeMin && BIASED && CPT == 16), "pruned walk: biased minimum pass, fast layout");
+  static_assert(!PRUNE || (MODE == kModeMin && CPT == 16), "pruned walk: minimum pass, fast layout");
   extern __shared__ __align__(16) int4 s_rows4[];
   // linear terms; the block-bounded pass also keeps -L at 64 + v and a zero at 128
   __shared__ int sL[PRUNE ? 129 : 64];
@@ -182,10 +184,12 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
     if constexpr (MODE == kModeMin) {
       int best;
       if constexpr (PRUNE) {
-        PrunedMinWalker<R> W;
+        using VT = typename std::conditional<BIASED, float, int>::type;
+        PrunedMinWalker<R, VT> W;
         W.init(c, p.Ec, p.M, cP);
-        W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band + p.margin);  // two blocks per iteration
-        best = W.aux - VOps<float>::kBiasBits + W.s;
+        // two blocks per iteration
+        W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band + p.margin, p.one);
+        best = W.aux - VOps<VT>::kBiasBits + W.s;
       } else if (niter == 0) {
         // no walked variable (generic variant only): the single walked assignment is 0
         Walker<CPT, R, MODE> W;
@@ -251,6 +255,7 @@ cudaError_t launch_search_fast(int mode, const KParams& p, int blocks, int threa
 cudaError_t launch_search_biased(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_int_min5(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_biased_pruned(int R, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
+cudaError_t launch_search_int_pruned(int R, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t occupancy_packed(int threads, size_t smem, int* blocks_per_sm);
 size_t packed_smem_bytes(int C, int w);

@@ -32,6 +32,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "qubo_internal.h"
 
@@ -618,13 +619,21 @@ struct Walker {
 };
 
 // ------------------------------------------------------------------------------------------------
-// Minimum walk with block bounds (kModeMin, biased fp32 binade, 16 columns x 256 threads).
+// Minimum walk with block bounds (kModeMin, 16 columns x 256 threads; column energies in the
+// biased fp32 binade, or in int32 where sum |U_ij| is too large for the binade).
 //
 // Every state still costs its one add (eq. 9): each Gray step adds a walked row to all of the
-// thread's column energies with an fp32 add (an fp32 add is never merged or reordered by the
-// compiler, so every intermediate column energy is formed). What a block bound saves is the
-// minimum over the columns. A block is the 2^R steps between two shared-memory flips; inside it
-// only the register rows flip, so s is constant and, for every step d of block m and column j,
+// thread's column energies, in a form the compiler can neither merge nor drop, so every
+// intermediate column energy is formed:
+//  * fp32: an fp32 add, two columns per fp32x2 instruction (fp32 addition does not reassociate);
+//  * int32: a fused add-min against a bound of INT_MAX that the compiler cannot see (ALU pipe)
+//    where the flip adds the row, and a multiply-add by a -1 it cannot see (the FMA pipe's
+//    integer unit) where it subtracts it or where the sign is only known at run time. Plain
+//    integer adds would not do: additions whose intermediate sums nobody reads reassociate, and
+//    the compiler folds them. The two kinds split the adds between the two pipes.
+// What a block bound saves is the minimum over the columns. A block is the 2^R steps between two
+// shared-memory flips; inside it only the register rows flip, so s is constant and, for every
+// step d of block m and column j,
 //     E(d, j) - s = T[2^R m + d] + V_d[j] >= Tmin_m + min_j V_0[j] + D_par,
 // where Tmin_m is the least walked energy of the block (a table), V_0 the columns at the
 // block's first state and D_par <= 0 the most negative change of any of the thread's columns
@@ -644,12 +653,19 @@ struct Walker {
 // unit holding such a state reports its minimum exactly, every other unit reports the energy of
 // a state it evaluated (above E* + band), and the group minimum and the list of units within the
 // band are exactly those of the plain walk; the resolution passes are unchanged.
+//
+// Ranges (int32, sum |U_ij| = S < 2^30): column energies, walked energies, D_par and energies lie
+// in [-S, S], the running best minus s in [-2S, 2S]; the bound with band and margin (up to 2S)
+// reaches -4S and is formed in 64 bits.
 // ------------------------------------------------------------------------------------------------
-template <int R>
-struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
-  using B = Walker<16, R, kModeMin, float>;
-  using O = VOps<float>;
+template <int R, typename VT = float>
+struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
+  using B = Walker<16, R, kModeMin, VT>;
+  using O = VOps<VT>;
+  using V4 = typename O::V4;
   using RowBuf = typename B::RowBuf;
+  using LB = typename std::conditional<O::kInt, long long, int>::type;  // bound arithmetic
+  static constexpr bool kInt = O::kInt;
   static constexpr int kCPT = 16;
   static constexpr int kThreads = 256;      // 2^12 columns: the quad stride is a constant
   static constexpr int kBlock = 1 << R;     // steps per block
@@ -657,82 +673,154 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   static constexpr int kReadMask = 7;       // blocks between two reads of the group's best
   static_assert(R >= 3, "whole quads of walked energies per block");
   static_assert(kThreads * kCPT == 4096, "the control table's row offsets assume 2^12 columns");
+  // int32 walk: the columns in kSkewGroups groups, group G kSkewLag * G flips behind group 0, so
+  // that the add-mins (ALU pipe) of one flip meet the multiply-adds (FMA pipe) of another
+  static constexpr int kSkewGroups = 1;
+  static constexpr int kSkewLag = 2;
+  static constexpr int kSkewCols = kCPT / kSkewGroups;
 
   int dmin0, dmin1;  // D_par of even and odd blocks
   int g_best;        // G: the group's best energy known to this warp (absolute, image units)
+  int big;           // int32 walk: INT_MAX, the add-min's bound (from a kernel parameter)
+  int mone;          // int32 walk: -1 (from a kernel parameter)
 
-  // Column pairs: one fp32x2 instruction adds (or adds with a sign) the rows of two columns.
-  __device__ __forceinline__ void pair_add(int jj, float r0, float r1) {
-    const float2 t = __fadd2_rn(make_float2(this->V[jj], this->V[jj + 1]), make_float2(r0, r1));
-    this->V[jj] = t.x;
-    this->V[jj + 1] = t.y;
+  // --- column updates of the column pair (jj, jj + 1): the row added, subtracted, or added with
+  // a sign known only at run time (+1, -1, or 0 for no change).
+  __device__ __forceinline__ void cols_add(int jj, VT r0, VT r1) {
+    if constexpr (kInt) {
+      this->V[jj] = __viaddmin_s32(this->V[jj], r0, big);
+      this->V[jj + 1] = __viaddmin_s32(this->V[jj + 1], r1, big);
+    } else {
+      const float2 t = __fadd2_rn(make_float2(this->V[jj], this->V[jj + 1]), make_float2(r0, r1));
+      this->V[jj] = t.x;
+      this->V[jj + 1] = t.y;
+    }
   }
-  __device__ __forceinline__ void pair_fma(int jj, float r0, float r1, float2 sg) {
-    const float2 t = __ffma2_rn(make_float2(r0, r1), sg, make_float2(this->V[jj], this->V[jj + 1]));
-    this->V[jj] = t.x;
-    this->V[jj + 1] = t.y;
+  __device__ __forceinline__ void cols_sgn(int jj, VT r0, VT r1, VT sg) {
+    if constexpr (kInt) {
+      asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(this->V[jj]) : "r"(r0), "r"(sg));
+      asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(this->V[jj + 1]) : "r"(r1), "r"(sg));
+    } else {
+      const float2 t = __ffma2_rn(make_float2(r0, r1), make_float2(sg, sg), make_float2(this->V[jj], this->V[jj + 1]));
+      this->V[jj] = t.x;
+      this->V[jj + 1] = t.y;
+    }
+  }
+  __device__ __forceinline__ VT minus_one() const {
+    if constexpr (kInt) return mone;
+    else return -1.f;
+  }
+  __device__ __forceinline__ void cols_sub(int jj, VT r0, VT r1) { cols_sgn(jj, r0, r1, minus_one()); }
+  __device__ __forceinline__ void row_add(const VT* row) {
+#pragma unroll
+    for (int jj = 0; jj < kCPT; jj += 2) cols_add(jj, row[jj], row[jj + 1]);
+  }
+  __device__ __forceinline__ void row_sgn(const VT* row, VT sg) {
+#pragma unroll
+    for (int jj = 0; jj < kCPT; jj += 2) cols_sgn(jj, row[jj], row[jj + 1], sg);
+  }
+
+  // Flip D of a block (0 <= D < kBlock - 1) on the kSkewCols columns from j0 (int32 walk).
+  template <int D>
+  __device__ __forceinline__ void flip_cols(int j0, VT sgn) {
+    constexpr int a = ctz_c(D + 1);
+    constexpr int bit = ((D >> a) ^ (D >> (a + 1))) & 1;
+#pragma unroll
+    for (int j = j0; j < j0 + kSkewCols; ++j) {
+      if constexpr (a == R - 1) {
+        asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(this->V[j]) : "r"(this->Row[a][j]), "r"(sgn));
+      } else if constexpr (bit) {
+        asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(this->V[j]) : "r"(this->Row[a][j]), "r"(mone));
+      } else {
+        this->V[j] = __viaddmin_s32(this->V[j], this->Row[a][j], big);
+      }
+    }
+  }
+  // Slot T of the skewed block walk: column group G takes flip T - kSkewLag * G.
+  template <int T, int G = 0>
+  __device__ __forceinline__ void skew_slot(VT sgn) {
+    if constexpr (G < kSkewGroups) {
+      constexpr int D = T - kSkewLag * G;
+      if constexpr (D >= 0 && D + 1 < kBlock) flip_cols<D>(G * kSkewCols, sgn);
+      skew_slot<T, G + 1>(sgn);
+    }
+  }
+  template <int T>
+  __device__ __forceinline__ void body_skew(VT sgn) {
+    if constexpr (T < kBlock - 1 + kSkewLag * (kSkewGroups - 1)) {
+      skew_slot<T>(sgn);
+      body_skew<T + 1>(sgn);
+    }
   }
 
   // Flips of steps 0..kBlock-2 of a block; position R-1 flips once, with sign sgn (+1 in even
   // blocks, -1 in odd ones); the others with the sign their Gray bit fixes.
   template <int D>
-  __device__ __forceinline__ void body(float sgn) {
-    if constexpr (D + 1 < kBlock) {
+  __device__ __forceinline__ void body(VT sgn) {
+    if constexpr (kInt && kSkewGroups > 1) {
+      if constexpr (D == 0) body_skew<0>(sgn);
+    } else if constexpr (D + 1 < kBlock) {
       constexpr int a = ctz_c(D + 1);
       if constexpr (a == R - 1) {
-#pragma unroll
-        for (int jj = 0; jj < kCPT; jj += 2) pair_fma(jj, this->Row[a][jj], this->Row[a][jj + 1], make_float2(sgn, sgn));
+        row_sgn(this->Row[a], sgn);
       } else {
         constexpr int bit = ((D >> a) ^ (D >> (a + 1))) & 1;  // bit a of gray(D): 1 -> the flip clears it
-#pragma unroll
-        for (int jj = 0; jj < kCPT; jj += 2) {
-          if (bit) pair_fma(jj, this->Row[a][jj], this->Row[a][jj + 1], make_float2(-1.f, -1.f));
-          else pair_add(jj, this->Row[a][jj], this->Row[a][jj + 1]);
-        }
+        if (bit) row_sgn(this->Row[a], minus_one());
+        else row_add(this->Row[a]);
       }
       body<D + 1>(sgn);
     }
   }
 
   __device__ __forceinline__ void init_bounds() {
-    float lo0 = 0.f, lo1 = 0.f;
+    if constexpr (kInt) {
+      int lo0 = 0, lo1 = 0;
 #pragma unroll
-    for (int jj = 0; jj < kCPT; ++jj) {
-      float neg = 0.f;  // sum of the negative parts of rows 0..R-2 (exact: integer-valued)
+      for (int jj = 0; jj < kCPT; ++jj) {
+        int neg = 0;  // sum of the negative parts of rows 0..R-2
 #pragma unroll
-      for (int a = 0; a < R - 1; ++a) neg = __fadd_rn(neg, fminf(this->Row[a][jj], 0.f));
-      const float r = this->Row[R - 1][jj];
-      lo0 = fminf(lo0, __fadd_rn(neg, fminf(r, 0.f)));
-      lo1 = fminf(lo1, __fadd_rn(neg, fminf(-r, 0.f)));
+        for (int a = 0; a < R - 1; ++a) neg += min(this->Row[a][jj], 0);
+        const int r = this->Row[R - 1][jj];
+        lo0 = min(lo0, neg + min(r, 0));
+        lo1 = min(lo1, neg + min(-r, 0));
+      }
+      dmin0 = lo0;
+      dmin1 = lo1;
+    } else {
+      float lo0 = 0.f, lo1 = 0.f;
+#pragma unroll
+      for (int jj = 0; jj < kCPT; ++jj) {
+        float neg = 0.f;  // sum of the negative parts of rows 0..R-2 (exact: integer-valued)
+#pragma unroll
+        for (int a = 0; a < R - 1; ++a) neg = __fadd_rn(neg, fminf(this->Row[a][jj], 0.f));
+        const float r = this->Row[R - 1][jj];
+        lo0 = fminf(lo0, __fadd_rn(neg, fminf(r, 0.f)));
+        lo1 = fminf(lo1, __fadd_rn(neg, fminf(-r, 0.f)));
+      }
+      dmin0 = static_cast<int>(lo0);
+      dmin1 = static_cast<int>(lo1);
     }
-    dmin0 = static_cast<int>(lo0);
-    dmin1 = static_cast<int>(lo1);
   }
 
   // One block: bound test, then the walk with or without per-step minima. On return V holds the
   // block's last state. lbo = the block's least walked energy + D_par - band; thr = min(this
-  // thread's best, G) relative to s, both in the biased bit image.
-  __device__ __forceinline__ void block(const WalkCtx& c, int m, int lbo, int thr, float sgn) {
-    const int m0 = vmin_bits<float, kCPT>(this->V);
-    // biased binade: |every term| <= 4 sum|U| < 2^24, far inside int32 around the bias
-    if (__all_sync(0xffffffffu, m0 + lbo > thr)) {
+  // thread's best, G) relative to s, both in the order image of the column energies.
+  __device__ __forceinline__ void block(const WalkCtx& c, int m, LB lbo, int thr, VT sgn) {
+    const int m0 = vmin_bits<VT, kCPT>(this->V);
+    // biased binade: |every term| <= 4 sum|U| < 2^24, far inside int32 around the bias;
+    // int32: the sum is formed in 64 bits
+    if (__all_sync(0xffffffffu, static_cast<LB>(m0) + lbo > thr)) {
       body<0>(sgn);
     } else {
       exact_block(c, m, m0, sgn);
     }
   }
 
-  // Flip of a register row whose position and sign are known at run time.
-  __device__ __forceinline__ void flip_rt(const float* row, float sg) {
-#pragma unroll
-    for (int jj = 0; jj < kCPT; jj += 2) pair_fma(jj, row[jj], row[jj + 1], make_float2(sg, sg));
-  }
-
   // Register row a (2 <= a < R) added with sign sg.
   template <int A = 2>
-  __device__ __forceinline__ void flip_row_rt(int a, float sg) {
+  __device__ __forceinline__ void flip_row_rt(int a, VT sg) {
     if constexpr (A < R) {
-      if (a == A) flip_rt(this->Row[A], sg);
+      if (a == A) row_sgn(this->Row[A], sg);
       else flip_row_rt<A + 1>(a, sg);
     }
   }
@@ -740,28 +828,27 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   // The block walked with every per-step minimum (rare: the bound did not clear it). A loop over
   // groups of four steps keeps the code small: in group k the flips of steps 4k and 4k + 2 are
   // row 0 (+, -), of step 4k + 1 row 1 (- when k is odd), of step 4k + 3 row 2 + ctz(k + 1).
-  __device__ __forceinline__ void exact_block(const WalkCtx& c, int m, int m0, float sgn) {
+  __device__ __forceinline__ void exact_block(const WalkCtx& c, int m, int m0, VT sgn) {
     static_assert(R >= 3, "groups of four steps: rows 0 and 1 inside, rows 2..R-1 between");
     const int4* T4 = reinterpret_cast<const int4*>(c.T) + (static_cast<uint32_t>(m) << (R - 2));
+    const VT one = -minus_one();
     int4 tq = __ldg(T4);
     this->aux = __viaddmin_s32(m0, tq.x, this->aux);
 #pragma unroll 1
     for (int k = 0; k < kBlock / 4; ++k) {
-#pragma unroll
-      for (int jj = 0; jj < kCPT; jj += 2) pair_add(jj, this->Row[0][jj], this->Row[0][jj + 1]);
-      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.y, this->aux);
-      flip_rt(this->Row[1], (k & 1) ? -1.f : 1.f);
-      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.z, this->aux);
-#pragma unroll
-      for (int jj = 0; jj < kCPT; jj += 2) pair_fma(jj, this->Row[0][jj], this->Row[0][jj + 1], make_float2(-1.f, -1.f));
-      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.w, this->aux);
+      row_add(this->Row[0]);
+      this->aux = __viaddmin_s32(vmin_bits<VT, kCPT>(this->V), tq.y, this->aux);
+      row_sgn(this->Row[1], (k & 1) ? minus_one() : one);
+      this->aux = __viaddmin_s32(vmin_bits<VT, kCPT>(this->V), tq.z, this->aux);
+      row_sgn(this->Row[0], minus_one());
+      this->aux = __viaddmin_s32(vmin_bits<VT, kCPT>(this->V), tq.w, this->aux);
       if (k + 1 == kBlock / 4) break;  // the block's last state
       const int a = 2 + __ffs(k + 1) - 1;
       const int d = 4 * k + 3;
-      const float sg = (a == R - 1) ? sgn : ((((d >> a) ^ (d >> (a + 1))) & 1) ? -1.f : 1.f);
+      const VT sg = (a == R - 1) ? sgn : ((((d >> a) ^ (d >> (a + 1))) & 1) ? minus_one() : one);
       flip_row_rt(a, sg);
       tq = __ldg(T4 + k + 1);
-      this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), tq.x, this->aux);
+      this->aux = __viaddmin_s32(vmin_bits<VT, kCPT>(this->V), tq.x, this->aux);
     }
   }
 
@@ -781,35 +868,39 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, float> {
   // Whole unit: nblocks (even, < 2^31) blocks of 2^R steps, each but the last followed by a
   // shared-row flip; blk: per-block control (least T, the flip that follows; one padding entry);
   // c.sL holds L, -L at 64 + v and a zero at 128. gbest: the group's published best (absolute
-  // image units); band: resolution band.
+  // image units); band: resolution band plus margin; one: a kernel parameter equal to 1.
   __device__ __forceinline__ void walk(const WalkCtx& c, int nblocks, const BlockCtl* __restrict__ blk, int* gbest,
-                                       int band) {
+                                       int band, int one) {
+    big = kIntInf - (one - 1);
+    mone = -one;
     init_bounds();
-    const int dmb0 = dmin0 - band, dmb1 = dmin1 - band;
+    const LB dmb0 = static_cast<LB>(dmin0) - band, dmb1 = static_cast<LB>(dmin1) - band;
     g_best = __ldcg(gbest);
     // a real best from the first state's columns, so the running best never leaves its range
-    this->aux = __viaddmin_s32(vmin_bits<float, kCPT>(this->V), __ldg(c.T), kIntInf);
+    this->aux = __viaddmin_s32(vmin_bits<VT, kCPT>(this->V), __ldg(c.T), kIntInf);
     const int4* ctl4 = reinterpret_cast<const int4*>(blk);
-    const float4* rows = reinterpret_cast<const float4*>(c.rows4) + c.thread;
+    const V4* rows = reinterpret_cast<const V4*>(c.rows4) + c.thread;
     int4 ctl = __ldg(ctl4);
     for (int m = 0; m < nblocks; ++m) {
       const int4 next = __ldg(ctl4 + m + 1);  // one block ahead (the table has a padding entry)
       RowBuf rb;
       {
-        const float4* rp = rows + ctl.y;  // in flight while the block is walked
+        const V4* rp = rows + ctl.y;  // in flight while the block is walked
 #pragma unroll
         for (int k = 0; k < kCPT / 4; ++k) rb.q[k] = rp[k * kThreads];
       }
       const bool odd = m & 1;
       const int thr = min(this->aux, O::kBiasBits + g_best - this->s);
-      block(c, m, ctl.x + (odd ? dmb1 : dmb0), thr, odd ? -1.f : 1.f);
+      block(c, m, static_cast<LB>(ctl.x) + (odd ? dmb1 : dmb0), thr, odd ? minus_one() : -minus_one());
       // the flip that follows (a no-op after the last block: sign 0, linear term 0)
-      const float dsgn = __int_as_float(ctl.z);
-      const float2 dsgn2 = make_float2(dsgn, dsgn);
+      const float dsgn_f = __int_as_float(ctl.z);
+      VT dsgn;
+      if constexpr (kInt) dsgn = static_cast<int>(dsgn_f);
+      else dsgn = dsgn_f;
 #pragma unroll
       for (int k = 0; k < kCPT / 4; ++k) {
-        pair_fma(4 * k + 0, rb.q[k].x, rb.q[k].y, dsgn2);
-        pair_fma(4 * k + 2, rb.q[k].z, rb.q[k].w, dsgn2);
+        cols_sgn(4 * k + 0, rb.q[k].x, rb.q[k].y, dsgn);
+        cols_sgn(4 * k + 2, rb.q[k].z, rb.q[k].w, dsgn);
       }
       const int dl = c.sL[ctl.w];
       this->s += dl;

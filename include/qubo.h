@@ -97,8 +97,9 @@ typedef struct qubo_plan_desc {
   int biased;          /* 1: the minimum pass adds columns as fp32 numbers in the exact binade
                           [2^23, 2^24): int32 input whose sum |U_ij| <= 2^22 - 1, and fp32 input
                           (its fixed-point image is scaled into that range); n >= 30 */
-  int pruned;          /* 1: the biased minimum pass forms its per-step minima only in blocks of
-                          2^6 or 2^7 Gray steps (2^7 from 14 walked bits on) whose lower bound does
+  int pruned;          /* 1: the minimum pass (biased fp32 columns, or int32 columns where sum
+                          |U_ij| is too large for them) forms its per-step minima only in blocks of
+                          2^6 or 2^7 Gray steps (2^7 from 12 walked bits on) whose lower bound does
                           not clear the best energy found so far (every state is still added;
                           results are unchanged) */
 } qubo_plan_desc;
@@ -261,7 +262,8 @@ QUBO_API double qubo_kernel_time_ms(void);
  * eq. 9), which is otherwise unchanged: every state is still added, and blocks of Gray steps whose
  * lower bound clears the best energy found so far skip their per-step minima. With 0, calls
  * planned from then on take minimum passes that form every step's minimum: the packed 16x2 pass
- * for int32 input with sum |U| < 2^14, the biased fp32-binade pass without bounds otherwise.
+ * for int32 input with sum |U| < 2^14, the biased fp32-binade pass without bounds up to 2^22,
+ * the int32 pass without bounds above.
  * Results are identical either way; the switch exists to test and measure each pass.
  * Process-wide, read when a call is planned (qubo_plan reports it in `pruned`); calls already
  * planned are not affected. The batched calls have no bounded pass and ignore it. */

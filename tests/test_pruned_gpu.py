@@ -1,10 +1,10 @@
 """The block-bounded minimum passes against the oracle where the bound is tightest.
 
-The biased and int32 minimum passes skip the per-step minima of a block of 16 Gray steps when a
-lower bound of every state in it lies above the group's best energy found so far (the states are
-still added, eq. 9). A block holding a state at the minimum (or inside the fp32 band) always has
-its bound at or below the threshold, so it is walked exactly. These cases put minimisers in many
-work units and many blocks at once: the results must still be bit-exact.
+The biased (fp32-binade) and int32 minimum passes skip the per-step minima of a block of 2^6 or
+2^7 Gray steps when a lower bound of every state in it lies above the group's best energy found
+so far (the states are still added, eq. 9). A block holding a state at the minimum (or inside the fp32
+band) always has its bound at or below the threshold, so it is walked exactly. These cases put
+minimisers in many work units and many blocks at once: the results must still be bit-exact.
 """
 import numpy as np
 import pytest
@@ -44,7 +44,8 @@ def test_plans_use_the_bounded_passes(q):
 @pytest.mark.parametrize("lo,hi,seed", [(-1000, 1000, 901), (-(1 << 17), 1 << 17, 902), (-2, 2, 903)])
 def test_minimisers_repeated_in_every_unit(q, lo, hi, seed):
     # 2^7 copies of the 27-variable landscape: one minimiser set per assignment of x_0..x_6, in
-    # many units; biased pass (entries to 1000), int32 pass (2^17) and packed pass (2)
+    # many units; bounded biased pass (entries to 1000, and narrow ones) and bounded int32 pass
+    # (entries to 2^17)
     sub = qi.random_upper_int(27, lo, hi, seed)
     e, x, t = O.solve(sub)
     Q = with_free_prefix(sub, 7)
@@ -104,3 +105,73 @@ def test_slice_range_starting_above_zero(q):
     ties = sum(r[2] for r in recs if r[0] == best)
     first = min(oracle.rank_of_bits(r[1]) for r in recs if r[0] == best)
     assert (e, t, oracle.rank_of_bits(x)) == (best, ties, first) and best > 0
+
+
+@pytest.mark.parametrize("d", [1e-9, 3e-7])
+def test_fp32_near_ties_inside_the_band(q, d):
+    # Three decoupled variables around a 27-variable fp32 landscape: x_0 with diagonal +d (in the
+    # prefix: another work unit), x_15 with diagonal 0 and x_29 with -d (cached: the same unit).
+    # In the fixed-point image the +-d round to 0, so the states x*, x* + e_0 and x* + e_29 tie
+    # inside the band; the fp64 re-evaluation decides: x_0 = 0, x_29 = 1, and x_15 either way
+    # (an exact fp64 tie: twice the landscape's minimisers, the lower rank has x_15 = 0).
+    sub = qi.random_symmetric_normal_f32(27, 909)
+    e, x, t = O.solve(sub)
+    n = 30
+    rest = [i for i in range(n) if i not in (0, 15, 29)]
+    Q = np.zeros((n, n), np.float32)
+    Q[np.ix_(rest, rest)] = sub
+    Q[0, 0], Q[29, 29] = np.float32(d), np.float32(-d)
+    assert q.plan(n, q.FP32)["pruned"] == 1
+    ge, gx, gt = q.solve(Q)
+    tol = 1e-3 * float(np.abs(Q.astype(np.float64)).sum()) * 2.0 ** -20
+    want = np.zeros(n, np.uint8)
+    want[rest] = x
+    want[29] = 1
+    assert (gx == want).all() and gt == 2 * t
+    U = O.fold_f32(Q)
+    assert ge == O.eval64(U, gx) and abs(ge - (e - float(np.float32(d)))) <= tol
+    # the states one flip away in x_0 or x_29 lie inside the fp32 band but above in fp64
+    for v in (0, 29):
+        y = gx.copy()
+        y[v] ^= 1
+        assert O.eval64(U, y) > ge
+
+
+@pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
+def test_int32_bounded_pass_at_the_range_limit(q, sign):
+    # sum |U| = 2^30 - 1, the largest int32 input: running values reach +-S, the bound with the
+    # walked energy and D_par reaches -3S (formed in 64 bits); all-negative entries give
+    # E = -S at x = 1, all-positive ones the zero state alone
+    n = 30
+    lo, hi = {"mixed": (-(1 << 21), 1 << 21), "negative": (-(1 << 21), -1), "positive": (1, 1 << 21)}[sign]
+    total = (1 << 30) - 1
+    Q = np.triu(qi.random_upper_int(n, lo, hi, 910)).astype(np.int64)
+    Q[0, 0] = 0
+    rest = int(np.abs(Q).sum())
+    assert rest < total
+    Q[0, 0] = (total - rest) if sign == "positive" else -(total - rest)
+    Q = Q.astype(np.int32)
+    assert int(np.abs(Q.astype(np.int64)).sum()) == total
+    assert q.plan(n)["pruned"] == 1
+    want = O.solve(Q)
+    e, x, t = q.solve(Q)
+    assert (e, t) == (want[0], want[2]) and (x == want[1]).all()
+    if sign == "negative":
+        assert e == -total and x.all()
+    if sign == "positive":
+        assert e == 0 and t == 1 and not x.any()
+
+
+def test_int32_bounded_pass_ties_in_many_units(q):
+    # wide entries, 2^6 copies of every minimiser (free prefix variables), and slices of it
+    sub = qi.random_upper_int(26, -(1 << 19), 1 << 19, 911)
+    e, x, t = O.solve(sub)
+    Q = with_free_prefix(sub, 6)
+    assert int(np.abs(Q.astype(np.int64)).sum()) >= 1 << 22
+    ge, gx, gt = q.solve(Q)
+    assert (ge, gt) == (e, t << 6) and not gx[:6].any() and (gx[6:] == x).all()
+    ids = np.array([0, 5, 63], dtype=np.uint64)
+    se, sx, st = q.solve_slices(Q, 6, ids)
+    for i, sid in enumerate(ids):
+        assert (int(se[i]), int(st[i])) == (e, t)
+        assert (sx[i][6:] == x).all() and oracle.rank_of_bits(sx[i][:6]) == int(sid)
