@@ -225,6 +225,74 @@ __global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* 
   }
 }
 
+// Whole problems: greedy one-flip descents, one per warp from a hashed start state, over the
+// int32 image; the least energy reached, an energy some state attains, lowers the group's
+// starting best of the bounded minimum pass (gthr), so that the first units already skip most
+// blocks. It decides nothing else: the walk still visits every state, and any attained energy is
+// a valid threshold (it is never below the minimum). Lane l holds the fields of variables l and
+// l + 32, g[v] = U_vv + sum over set u != v of U(u, v) (the energy change when x_v goes from 0 to
+// 1); each step flips the variable of the most negative change (lowest index among equals).
+constexpr int kSeedMaxN = 62;
+constexpr int kSeedBlocks = 32, kSeedThreads = 128;  // 128 descents
+__global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, const DevHeader* __restrict__ hdr,
+                                                                   const int32_t* __restrict__ U, int32_t* gthr) {
+  __shared__ int32_t sU[kSeedMaxN * kSeedMaxN];
+  if (hdr->status != QUBO_OK || n > kSeedMaxN) return;
+  for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
+    const int i = idx / n, j = idx - i * n;
+    sU[idx] = (j >= i) ? U[idx] : U[j * n + i];  // symmetric: sU[i][j] = U[min(i,j)][max(i,j)]
+  }
+  __syncthreads();
+  const int lane = threadIdx.x & 31;
+  // start state: a SplitMix64-style hash of the warp's index
+  uint64_t z = (uint64_t)((blockIdx.x * blockDim.x + threadIdx.x) / 32 + 1) * 0x9E3779B97F4A7C15ull;
+  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
+  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
+  uint64_t x = z ^ (z >> 31);
+  const int v0 = lane, v1 = lane + 32;
+  const bool h0 = v0 < n, h1 = v1 < n;
+  int32_t g0 = h0 ? sU[v0 * n + v0] : 0, g1 = h1 ? sU[v1 * n + v1] : 0;
+  for (int u = 0; u < n; ++u) {
+    if (!((x >> u) & 1u)) continue;
+    if (h0 && u != v0) g0 += sU[u * n + v0];
+    if (h1 && u != v1) g1 += sU[u * n + v1];
+  }
+  // 2 E(x) = sum over set v of (g[v] + U_vv)
+  long long twice = 0;
+  if (h0 && ((x >> v0) & 1u)) twice += (long long)g0 + sU[v0 * n + v0];
+  if (h1 && ((x >> v1) & 1u)) twice += (long long)g1 + sU[v1 * n + v1];
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) twice += __shfl_xor_sync(0xffffffffu, twice, off);
+  int32_t e = (int32_t)(twice / 2);
+  for (int it = 0; it < 4 * n; ++it) {  // each flip lowers E, so this ends long before the cap
+    // key: (change + 2^31) in the high word, the variable in the low word; the least key wins
+    unsigned long long key = ~0ull;
+    if (h0) {
+      const int32_t d = ((x >> v0) & 1u) ? -g0 : g0;
+      key = ((unsigned long long)((long long)d + 0x80000000ll) << 32) | (unsigned)v0;
+    }
+    if (h1) {
+      const int32_t d = ((x >> v1) & 1u) ? -g1 : g1;
+      const unsigned long long k1 = ((unsigned long long)((long long)d + 0x80000000ll) << 32) | (unsigned)v1;
+      key = k1 < key ? k1 : key;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
+      key = o < key ? o : key;
+    }
+    const int32_t best = (int32_t)((long long)(key >> 32) - 0x80000000ll);
+    if (best >= 0) break;  // a local minimum: no single flip lowers E
+    const int bv = (int)(key & 0xffffffffu);
+    const int32_t sg = ((x >> bv) & 1u) ? -1 : 1;
+    x ^= (uint64_t)1 << bv;
+    e += best;
+    if (h0 && v0 != bv) g0 += sg * sU[bv * n + v0];
+    if (h1 && v1 != bv) g1 += sg * sU[bv * n + v1];
+  }
+  if (lane == 0) atomicMin(gthr, e);
+}
+
 // ------------------------------------------------------------------------------------------------
 // A5: per-group minimum over its units (one block per group), and accumulator reset.
 // ------------------------------------------------------------------------------------------------
@@ -356,6 +424,11 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk, seed);
     ++nl;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (seed) {
+      descent_seed_kernel<<<kSeedBlocks, kSeedThreads, 0, stream>>>(p.n, w.hdr, w.U, seed);
+      ++nl;
+      if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
   }
 
   memset(&kp, 0, sizeof(kp));
