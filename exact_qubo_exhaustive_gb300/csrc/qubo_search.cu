@@ -225,19 +225,24 @@ __global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* 
   }
 }
 
-// Whole problems: greedy one-flip descents, one per warp from a hashed start state, over the
-// int32 image; the least energy reached, an energy some state attains, lowers the group's
-// starting best of the bounded minimum pass (gthr), so that the first units already skip most
-// blocks. It decides nothing else: the walk still visits every state, and any attained energy is
-// a valid threshold (it is never below the minimum). Lane l holds the fields of variables l and
-// l + 32, g[v] = U_vv + sum over set u != v of U(u, v) (the energy change when x_v goes from 0 to
-// 1); each step flips the variable of the most negative change (lowest index among equals).
+// Single-group searches (a whole problem or a slice range): greedy one-flip descents, one per warp
+// from a hashed start state, over the int32 image; the least energy reached, an energy some state
+// of the group attains, lowers the group's starting best of the bounded minimum pass (gthr), so
+// that the first units already skip most blocks. It decides nothing else: the walk still visits
+// every state, and any attained energy of the group is a valid threshold (it is never below the
+// group's minimum). With F > 0 the first F variables stay fixed to a unit prefix of the group,
+// gbase[0] + (a hash mod upg), so that the state lies in the group; with F = 0 (a whole problem)
+// every variable may flip. Lane l holds the fields of variables l and l + 32, g[v] = U_vv + sum
+// over set u != v of U(u, v) (the energy change when x_v goes from 0 to 1); each step flips the
+// free variable of the most negative change (lowest index among equals).
 constexpr int kSeedMaxN = 62;
 constexpr int kSeedBlocks = 32, kSeedThreads = 128;  // 128 descents
-__global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, const DevHeader* __restrict__ hdr,
-                                                                   const int32_t* __restrict__ U, int32_t* gthr) {
+__global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, int F, uint64_t upg,
+                                                                   const DevHeader* __restrict__ hdr,
+                                                                   const int32_t* __restrict__ U,
+                                                                   const uint64_t* __restrict__ gbase, int32_t* gthr) {
   __shared__ int32_t sU[kSeedMaxN * kSeedMaxN];
-  if (hdr->status != QUBO_OK || n > kSeedMaxN) return;
+  if (hdr->status != QUBO_OK || n > kSeedMaxN || F >= n) return;
   for (int idx = threadIdx.x; idx < n * n; idx += blockDim.x) {
     const int i = idx / n, j = idx - i * n;
     sU[idx] = (j >= i) ? U[idx] : U[j * n + i];  // symmetric: sU[i][j] = U[min(i,j)][max(i,j)]
@@ -249,8 +254,13 @@ __global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, const
   z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
   z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
   uint64_t x = z ^ (z >> 31);
+  if (F > 0) {  // the prefix: a unit of the group (bit F - 1 - f of P is variable f)
+    const uint64_t P = gbase[0] + (z % upg);
+    for (int f = 0; f < F; ++f) x = (x & ~((uint64_t)1 << f)) | (((P >> (F - 1 - f)) & 1u) << f);
+  }
   const int v0 = lane, v1 = lane + 32;
   const bool h0 = v0 < n, h1 = v1 < n;
+  const bool f0 = h0 && v0 >= F, f1 = h1 && v1 >= F;  // free to flip
   int32_t g0 = h0 ? sU[v0 * n + v0] : 0, g1 = h1 ? sU[v1 * n + v1] : 0;
   for (int u = 0; u < n; ++u) {
     if (!((x >> u) & 1u)) continue;
@@ -267,11 +277,11 @@ __global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, const
   for (int it = 0; it < 4 * n; ++it) {  // each flip lowers E, so this ends long before the cap
     // key: (change + 2^31) in the high word, the variable in the low word; the least key wins
     unsigned long long key = ~0ull;
-    if (h0) {
+    if (f0) {
       const int32_t d = ((x >> v0) & 1u) ? -g0 : g0;
       key = ((unsigned long long)((long long)d + 0x80000000ll) << 32) | (unsigned)v0;
     }
-    if (h1) {
+    if (f1) {
       const int32_t d = ((x >> v1) & 1u) ? -g1 : g1;
       const unsigned long long k1 = ((unsigned long long)((long long)d + 0x80000000ll) << 32) | (unsigned)v1;
       key = k1 < key ? k1 : key;
@@ -419,13 +429,18 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   if (p.prune) {
     const uint32_t nb = 1u << (p.w - p.prune_r);
-    // a whole problem (one group from unit 0) seeds its best with the least walked energy
-    int32_t* seed = (!p.host_gbase && p.gbase0 == 0 && p.ngroups == 1) ? w.gthr : nullptr;
+    // one group that holds unit 0 seeds its best with the least walked energy (the energies of
+    // states of unit 0)
+    const bool from_unit0 = !p.host_gbase && p.gbase0 == 0 && p.ngroups == 1;
+    int32_t* seed = from_unit0 ? w.gthr : nullptr;
     block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk, seed);
     ++nl;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    if (seed) {
-      descent_seed_kernel<<<kSeedBlocks, kSeedThreads, 0, stream>>>(p.n, w.hdr, w.U, seed);
+    if (p.ngroups == 1) {
+      // descents over every variable when the group is all units, else with its prefix fixed
+      const bool all_units = from_unit0 && p.upg == ((uint64_t)1 << p.F);
+      descent_seed_kernel<<<kSeedBlocks, kSeedThreads, 0, stream>>>(p.n, all_units ? 0 : p.F, p.upg, w.hdr, w.U,
+                                                                    w.gbase, w.gthr);
       ++nl;
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }

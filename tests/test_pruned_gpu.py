@@ -175,3 +175,42 @@ def test_int32_bounded_pass_ties_in_many_units(q):
     for i, sid in enumerate(ids):
         assert (int(se[i]), int(st[i])) == (e, t)
         assert (sx[i][6:] == x).all() and oracle.rank_of_bits(sx[i][:6]) == int(sid)
+
+
+@pytest.mark.parametrize("first,count", [(0, 8), (8, 8), (3, 1)])
+def test_slice_ranges_seed_inside_their_range(q, first, count):
+    # x_0 = 1 lowers every energy by 200000, so every state of slices 8..15 (k = 4) lies below
+    # every state of slices 0..7: a starting best taken from outside the range would be below
+    # the range's minimum. Each range's answer must be its own.
+    n, k = 31, 4
+    Q = qi.random_upper_int(n, -500, 500, 912)
+    Q[0, 0] = -200000
+    e, x, t = q.solve_slice_range(Q, k, first, count)
+    recs = [O.solve_slice(Q, k, s) for s in range(first, first + count)]
+    best = min(r[0] for r in recs)
+    ties = sum(r[2] for r in recs if r[0] == best)
+    rank = min(oracle.rank_of_bits(r[1]) for r in recs if r[0] == best)
+    assert (e, t, oracle.rank_of_bits(x)) == (best, ties, rank)
+
+
+@pytest.mark.parametrize("first,count", [(0, 8), (8, 8)])
+def test_device_slice_ranges_seed_inside_their_range(q, first, count):
+    # the device entry of the sharded search (one range per rank): the same instance, a range
+    # from slice 0 that is not the whole problem, and one above it
+    torch = pytest.importorskip("torch")
+    n, k = 31, 4
+    Q = qi.random_upper_int(n, -500, 500, 912)
+    Q[0, 0] = -200000
+    dq = torch.from_numpy(Q).cuda()
+    nb = max(q.slice_range_workspace_bytes(n, q.INT32, k, count), 256)
+    ws = torch.empty(nb, dtype=torch.uint8, device="cuda")
+    res = torch.zeros(32, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream()
+    q.solve_slice_range_device(n, dq, q.INT32, k, first, count, ws, nb, s.cuda_stream, res)
+    torch.cuda.synchronize()
+    r = np.frombuffer(res.cpu().numpy().tobytes(), dtype=q.RESULT_DTYPE)[0]
+    recs = [O.solve_slice(Q, k, s_) for s_ in range(first, first + count)]
+    best = min(rr[0] for rr in recs)
+    ties = sum(rr[2] for rr in recs if rr[0] == best)
+    rank = min(oracle.rank_of_bits(rr[1]) for rr in recs if rr[0] == best)
+    assert (int(r["status"]), float(r["min_energy"]), int(r["tie_count"]), int(r["argmin_rank"])) == (0, best, ties, rank)
