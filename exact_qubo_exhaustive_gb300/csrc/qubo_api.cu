@@ -297,6 +297,7 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
     }
   }
   p.packed = p.packed_ok && !p.prune;
+  p.packed_pruned = p.packed_ok && p.prune;
   *out = p;
   return QUBO_OK;
 }
@@ -368,6 +369,7 @@ int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p) 
 void plan_without_bounds(Plan* p) {
   p->prune = false;
   p->packed = p->packed_ok;
+  p->packed_pruned = false;
 }
 
 int record_launch_count(int launches) {
@@ -690,7 +692,7 @@ int qubo_plan(int n, int dtype, int k_prefix, int cache_bits, qubo_plan_desc* ou
   out->units = p.total_units;
   out->workspace_bytes = layout_workspace(p, nullptr).bytes;
   out->smem_bytes = p.smem_bytes;
-  out->packed = p.packed ? 1 : 0;
+  out->packed = (p.packed || p.packed_pruned) ? 1 : 0;
   out->biased = p.biased ? 1 : 0;
   out->pruned = p.prune ? 1 : 0;
   return QUBO_OK;

@@ -101,7 +101,8 @@ struct Plan {
   int bound_margin = 0;    // extra margin of its bound test: unit minima up to E* + margin stay exact
   bool biased = false;     // biased-binade minimum pass (fast variant, int32, w >= kBiasedR + 1)
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
-  bool packed_ok = false;  //   the packed pass fits this plan (it runs when the bounded pass does not)
+  bool packed_ok = false;  //   the packed pass fits this plan
+  bool packed_pruned = false;  // the packed pass with block bounds runs (packed_ok and prune)
   int packed_threads = 0;  // 2^C / 32
   int packed_blocks = 0;
   size_t packed_smem = 0;

@@ -8,6 +8,7 @@
 namespace qgb {
 namespace {
 using packed::combine;
+using packed::PackedPrunedWalker;
 using packed::PackedWalker;
 
 template <int R>
@@ -74,9 +75,99 @@ __global__ void __launch_bounds__(128, 2) packed_min_kernel(const KParams p) {
   }
 }
 
+// The packed pass with block bounds (PackedPrunedWalker): the same staging and unit loop, the
+// block control table of the bounded passes, and each unit's minimum published to its group.
+template <int R>
+__global__ void __launch_bounds__(128, 2) packed_pruned_kernel(const KParams p) {
+  extern __shared__ __align__(16) int4 s_rows4[];
+  __shared__ int sL[129];  // L, -L at 64 + v and a zero at 128
+  __shared__ int s_red[32];
+  if (p.hdr->status != QUBO_OK) return;
+  if (min_pass_owner(p) != kOwnerPacked) return;
+
+  const int tid = threadIdx.x;
+  const int nthreads = blockDim.x;
+  const int n = p.n, C = p.C, F = p.F, w = p.w;
+  const int ncols = 1 << C;
+  const int nwords = ncols >> 1;
+  const int ndyn = w - R;
+
+  uint32_t* s_words = reinterpret_cast<uint32_t*>(s_rows4);
+  for (int idx = tid; idx < ndyn * nwords; idx += nthreads) {
+    const int rr = idx >> (C - 1), q = idx & (nwords - 1);
+    const int v = n - C - 1 - (R + rr);
+    const int2 m = reinterpret_cast<const int2*>(p.M + (size_t)v * ncols)[q];
+    s_words[idx] = combine(m.x, m.y);
+  }
+
+  WalkCtx c{};
+  c.n = n;
+  c.C = C;
+  c.F = F;
+  c.w = w;
+  c.nthreads = nthreads;
+  c.thread = tid;
+  c.sL = sL;
+  c.rows4 = s_rows4;
+  c.rows1 = nullptr;
+  c.T = reinterpret_cast<const int*>(p.T2);
+  c.t_global = true;
+
+  const int nblocks = 1 << (w - R);
+  const int lane = tid & 31, warp = tid >> 5;
+  const uint64_t nitems = p.unit_end - p.unit_begin;
+  for (uint64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+    const uint64_t u = p.unit_begin + item;
+    const uint64_t g = u / p.upg;
+    const uint64_t P = p.gbase[g] + (u - g * p.upg);
+    __syncthreads();  // previous item is done with sL; staged rows are visible
+    unit_linear_terms(p.U, n, F, P, sL, tid, nthreads);
+    __syncthreads();
+    for (int v = tid; v <= 64; v += nthreads) sL[64 + v] = v < n ? -sL[v] : 0;
+    __syncthreads();
+    int cP = 0;
+    for (int f = 0; f < F; ++f) cP += sL[f];
+    PackedPrunedWalker<R> W;
+    W.init(c, p.Ec, packed::GlobalRows{p.M, 1 << C}, cP);
+    int best = W.walk(c, nblocks, p.blk, p.T2, p.gthr + g, p.hdr->band + p.margin, p.one);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+    if (lane == 0) s_red[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+      int b = s_red[0];
+      for (int k = 1; k < (nthreads >> 5); ++k) b = min(b, s_red[k]);
+      p.unit_min[u] = b;
+      atomicMin(p.gthr + g, b);
+    }
+  }
+}
+
+template <int R>
+cudaError_t launch_pruned(const KParams& p, uint64_t nunits, cudaStream_t s) {
+  auto k = packed_pruned_kernel<R>;
+  const size_t smem = (size_t)(p.w - R) << (p.C + 1);
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int occ = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, PackedPrunedWalker<R>::kThreads, smem)) != cudaSuccess)
+    return e;
+  const uint64_t full = (uint64_t)device_info().sms * (uint64_t)(occ > 0 ? occ : 1);
+  const int blocks = (int)(nunits < full ? nunits : full);
+  k<<<blocks, PackedPrunedWalker<R>::kThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t packed_smem_bytes(int C, int w) { return (size_t)(w - kPackedR) << (C + 1); }
+
+cudaError_t launch_search_packed_pruned(int R, const KParams& p, uint64_t nunits, cudaStream_t s) {
+  if (p.C != 12) return cudaErrorInvalidConfiguration;  // 128 threads x 32 columns
+  if (R == kPruneRLong) return launch_pruned<kPruneRLong>(p, nunits, s);
+  if (R == kPruneRShort) return launch_pruned<kPruneRShort>(p, nunits, s);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s) {
   auto k = packed_min_kernel<kPackedR>;

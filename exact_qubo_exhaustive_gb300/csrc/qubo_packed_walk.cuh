@@ -380,5 +380,186 @@ struct PackedWalker {
   }
 };
 
+// ------------------------------------------------------------------------------------------------
+// Packed minimum walk with block bounds (128 threads x 32 columns, two per 32-bit word).
+//
+// The block bound, the threshold and the exactness argument are those of PrunedMinWalker
+// (qubo_walk.cuh), taken over the 32 columns (both halves of every word). What changes is how
+// every state still gets its add: one word instruction adds a row to two columns, in forms no
+// compiler can fold because they depend on values it cannot see: a flip that adds the row is an
+// unsigned fused add-min against a UINT_MAX read from a kernel parameter (ALU pipe); a flip that
+// subtracts it, or whose sign is known only at run time, is a multiply-add by -1 from the same
+// parameter or by the sign (the FMA pipe's integer unit). Word arithmetic modulo 2^32 is exact
+// per half (the representation above), so each instruction advances two states exactly.
+// ------------------------------------------------------------------------------------------------
+template <int R>
+struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
+  using B = PackedWalker<R, kModeMin, GlobalRows>;
+  using RowBuf = typename B::RowBuf;
+  static constexpr int kThreads = 128;    // 2^12 columns: the word-quad stride is a constant
+  static constexpr int kBlock = 1 << R;   // steps per block
+  static constexpr int kRefreshMask = 3;  // blocks between two publications of the warp's best
+  static constexpr int kReadMask = 7;     // blocks between two reads of the group's best
+  static_assert(R >= 3, "whole quads of walked energies per block");
+
+  int dmin0, dmin1;  // D_par of even and odd blocks (least change of one column over a block)
+  int g_best;        // G: the group's best energy known to this warp
+  int best;          // this thread's best energy minus s
+  uint32_t big;      // UINT_MAX, the add-min's bound (from a kernel parameter)
+  uint32_t mone;     // -1 modulo 2^32 (from a kernel parameter)
+
+  __device__ __forceinline__ void words_add(const uint32_t* row) {
+#pragma unroll
+    for (int jj = 0; jj < kPW; ++jj) this->V[jj] = __viaddmin_u32(this->V[jj], row[jj], big);
+  }
+  __device__ __forceinline__ void words_sgn(const uint32_t* row, uint32_t sg) {
+#pragma unroll
+    for (int jj = 0; jj < kPW; ++jj) asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(this->V[jj]) : "r"(row[jj]), "r"(sg));
+  }
+
+  // Flips of steps 0..kBlock-2 of a block; position R-1 flips once, with sign sgn (+1 in even
+  // blocks, -1 in odd ones); the others with the sign their Gray bit fixes.
+  template <int D>
+  __device__ __forceinline__ void body(uint32_t sgn) {
+    if constexpr (D + 1 < kBlock) {
+      constexpr int a = ctz_c(D + 1);
+      if constexpr (a == R - 1) {
+        words_sgn(this->Row[a], sgn);
+      } else {
+        constexpr int bit = ((D >> a) ^ (D >> (a + 1))) & 1;  // bit a of gray(D): 1 -> the flip clears it
+        if (bit) words_sgn(this->Row[a], mone);
+        else words_add(this->Row[a]);
+      }
+      body<D + 1>(sgn);
+    }
+  }
+
+  // The two signed values of a row word combine(lo, hi) = hi * 2^16 + lo.
+  static __device__ __forceinline__ void split(uint32_t w, int& lo, int& hi) {
+    lo = (int)(int16_t)(w & 0xffffu);
+    hi = ((int)w - lo) >> 16;
+  }
+
+  __device__ __forceinline__ void init_bounds() {
+    int lo0 = 0, lo1 = 0;
+#pragma unroll
+    for (int jj = 0; jj < kPW; ++jj) {
+      int neg_l = 0, neg_h = 0;  // sums of the negative parts of rows 0..R-2, per half
+#pragma unroll
+      for (int a = 0; a < R - 1; ++a) {
+        int l, h;
+        split(this->Row[a][jj], l, h);
+        neg_l += min(l, 0);
+        neg_h += min(h, 0);
+      }
+      int rl, rh;
+      split(this->Row[R - 1][jj], rl, rh);
+      lo0 = min(lo0, min(neg_l + min(rl, 0), neg_h + min(rh, 0)));
+      lo1 = min(lo1, min(neg_l + min(-rl, 0), neg_h + min(-rh, 0)));
+    }
+    dmin0 = lo0;
+    dmin1 = lo1;
+  }
+
+  // Least column value of the two halves of a 16x2 minimum word.
+  static __device__ __forceinline__ int lesser_half(uint32_t m) {
+    return min((int)(m & 0xffffu), (int)(m >> 16)) - (int)kHalfBias;
+  }
+
+  // The block walked with every per-step minimum (rare: the bound did not clear it), in groups of
+  // four steps as in PrunedMinWalker::exact_block, with the packed per-half add-min of the walked
+  // energy (T2: T modulo 2^16 in both halves).
+  __device__ __forceinline__ void exact_block(const uint32_t* __restrict__ T2, int m, uint32_t pm0, uint32_t sgn) {
+    const uint4* T4 = reinterpret_cast<const uint4*>(T2) + (static_cast<uint32_t>(m) << (R - 2));
+    const uint32_t one = 0u - mone;
+    uint4 tq = __ldg(T4);
+    uint32_t pa = __viaddmin_u16x2(pm0, tq.x, 0xffffffffu);
+#pragma unroll 1
+    for (int k = 0; k < kBlock / 4; ++k) {
+      words_add(this->Row[0]);
+      pa = __viaddmin_u16x2(pmin_all<kPW>(this->V), tq.y, pa);
+      words_sgn(this->Row[1], (k & 1) ? mone : one);
+      pa = __viaddmin_u16x2(pmin_all<kPW>(this->V), tq.z, pa);
+      words_sgn(this->Row[0], mone);
+      pa = __viaddmin_u16x2(pmin_all<kPW>(this->V), tq.w, pa);
+      if (k + 1 == kBlock / 4) break;  // the block's last state
+      const int a = 2 + __ffs(k + 1) - 1;
+      const int d = 4 * k + 3;
+      const uint32_t sg = (a == R - 1) ? sgn : ((((d >> a) ^ (d >> (a + 1))) & 1) ? mone : one);
+      flip_row_rt(a, sg);
+      tq = __ldg(T4 + k + 1);
+      pa = __viaddmin_u16x2(pmin_all<kPW>(this->V), tq.x, pa);
+    }
+    best = min(best, lesser_half(pa));
+  }
+
+  template <int A = 2>
+  __device__ __forceinline__ void flip_row_rt(int a, uint32_t sg) {
+    if constexpr (A < R) {
+      if (a == A) words_sgn(this->Row[A], sg);
+      else flip_row_rt<A + 1>(a, sg);
+    }
+  }
+
+  __device__ __forceinline__ void exchange_best(int* gbest, bool read) {
+    const int v = __reduce_min_sync(0xffffffffu, best + this->s);
+    if (v < g_best) {
+      if ((threadIdx.x & 31) == 0) atomicMin(gbest, v);
+      g_best = v;
+    }
+    if (read) g_best = min(g_best, __ldcg(gbest));
+  }
+
+  // Whole unit: nblocks (even) blocks of 2^R steps, each but the last followed by a shared-row
+  // flip, as PrunedMinWalker::walk (blk: the same control table; its row offsets count the 16-
+  // column layout's quads, twice this layout's word quads). Returns this thread's best energy.
+  __device__ __forceinline__ int walk(const WalkCtx& c, int nblocks, const BlockCtl* __restrict__ blk,
+                                      const uint32_t* __restrict__ T2, int* gbest, int band, int one) {
+    big = 0xffffffffu - (uint32_t)(one - 1);
+    mone = 0u - (uint32_t)one;
+    init_bounds();
+    const int dmb0 = dmin0 - band, dmb1 = dmin1 - band;
+    g_best = __ldcg(gbest);
+    // a real best from the first state's columns
+    best = lesser_half(__viaddmin_u16x2(pmin_all<kPW>(this->V), __ldg(T2), 0xffffffffu));
+    const int4* ctl4 = reinterpret_cast<const int4*>(blk);
+    const uint4* rows = reinterpret_cast<const uint4*>(c.rows4) + c.thread;
+    int4 ctl = __ldg(ctl4);
+    for (int m = 0; m < nblocks; ++m) {
+      const int4 next = __ldg(ctl4 + m + 1);  // one block ahead (the table has a padding entry)
+      RowBuf rb;
+      {
+        const uint4* rp = rows + (ctl.y >> 1);  // in flight while the block is walked
+#pragma unroll
+        for (int k = 0; k < kPW / 4; ++k) rb.q[k] = rp[k * kThreads];
+      }
+      const bool odd = m & 1;
+      const int thr = min(best, g_best - this->s);
+      const uint32_t pm0 = pmin_all<kPW>(this->V);
+      const uint32_t sgn = odd ? mone : 0u - mone;
+      if (__all_sync(0xffffffffu, lesser_half(pm0) + ctl.x + (odd ? dmb1 : dmb0) > thr)) {
+        body<0>(sgn);
+      } else {
+        exact_block(T2, m, pm0, sgn);
+      }
+      // the flip that follows (a no-op after the last block: sign 0, linear term 0)
+      const uint32_t dsg = (uint32_t)static_cast<int>(__int_as_float(ctl.z));
+#pragma unroll
+      for (int k = 0; k < kPW / 4; ++k) {
+        asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(this->V[4 * k + 0]) : "r"(rb.q[k].x), "r"(dsg));
+        asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(this->V[4 * k + 1]) : "r"(rb.q[k].y), "r"(dsg));
+        asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(this->V[4 * k + 2]) : "r"(rb.q[k].z), "r"(dsg));
+        asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(this->V[4 * k + 3]) : "r"(rb.q[k].w), "r"(dsg));
+      }
+      const int dl = c.sL[ctl.w];
+      this->s += dl;
+      best -= dl;
+      ctl = next;
+      if ((m & kRefreshMask) == kRefreshMask) exchange_best(gbest, (m & kReadMask) == kReadMask);
+    }
+    return best + this->s;
+  }
+};
+
 }  // namespace packed
 }  // namespace qgb

@@ -383,7 +383,7 @@ Work layout_workspace(const Plan& p, unsigned char* base) {
   w.M = reinterpret_cast<int32_t*>(take((size_t)(p.n - p.C > 0 ? p.n - p.C : 1) * ncols * 4));
   w.Ec = reinterpret_cast<int32_t*>(take(ncols * 4 < 16 ? 16 : ncols * 4));
   w.T = reinterpret_cast<int32_t*>(take(nT * 4));
-  if (p.packed) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
+  if (p.packed || p.packed_pruned) w.T2 = reinterpret_cast<uint32_t*>(take(nT * 4));
   if (p.prune) {
     w.blk = reinterpret_cast<BlockCtl*>(take(((nT >> p.prune_r) + 1) * sizeof(BlockCtl)));
     w.gthr = reinterpret_cast<int32_t*>(take((size_t)p.ngroups * 4));
@@ -453,7 +453,7 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
   kp.w = p.w;
   kp.dtype = p.dtype;
   kp.biased_active = p.biased ? 1 : 0;
-  kp.packed_active = p.packed ? 1 : 0;
+  kp.packed_active = (p.packed || p.packed_pruned) ? 1 : 0;
   kp.seg_bits = p.seg_bits;
   kp.ngroups = p.ngroups;
   kp.upg = p.upg;
@@ -495,7 +495,12 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     kp.unit_end = (u0 + chunk < p.total_units) ? u0 + chunk : p.total_units;
     const uint64_t nunits = kp.unit_end - kp.unit_begin;
     const int blocks = (int)(nunits < (uint64_t)p.blocks ? nunits : (uint64_t)p.blocks);
-    if (p.packed) {
+    if (p.packed_pruned) {
+      // packed 16x2 CUDA-core pass with block bounds (exits at once unless it owns the minimum
+      // pass) ...
+      if ((e = launch_search_packed_pruned(p.prune_r, kp, nunits, stream)) != cudaSuccess) return e;
+      ++nl;
+    } else if (p.packed) {
       // packed 16x2 CUDA-core pass (exits at once unless it owns the minimum pass) ...
       const int pb = (int)(nunits < (uint64_t)p.packed_blocks ? nunits : (uint64_t)p.packed_blocks);
       if ((e = launch_search_packed(kp, pb, p.packed_threads, p.packed_smem, stream)) != cudaSuccess) return e;

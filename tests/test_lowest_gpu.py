@@ -90,19 +90,21 @@ def _full_rank(bits_by_pos, n):
     return (bits_by_pos.astype(np.uint64) * w).sum(axis=1)
 
 
-@pytest.mark.parametrize("n,n0,k,seed,scale", [(30, 18, 1000, 1, 1), (31, 19, 4000, 2, 1), (32, 20, 300, 3, 1),
-                                                (30, 18, 1000, 4, 1024)])
-def test_lowest_bounded_separable_instances(q, n, n0, k, seed, scale):
+@pytest.mark.parametrize("n,n0,k,seed,scale,rng_core,rng_d", [
+    (30, 18, 1000, 1, 1, 1000, 400), (31, 19, 4000, 2, 1, 1000, 400), (32, 20, 300, 3, 1, 1000, 400),
+    (30, 18, 1000, 4, 1024, 1000, 400), (30, 18, 500, 5, 1, 9, 5)])
+def test_lowest_bounded_separable_instances(q, n, n0, k, seed, scale, rng_core, rng_d):
     # n0 coupled variables at random positions and n - n0 variables with a diagonal term only:
     # E(x) = E_core(x_core) + sum_i d_i x_i. If c lies beyond the core's k lowest (ties at the
     # k-th energy included), k core states c' have E(c') < E(c), and every (c', y) lies strictly
     # below (c, y); so the k lowest keys combine the core's k lowest (the oracle's) with all
-    # 2^(n - n0) diagonal parts. scale 1024 puts sum |U| above 2^22: the int32 bounded pass
+    # 2^(n - n0) diagonal parts. scale 1024 puts sum |U| above 2^22 (the int32 bounded pass);
+    # entries to 9 keep it below 2^14 (the packed bounded pass)
     rng = qi.Stream(3100 + seed)
     pos = np.sort(np.argsort(rng.raw(n))[:n0])
     free = np.array([i for i in range(n) if i not in set(pos.tolist())])
-    core = qi.random_upper_int(n0, -1000, 1000, 3110 + seed) * np.int32(scale)
-    d = rng.integers(-400, 400, n - n0) * scale
+    core = qi.random_upper_int(n0, -rng_core, rng_core, 3110 + seed) * np.int32(scale)
+    d = rng.integers(-rng_d, rng_d, n - n0) * scale
     Q = np.zeros((n, n), np.int32)
     Q[np.ix_(pos, pos)] = core
     Q[free, free] = d

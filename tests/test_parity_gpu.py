@@ -93,11 +93,10 @@ def test_infeasible_explicit_plan_is_an_error(q):
 def test_plans_pick_fast_kernel_for_large_n(q):
     p = q.plan(40)
     assert p["variant"] == 1 and p["cache_bits"] == 12 and p["units"] >= 1024
-    # the bounded biased pass; the packed pass runs only without bounds
-    assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 0
+    # the bounded passes; the packed one is planned too (it checks sum |U| < 2^14 on the device
+    # and exits at once otherwise, leaving the biased or int32 pass to run)
+    assert p["pruned"] == 1 and p["biased"] == 1 and p["packed"] == 1
     with no_bounds(q):
-        # the packed pass is planned (it checks sum |U| < 2^14 on the device and exits at once
-        # otherwise, leaving the biased pass to run)
         p = q.plan(40)
         assert p["pruned"] == 0 and p["biased"] == 1 and p["packed"] == 1
         assert q.plan(40, q.FP32)["pruned"] == 0
@@ -174,15 +173,15 @@ def test_fewer_threads_than_variables(q):
 
 
 # ---------------------------------------------------------------- packed 16x2 minimum pass
-# Narrow inputs (sum |U| < 2^14) take the bounded biased pass by default and the packed pass
-# without block bounds: both are checked, and the k-lowest driver on the same inputs.
+# Narrow inputs (sum |U| < 2^14) take the packed pass, with block bounds by default and without
+# them through the switch: both are checked, and the k-lowest driver on the same inputs.
 
 @pytest.mark.parametrize("n,lo,hi,seed", [(30, -30, 30, 1), (30, -9, 9, 3), (31, -3, 3, 4), (31, 0, 2, 5)])
 def test_packed_pass_small_range(q, n, lo, hi, seed):
     Q = qi.random_upper_int(n, lo, hi, 2400 + seed)
     assert int(np.abs(Q.astype(np.int64)).sum()) <= (1 << 14) - 1
-    assert q.plan(n)["packed"] == 0 and q.plan(n)["pruned"] == 1
-    e, x, t = check_int(q, Q)
+    assert q.plan(n)["packed"] == 1 and q.plan(n)["pruned"] == 1
+    e, x, t = check_int(q, Q)  # the bounded packed pass
     with no_bounds(q):
         assert q.plan(n)["packed"] == 1 and q.plan(n)["pruned"] == 0
         check_int(q, Q)  # the packed pass: every unit minimum feeds the tie and argmin passes
@@ -192,8 +191,8 @@ def test_packed_pass_small_range(q, n, lo, hi, seed):
 
 @pytest.mark.parametrize("sign", ["mixed", "negative", "positive"])
 def test_packed_range_limit_is_exact(q, sign):
-    # without bounds sum |U| = 2^14 - 1 runs the packed pass (values pushed to +-sum |U|), 2^14
-    # the biased one; with bounds both run the bounded biased pass
+    # sum |U| = 2^14 - 1 runs the packed pass (values pushed to +-sum |U|), 2^14 the biased
+    # one; with and without block bounds
     n = 30
     lo, hi = {"mixed": (-50, 50), "negative": (-50, -1), "positive": (1, 50)}[sign]
     for total in ((1 << 14) - 1, 1 << 14):
@@ -216,8 +215,8 @@ def test_packed_range_limit_is_exact(q, sign):
 
 
 def test_packed_pass_all_ties(q):
-    # Q = 0: every state ties; every block's bound equals the threshold, so the bounded pass walks
-    # every block exactly, and the resolve pass counts 2^n; so does the packed pass
+    # Q = 0: every state ties; every block's bound equals the threshold, so the bounded packed
+    # pass walks every block exactly, and the resolve pass counts 2^n; so does the unbounded one
     Z = np.zeros((30, 30), np.int32)
     e, x, t = q.solve(Z)
     assert (e, t) == (0, 1 << 30) and not x.any()

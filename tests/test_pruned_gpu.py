@@ -44,8 +44,8 @@ def test_plans_use_the_bounded_passes(q):
 @pytest.mark.parametrize("lo,hi,seed", [(-1000, 1000, 901), (-(1 << 17), 1 << 17, 902), (-2, 2, 903)])
 def test_minimisers_repeated_in_every_unit(q, lo, hi, seed):
     # 2^7 copies of the 27-variable landscape: one minimiser set per assignment of x_0..x_6, in
-    # many units; bounded biased pass (entries to 1000, and narrow ones) and bounded int32 pass
-    # (entries to 2^17)
+    # many units; bounded biased pass (entries to 1000), packed pass (narrow ones) and int32 pass
+    # (entries to 2^17), all with block bounds
     sub = qi.random_upper_int(27, lo, hi, seed)
     e, x, t = O.solve(sub)
     Q = with_free_prefix(sub, 7)
