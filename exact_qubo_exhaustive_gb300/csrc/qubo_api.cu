@@ -366,6 +366,8 @@ int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p) 
   return QUBO_OK;
 }
 
+bool block_bounds_enabled() { return g_block_bounds.load() != 0; }
+
 void plan_without_bounds(Plan* p) {
   p->prune = false;
   p->packed = p->packed_ok;

@@ -9,6 +9,7 @@
 #include <type_traits>
 
 #include "qubo_packed_walk.cuh"
+#include "qubo_seed.cuh"
 #include "qubo_walk.cuh"
 
 namespace qgb {
@@ -234,6 +235,9 @@ static_assert(kPackedTiesR <= kPackedR, "a minimum-pass iteration is a whole num
 constexpr int kBatchMaxWalked = 11;     // walked bits per unit (plan_batched)
 constexpr int kBatchMaxIters = 1 << (kBatchMaxWalked - kPackedR - 1);  // packed iterations per unit
 constexpr int kBatchTabC = 12;
+// The bounded packed pass walks blocks of 2^kBatchPruneR steps: one iteration of the packed
+// minimum pass (kPackedR register rows), so its block minima index the same re-walk table.
+constexpr int kBatchPruneR = kPackedR + 1;
 static_assert(kBatchTabC == 12, "packed::HalfRows splits the cached bits 6 + 6");
 
 struct BatchTables {
@@ -252,6 +256,9 @@ struct BatchTables {
   int32_t* gmin;
   unsigned long long* grank;
   unsigned long long* gties;
+  BlockCtl* blk;      // batch x (2^(w - kBatchPruneR) + 1): block control tables (bounded packed pass)
+  int32_t* gthr;      // batch: best energy published so far (bounded packed pass)
+  int one;            // 1: the bounded walk derives its opaque constants from it
   size_t su, sm, sh, se, st;  // per-instance strides of U, M, H, Ec, T / T2
 };
 
@@ -638,6 +645,140 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
   }
 }
 
+// Block bounds of the batched packed pass, per instance (one block of 128 threads each): the
+// control table of its blocks of 2^R steps (as the single-problem block_table_kernel), and its
+// starting best: sum |U|, lowered to the least walked energy (energies of states of unit 0) and
+// to the least energy of four greedy descents (warp_descent; one per warp).
+template <int R>
+__global__ void __launch_bounds__(128) bseed_kernel(BatchTables b) {
+  __shared__ int32_t sU[kBatchTabMaxN * kBatchTabMaxN];
+  __shared__ int s_min;
+  const int g = blockIdx.x, tid = threadIdx.x;
+  if (b.status[g] != QUBO_OK || batch_class(b.S[g]) != kBatchPacked) return;
+  const int n = b.n, C = b.C, w = b.w;
+  const uint32_t nb = 1u << (w - R);
+  const int32_t* T = b.T + (size_t)g * b.st;
+  BlockCtl* blk = b.blk + (size_t)g * (nb + 1);
+  const int32_t* U = b.U + (size_t)g * b.su;
+  if (tid == 0) s_min = (int)b.S[g];  // no energy exceeds sum |U| (< 2^14 here)
+  for (int idx = tid; idx < n * n; idx += blockDim.x) {
+    const int i = idx / n, j = idx - i * n;
+    sU[idx] = (j >= i) ? U[idx] : U[j * n + i];
+  }
+  __syncthreads();
+  for (uint32_t m = tid; m <= nb; m += blockDim.x) {
+    const uint32_t mm = m < nb ? m : nb - 1;
+    const int4* T4 = reinterpret_cast<const int4*>(T + ((size_t)mm << R));
+    int tmin = kIntInf;
+    for (int q = 0; q < (1 << R) / 4; ++q) {
+      const int4 t = T4[q];
+      tmin = min(tmin, __vimin3_s32(t.x, t.y, min(t.z, t.w)));
+    }
+    if (m < nb) atomicMin(&s_min, tmin);
+    BlockCtl bc;
+    bc.tmin = tmin;
+    if (m + 1 < nb) {
+      const int rr = __ffs((int)(m + 1)) - 1;
+      const bool up = !(((m + 1) >> (rr + 1)) & 1u);
+      bc.row = rr << (C - 2);
+      bc.dsgn = up ? 1.f : -1.f;
+      bc.lvx = (up ? 0 : 64) + (n - C - 1 - (R + rr));
+    } else {
+      bc.row = 0;
+      bc.dsgn = 0.f;
+      bc.lvx = 128;
+    }
+    blk[m] = bc;
+  }
+  const int32_t e = warp_descent(sU, n, 0, 0, 1, (uint64_t)g * 4 + (tid >> 5));
+  if ((tid & 31) == 0) atomicMin(&s_min, e);
+  __syncthreads();
+  if (tid == 0) b.gthr[g] = s_min;
+}
+
+// The packed minimum pass with block bounds (PackedPrunedWalker) over the units of the instances
+// with sum |U| <= kPackedMaxAbsSum: the unit loop and staging of bpacked_kernel, each unit's
+// minimum published to its instance's best, and the minima of the exactly walked blocks recorded
+// for the re-walk (a block no warp walked exactly holds no state at the instance minimum).
+template <int R>
+__global__ void __launch_bounds__(128, 2) bpacked_pruned_kernel(BatchTables b) {
+  static_assert(R == kPackedR + 1, "a block is one iteration of the packed minimum pass");
+  extern __shared__ __align__(16) int4 s_rows4[];
+  __shared__ int sL[129];  // L, -L at 64 + v and a zero at 128
+  __shared__ int s_red[32];
+  __shared__ __align__(16) int sH[(kBatchTabMaxN - kBatchTabC) * packed::HalfRows::kStride];
+  __shared__ int s_seg[kBatchMaxIters];  // per-block minima of the current unit
+  __shared__ uint4 s_dw[4 * 128];        // per-column changes (block bound)
+  const int tid = threadIdx.x, nthreads = blockDim.x;
+  const int n = b.n, C = b.C, F = b.F, w = b.w;
+  const int ndyn = w - R;
+  const int nblocks = 1 << (w - R);  // = the packed pass's iterations per unit
+  const uint64_t units = (uint64_t)b.batch << F;
+  const int lane = tid & 31, warp = tid >> 5;
+  uint32_t* s_words = reinterpret_cast<uint32_t*>(s_rows4);
+  int staged = -1;
+  WalkCtx c{};
+  c.n = n;
+  c.C = C;
+  c.F = F;
+  c.w = w;
+  c.nthreads = nthreads;
+  c.thread = tid;
+  c.sL = sL;
+  c.rows4 = s_rows4;
+  c.rows1 = nullptr;
+  c.t_global = true;
+  const uint64_t u_begin = units * blockIdx.x / gridDim.x, u_end = units * (blockIdx.x + 1) / gridDim.x;
+  for (uint64_t u = u_begin, next; u < u_end; u = next) {
+    const int g = (int)(u >> F);
+    const uint64_t P = u & (((uint64_t)1 << F) - 1);
+    next = u + 1;
+    if (b.status[g] != QUBO_OK || batch_class(b.S[g]) != kBatchPacked) {  // not this pass's: skip it whole
+      next = (uint64_t)(g + 1) << F;
+      continue;
+    }
+    __syncthreads();
+    const packed::HalfRows rows{sH};
+    if (g != staged) {
+      const int nh = (n - C) * packed::HalfRows::kStride;
+      const int4* H4 = reinterpret_cast<const int4*>(b.H + (size_t)g * b.sh);
+      for (int idx = tid; idx < (nh >> 2); idx += nthreads) reinterpret_cast<int4*>(sH)[idx] = H4[idx];
+      __syncthreads();
+      const int lq = C - 2;  // log2 of the int4 quads per row (two words each)
+      for (int idx = tid; idx < (ndyn << lq); idx += nthreads) {
+        const int rr = idx >> lq, q = idx & ((1 << lq) - 1);
+        const int4 m = rows.quad(n - C - 1 - (R + rr), q);
+        reinterpret_cast<uint2*>(s_words)[idx] = make_uint2(packed::combine(m.x, m.y), packed::combine(m.z, m.w));
+      }
+      staged = g;
+    }
+    bunit_terms(b.U + (size_t)g * b.su, n, F, P, sL);
+    if (tid < nblocks) s_seg[tid] = kIntInf;
+    __syncthreads();
+    for (int v = tid; v <= 64; v += nthreads) sL[64 + v] = v < n ? -sL[v] : 0;
+    __syncthreads();
+    int cP = 0;
+    for (int f = 0; f < F; ++f) cP += sL[f];
+    const uint32_t* T2 = b.T2 + (size_t)g * b.st;
+    c.T = reinterpret_cast<const int*>(T2);
+    packed::PackedPrunedWalker<R, packed::HalfRows> W;
+    W.init(c, b.Ec + (size_t)g * b.se, rows, cP);
+    int best = W.walk(c, nblocks, b.blk + (size_t)g * (nblocks + 1), T2, b.gthr + g, 0, b.one, s_seg, s_dw);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
+    if (lane == 0) s_red[warp] = best;
+    __syncthreads();
+    if (tid == 0) {
+      int m = s_red[0];
+      for (int k = 1; k < (nthreads >> 5); ++k) m = min(m, s_red[k]);
+      b.unit_min[u] = m;
+      atomicMin(b.gthr + g, m);
+    }
+    int32_t* seg_min = b.seg_min + (size_t)u * walk_iterations<kPackedR>(w);
+    if (tid < nblocks) seg_min[tid] = s_seg[tid];
+  }
+}
+
 // Instance minima over their units.
 __global__ void bgroup_kernel(BatchTables b) {
   const int g = blockIdx.x * blockDim.x + threadIdx.x;
@@ -695,6 +836,10 @@ BatchTables batch_tables(const BatchPlan& bp, unsigned char* base, size_t* bytes
   t.gmin = reinterpret_cast<int32_t*>(take(B * 4));
   t.grank = reinterpret_cast<unsigned long long*>(take(B * 8));
   t.gties = reinterpret_cast<unsigned long long*>(take(B * 8));
+  const size_t nblk = bp.w > kBatchPruneR ? ((size_t)1 << (bp.w - kBatchPruneR)) + 1 : 1;
+  t.blk = reinterpret_cast<BlockCtl*>(take(B * nblk * sizeof(BlockCtl)));
+  t.gthr = reinterpret_cast<int32_t*>(take(B * 4));
+  t.one = 1;
   if (bytes) *bytes = off;
   return t;
 }
@@ -737,6 +882,17 @@ bool plan_batched(int batch, int n, BatchPlan* bp) {
         occ < 1)
       occ = 1;
     p.packed_blocks = std::max(1, di.sms) * occ;
+    // the packed pass with block bounds: at least two blocks of 2^kBatchPruneR steps per unit
+    p.pruned = block_bounds_enabled() && p.w >= kBatchPruneR + 1;
+    if (p.pruned) {
+      p.smem_pruned = (size_t)(p.w - kBatchPruneR) << (p.C + 1);
+      auto kp = bpacked_pruned_kernel<kBatchPruneR>;
+      if (set_smem(kp, p.smem_pruned) != cudaSuccess ||
+          cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kp, (1 << p.C) / 32, p.smem_pruned) != cudaSuccess ||
+          occ < 1)
+        occ = 1;
+      p.pruned_blocks = std::max(1, di.sms) * occ;
+    }
     *bp = p;
     return true;
   }
@@ -782,8 +938,18 @@ cudaError_t run_batched(const BatchPlan& bp, const void* d_Q, void* d_ws, qubo_r
   btables_kernel<<<bp.batch, 256, 0, stream>>>(t);
   ++nl;
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  if ((e = set_smem(bpacked_kernel<kPackedR, kModeMin>, bp.smem_packed)) != cudaSuccess) return e;
-  bpacked_kernel<kPackedR, kModeMin><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
+  if (bp.pruned) {
+    // packed instances: block tables and starting bests, then the bounded packed pass
+    bseed_kernel<kBatchPruneR><<<bp.batch, 128, 0, stream>>>(t);
+    ++nl;
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    auto kp = bpacked_pruned_kernel<kBatchPruneR>;
+    if ((e = set_smem(kp, bp.smem_pruned)) != cudaSuccess) return e;
+    kp<<<bp.pruned_blocks, (1 << bp.C) / 32, bp.smem_pruned, stream>>>(t);
+  } else {
+    if ((e = set_smem(bpacked_kernel<kPackedR, kModeMin>, bp.smem_packed)) != cudaSuccess) return e;
+    bpacked_kernel<kPackedR, kModeMin><<<bp.packed_blocks, (1 << bp.C) / 32, bp.smem_packed, stream>>>(t);
+  }
   ++nl;
   auto kb = bwalk_kernel<kBiasedR, float, kModeMin>;
   if ((e = set_smem(kb, bp.smem_biased)) != cudaSuccess) return e;

@@ -155,6 +155,9 @@ struct BatchPlan {
   int blocks = 0;          // persistent grid of the 256-thread passes
   int packed_blocks = 0;   // persistent grid of the 128-thread packed pass
   size_t smem_int = 0, smem_biased = 0, smem_packed = 0;
+  bool pruned = false;     // packed instances take the packed pass with block bounds
+  int pruned_blocks = 0;   // its persistent grid
+  size_t smem_pruned = 0;
 };
 bool plan_batched(int batch, int n, BatchPlan* bp);
 size_t batched_workspace_bytes(const BatchPlan& bp);
@@ -166,6 +169,7 @@ bool valid_dtype(int dtype);
 size_t dtype_bytes(int dtype);
 int plan_whole_problem(int n, int dtype, int k_prefix, int cache_bits, Plan* p);
 void plan_without_bounds(Plan* p);  // minimum passes that report every unit's exact minimum
+bool block_bounds_enabled();        // qubo_enable_block_bounds (default on)
 int record_launch_count(int launches);
 int record_cuda_error(cudaError_t e, const char* where);  // returns QUBO_ERR_CUDA
 std::mutex& api_mutex();      // serialises the host entry points

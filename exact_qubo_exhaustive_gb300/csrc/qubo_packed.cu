@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(128, 2) packed_pruned_kernel(const KParams p) 
   extern __shared__ __align__(16) int4 s_rows4[];
   __shared__ int sL[129];  // L, -L at 64 + v and a zero at 128
   __shared__ int s_red[32];
+  __shared__ uint4 s_dw[4 * PackedPrunedWalker<R>::kThreads];  // per-column changes (block bound)
   if (p.hdr->status != QUBO_OK) return;
   if (min_pass_owner(p) != kOwnerPacked) return;
 
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(128, 2) packed_pruned_kernel(const KParams p) 
     for (int f = 0; f < F; ++f) cP += sL[f];
     PackedPrunedWalker<R> W;
     W.init(c, p.Ec, packed::GlobalRows{p.M, 1 << C}, cP);
-    int best = W.walk(c, nblocks, p.blk, p.T2, p.gthr + g, p.hdr->band + p.margin, p.one);
+    int best = W.walk(c, nblocks, p.blk, p.T2, p.gthr + g, p.hdr->band + p.margin, p.one, nullptr, s_dw);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) best = min(best, __shfl_xor_sync(0xffffffffu, best, off));
     if (lane == 0) s_red[warp] = best;

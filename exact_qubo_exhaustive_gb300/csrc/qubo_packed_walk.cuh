@@ -392,9 +392,9 @@ struct PackedWalker {
 // parameter or by the sign (the FMA pipe's integer unit). Word arithmetic modulo 2^32 is exact
 // per half (the representation above), so each instruction advances two states exactly.
 // ------------------------------------------------------------------------------------------------
-template <int R>
-struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
-  using B = PackedWalker<R, kModeMin, GlobalRows>;
+template <int R, class RS = GlobalRows>
+struct PackedPrunedWalker : PackedWalker<R, kModeMin, RS> {
+  using B = PackedWalker<R, kModeMin, RS>;
   using RowBuf = typename B::RowBuf;
   static constexpr int kThreads = 128;    // 2^12 columns: the word-quad stride is a constant
   static constexpr int kBlock = 1 << R;   // steps per block
@@ -402,7 +402,21 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
   static constexpr int kReadMask = 7;     // blocks between two reads of the group's best
   static_assert(R >= 3, "whole quads of walked energies per block");
 
-  int dmin0, dmin1;  // D_par of even and odd blocks (least change of one column over a block)
+  // Per column, the most negative change over an even block, as the packed signed pair of each
+  // word: DW = combine(D_lo, D_hi), kept in shared memory (s_dw: 4 word quads per thread, quad k
+  // of thread t at k * kThreads + t) so that it takes no registers from the block body. Over an
+  // odd block row R-1 enters removed, so the change is DW - Row[R-1]. The per-column bound is
+  // min_j (V_0[j] + D[j]) + Tmin_m, the tightest bound that takes the walked energies and the
+  // columns apart (every state of the block has E - s = T[d] + V_d[j] >= Tmin_m + V_0[j] + D[j]);
+  // the cheap one uses min_j V_0[j] + min_j D[j] and is tested first.
+  uint4* s_dw;
+  int dmin0, dmin1;  // the least of those changes over the thread's columns (even, odd blocks)
+  // The per-column bound pays where blocks often fail the cheap one: short units (R = 6; the
+  // batched n=24 workload had 18 % of its warp-blocks walked exactly with the cheap bound alone,
+  // and its pass went from 2.60 to 2.23 ms with both). With R = 7 it is compiled out: there the
+  // cheap bound clears almost every block (n=40 with entries in [-4, 4]: 0.001 % walked
+  // exactly), and the extra code cost 4 % (19.05 against 19.88 ms).
+  static constexpr bool kColumnBound = R <= 6;
   int g_best;        // G: the group's best energy known to this warp
   int best;          // this thread's best energy minus s
   uint32_t big;      // UINT_MAX, the add-min's bound (from a kernel parameter)
@@ -454,11 +468,35 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
       }
       int rl, rh;
       split(this->Row[R - 1][jj], rl, rh);
+      if (kColumnBound && s_dw) {
+        uint32_t* q = reinterpret_cast<uint32_t*>(s_dw + (jj >> 2) * kThreads + threadIdx.x);
+        q[jj & 3] = combine(neg_l + min(rl, 0), neg_h + min(rh, 0));
+      }
       lo0 = min(lo0, min(neg_l + min(rl, 0), neg_h + min(rh, 0)));
       lo1 = min(lo1, min(neg_l + min(-rl, 0), neg_h + min(-rh, 0)));
     }
     dmin0 = lo0;
     dmin1 = lo1;
+  }
+
+  // Least lower bound over the thread's columns, relative to s without the walked energy:
+  // min_j (V_0[j] + D[j]) for a block of parity odd. Every sum stays inside a half's range
+  // (|V_0 + D| <= 2 sum |U| < 2^15), so the word adds are exact per half.
+  __device__ __forceinline__ int column_bound(bool odd) const {
+    uint32_t x[kPW];
+#pragma unroll
+    for (int k = 0; k < kPW / 4; ++k) {
+      const uint4 d = s_dw[k * kThreads + threadIdx.x];
+      x[4 * k + 0] = this->V[4 * k + 0] + d.x;
+      x[4 * k + 1] = this->V[4 * k + 1] + d.y;
+      x[4 * k + 2] = this->V[4 * k + 2] + d.z;
+      x[4 * k + 3] = this->V[4 * k + 3] + d.w;
+    }
+    if (odd) {
+#pragma unroll
+      for (int jj = 0; jj < kPW; ++jj) x[jj] -= this->Row[R - 1][jj];
+    }
+    return lesser_half(pmin_all<kPW>(x));
   }
 
   // Least column value of the two halves of a 16x2 minimum word.
@@ -468,8 +506,11 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
 
   // The block walked with every per-step minimum (rare: the bound did not clear it), in groups of
   // four steps as in PrunedMinWalker::exact_block, with the packed per-half add-min of the walked
-  // energy (T2: T modulo 2^16 in both halves).
-  __device__ __forceinline__ void exact_block(const uint32_t* __restrict__ T2, int m, uint32_t pm0, uint32_t sgn) {
+  // energy (T2: T modulo 2^16 in both halves). With s_seg, the warp's minimum over the block goes
+  // to s_seg[m] (shared; atomicMin): a block no warp walked exactly holds no state at or below
+  // the threshold, so its entry may stay at its start value.
+  __device__ __forceinline__ void exact_block(const uint32_t* __restrict__ T2, int m, uint32_t pm0, uint32_t sgn,
+                                              int* s_seg) {
     const uint4* T4 = reinterpret_cast<const uint4*>(T2) + (static_cast<uint32_t>(m) << (R - 2));
     const uint32_t one = 0u - mone;
     uint4 tq = __ldg(T4);
@@ -490,7 +531,12 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
       tq = __ldg(T4 + k + 1);
       pa = __viaddmin_u16x2(pmin_all<kPW>(this->V), tq.x, pa);
     }
-    best = min(best, lesser_half(pa));
+    const int bm = lesser_half(pa);
+    best = min(best, bm);
+    if (s_seg) {
+      const int wm = __reduce_min_sync(0xffffffffu, bm + this->s);
+      if ((threadIdx.x & 31) == 0) atomicMin(s_seg + m, wm);
+    }
   }
 
   template <int A = 2>
@@ -513,12 +559,16 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
   // Whole unit: nblocks (even) blocks of 2^R steps, each but the last followed by a shared-row
   // flip, as PrunedMinWalker::walk (blk: the same control table; its row offsets count the 16-
   // column layout's quads, twice this layout's word quads). Returns this thread's best energy.
+  // s_seg (optional): per-block minima of the exactly walked blocks (see exact_block). dw:
+  // shared memory for the per-column changes (kThreads x 16 words), or null for the cheap bound
+  // alone.
   __device__ __forceinline__ int walk(const WalkCtx& c, int nblocks, const BlockCtl* __restrict__ blk,
-                                      const uint32_t* __restrict__ T2, int* gbest, int band, int one) {
+                                      const uint32_t* __restrict__ T2, int* gbest, int band, int one,
+                                      int* s_seg = nullptr, uint4* dw = nullptr) {
     big = 0xffffffffu - (uint32_t)(one - 1);
     mone = 0u - (uint32_t)one;
+    s_dw = dw;
     init_bounds();
-    const int dmb0 = dmin0 - band, dmb1 = dmin1 - band;
     g_best = __ldcg(gbest);
     // a real best from the first state's columns
     best = lesser_half(__viaddmin_u16x2(pmin_all<kPW>(this->V), __ldg(T2), 0xffffffffu));
@@ -535,12 +585,18 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, GlobalRows> {
       }
       const bool odd = m & 1;
       const int thr = min(best, g_best - this->s);
-      const uint32_t pm0 = pmin_all<kPW>(this->V);
       const uint32_t sgn = odd ? mone : 0u - mone;
-      if (__all_sync(0xffffffffu, lesser_half(pm0) + ctl.x + (odd ? dmb1 : dmb0) > thr)) {
+      // the cheap bound (least column plus least change) first; where it does not clear every
+      // lane, the per-column one
+      const uint32_t pm0 = pmin_all<kPW>(this->V);
+      bool clear = __all_sync(0xffffffffu, lesser_half(pm0) + ctl.x + (odd ? dmin1 : dmin0) - band > thr);
+      if constexpr (kColumnBound) {
+        if (!clear && s_dw) clear = __all_sync(0xffffffffu, column_bound(odd) + ctl.x - band > thr);
+      }
+      if (clear) {
         body<0>(sgn);
       } else {
-        exact_block(T2, m, pm0, sgn);
+        exact_block(T2, m, pm0, sgn, s_seg);
       }
       // the flip that follows (a no-op after the last block: sign 0, linear term 0)
       const uint32_t dsg = (uint32_t)static_cast<int>(__int_as_float(ctl.z));

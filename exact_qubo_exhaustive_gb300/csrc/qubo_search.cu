@@ -2,6 +2,7 @@
 #include <cstring>
 
 #include "qubo_search_kernel.cuh"
+#include "qubo_seed.cuh"
 
 namespace qgb {
 
@@ -225,17 +226,11 @@ __global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* 
   }
 }
 
-// Single-group searches (a whole problem or a slice range): greedy one-flip descents, one per warp
-// from a hashed start state, over the int32 image; the least energy reached, an energy some state
-// of the group attains, lowers the group's starting best of the bounded minimum pass (gthr), so
-// that the first units already skip most blocks. It decides nothing else: the walk still visits
-// every state, and any attained energy of the group is a valid threshold (it is never below the
-// group's minimum). With F > 0 the first F variables stay fixed to a unit prefix of the group,
-// gbase[0] + (a hash mod upg), so that the state lies in the group; with F = 0 (a whole problem)
-// every variable may flip. Lane l holds the fields of variables l and l + 32, g[v] = U_vv + sum
-// over set u != v of U(u, v) (the energy change when x_v goes from 0 to 1); each step flips the
-// free variable of the most negative change (lowest index among equals).
-constexpr int kSeedMaxN = 62;
+// Single-group searches (a whole problem or a slice range): greedy one-flip descents
+// (warp_descent), one per warp; the least energy reached lowers the group's starting best of the
+// bounded minimum pass (gthr), so that the first units already skip most blocks. With F > 0 the
+// first F variables stay fixed to a unit prefix of the group, so that every state reached lies in
+// the group; with F = 0 (a whole problem) every variable may flip.
 constexpr int kSeedBlocks = 32, kSeedThreads = 128;  // 128 descents
 __global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, int F, uint64_t upg,
                                                                    const DevHeader* __restrict__ hdr,
@@ -248,59 +243,8 @@ __global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, int F
     sU[idx] = (j >= i) ? U[idx] : U[j * n + i];  // symmetric: sU[i][j] = U[min(i,j)][max(i,j)]
   }
   __syncthreads();
-  const int lane = threadIdx.x & 31;
-  // start state: a SplitMix64-style hash of the warp's index
-  uint64_t z = (uint64_t)((blockIdx.x * blockDim.x + threadIdx.x) / 32 + 1) * 0x9E3779B97F4A7C15ull;
-  z = (z ^ (z >> 30)) * 0xBF58476D1CE4E5B9ull;
-  z = (z ^ (z >> 27)) * 0x94D049BB133111EBull;
-  uint64_t x = z ^ (z >> 31);
-  if (F > 0) {  // the prefix: a unit of the group (bit F - 1 - f of P is variable f)
-    const uint64_t P = gbase[0] + (z % upg);
-    for (int f = 0; f < F; ++f) x = (x & ~((uint64_t)1 << f)) | (((P >> (F - 1 - f)) & 1u) << f);
-  }
-  const int v0 = lane, v1 = lane + 32;
-  const bool h0 = v0 < n, h1 = v1 < n;
-  const bool f0 = h0 && v0 >= F, f1 = h1 && v1 >= F;  // free to flip
-  int32_t g0 = h0 ? sU[v0 * n + v0] : 0, g1 = h1 ? sU[v1 * n + v1] : 0;
-  for (int u = 0; u < n; ++u) {
-    if (!((x >> u) & 1u)) continue;
-    if (h0 && u != v0) g0 += sU[u * n + v0];
-    if (h1 && u != v1) g1 += sU[u * n + v1];
-  }
-  // 2 E(x) = sum over set v of (g[v] + U_vv)
-  long long twice = 0;
-  if (h0 && ((x >> v0) & 1u)) twice += (long long)g0 + sU[v0 * n + v0];
-  if (h1 && ((x >> v1) & 1u)) twice += (long long)g1 + sU[v1 * n + v1];
-#pragma unroll
-  for (int off = 16; off > 0; off >>= 1) twice += __shfl_xor_sync(0xffffffffu, twice, off);
-  int32_t e = (int32_t)(twice / 2);
-  for (int it = 0; it < 4 * n; ++it) {  // each flip lowers E, so this ends long before the cap
-    // key: (change + 2^31) in the high word, the variable in the low word; the least key wins
-    unsigned long long key = ~0ull;
-    if (f0) {
-      const int32_t d = ((x >> v0) & 1u) ? -g0 : g0;
-      key = ((unsigned long long)((long long)d + 0x80000000ll) << 32) | (unsigned)v0;
-    }
-    if (f1) {
-      const int32_t d = ((x >> v1) & 1u) ? -g1 : g1;
-      const unsigned long long k1 = ((unsigned long long)((long long)d + 0x80000000ll) << 32) | (unsigned)v1;
-      key = k1 < key ? k1 : key;
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const unsigned long long o = __shfl_xor_sync(0xffffffffu, key, off);
-      key = o < key ? o : key;
-    }
-    const int32_t best = (int32_t)((long long)(key >> 32) - 0x80000000ll);
-    if (best >= 0) break;  // a local minimum: no single flip lowers E
-    const int bv = (int)(key & 0xffffffffu);
-    const int32_t sg = ((x >> bv) & 1u) ? -1 : 1;
-    x ^= (uint64_t)1 << bv;
-    e += best;
-    if (h0 && v0 != bv) g0 += sg * sU[bv * n + v0];
-    if (h1 && v1 != bv) g1 += sg * sU[bv * n + v1];
-  }
-  if (lane == 0) atomicMin(gthr, e);
+  const int32_t e = warp_descent(sU, n, F, gbase[0], upg, (blockIdx.x * blockDim.x + threadIdx.x) / 32);
+  if ((threadIdx.x & 31) == 0) atomicMin(gthr, e);
 }
 
 // ------------------------------------------------------------------------------------------------

@@ -266,7 +266,8 @@ QUBO_API double qubo_kernel_time_ms(void);
  * the int32 pass without bounds above.
  * Results are identical either way; the switch exists to test and measure each pass.
  * Process-wide, read when a call is planned (qubo_plan reports it in `pruned`); calls already
- * planned are not affected. The batched calls have no bounded pass and ignore it. */
+ * planned are not affected. In the batched calls it applies to the packed pass (instances with
+ * sum |U| < 2^14); their other passes have no bounds. */
 QUBO_API void qubo_enable_block_bounds(int enable);
 
 /* Number of kernel launches the last host or device call enqueued. */

@@ -64,3 +64,17 @@ def test_device_entry_matches_the_host_entry(batched_result):
     ranks = np.array([oracle.rank_of_bits(v) for v in x], dtype=np.uint64)
     assert (e == r["min_energy"].astype(np.int64)).all()
     assert (ranks == r["argmin_rank"]).all() and (t == r["tie_count"]).all()
+
+
+def test_without_block_bounds_the_same_results(batched_result):
+    # the packed pass of the batch with block bounds (the default) against the one without
+    torch = pytest.importorskip("torch")
+    import exact_qubo_exhaustive_gb300 as q
+    Qs, r = batched_result
+    q.enable_block_bounds(False)
+    try:
+        e, x, t = q.solve_batched(Qs[:512])
+    finally:
+        q.enable_block_bounds(True)
+    assert (e == r["min_energy"][:512]).all() and (t == r["tie_count"][:512]).all()
+    assert [oracle.rank_of_bits(v) for v in x] == [int(v) for v in r["argmin_rank"][:512]]

@@ -435,9 +435,10 @@ def test_batched_ties_and_other_sizes(q):
         assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all()
 
 
-def test_batched_mixed_passes_against_oracle(q):
-    # one batch whose instances take the packed, biased and int32 minimum passes, plus all-ties
-    # and many-ties instances
+@pytest.mark.parametrize("bounds", [True, False])
+def test_batched_mixed_passes_against_oracle(q, bounds):
+    # one batch whose instances take the packed (with and without block bounds), biased and int32
+    # minimum passes, plus all-ties and many-ties instances
     n = 24
     Qs = np.stack([qi.random_upper_int(n, -20, 20, 510), qi.random_upper_int(n, -1000, 1000, 511),
                    qi.random_upper_int(n, -(1 << 20), 1 << 20, 512), np.zeros((n, n), np.int32),
@@ -445,13 +446,18 @@ def test_batched_mixed_passes_against_oracle(q):
                    qi.random_upper_int(n, -5000, 5000, 515)])
     sums = np.abs(Qs.astype(np.int64)).sum(axis=(1, 2))
     assert sums[0] <= (1 << 14) - 1 < sums[1] <= (1 << 22) - 1 < sums[2]
-    e, x, t = q.solve_batched(Qs)
+    q.enable_block_bounds(bounds)
+    try:
+        e, x, t = q.solve_batched(Qs)
+    finally:
+        q.enable_block_bounds(True)
     for b in range(Qs.shape[0]):
         want = O.solve(Qs[b])
         assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), b
 
 
-def test_batched_packed_ties_across_steps_halves_and_columns(q):
+@pytest.mark.parametrize("bounds", [True, False])
+def test_batched_packed_ties_across_steps_halves_and_columns(q, bounds):
     # n = 24 instances of the packed pass (12 cached bits, 1 prefix bit, 11 walked bits) with
     # variables whose couplings are all zero: each doubles the minimum's multiplicity, and the
     # tied states then differ in a register-row bit (x_7..x_11 in the minimum pass, x_8..x_11 in
@@ -468,7 +474,11 @@ def test_batched_packed_ties_across_steps_halves_and_columns(q):
         Qs.append(Q)
     Qs = np.stack(Qs)
     assert np.abs(Qs.astype(np.int64)).sum(axis=(1, 2)).max() <= (1 << 14) - 1
-    e, x, t = q.solve_batched(Qs)
+    q.enable_block_bounds(bounds)
+    try:
+        e, x, t = q.solve_batched(Qs)
+    finally:
+        q.enable_block_bounds(True)
     for b, free in enumerate(free_sets):
         want = O.solve(Qs[b])
         assert (int(e[b]), int(t[b])) == (want[0], want[2]) and (x[b] == want[1]).all(), b
