@@ -673,11 +673,6 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
   static constexpr int kReadMask = 7;       // blocks between two reads of the group's best
   static_assert(R >= 3, "whole quads of walked energies per block");
   static_assert(kThreads * kCPT == 4096, "the control table's row offsets assume 2^12 columns");
-  // int32 walk: the columns in kSkewGroups groups, group G kSkewLag * G flips behind group 0, so
-  // that the add-mins (ALU pipe) of one flip meet the multiply-adds (FMA pipe) of another
-  static constexpr int kSkewGroups = 1;
-  static constexpr int kSkewLag = 2;
-  static constexpr int kSkewCols = kCPT / kSkewGroups;
 
   int dmin0, dmin1;  // D_par of even and odd blocks
   int g_best;        // G: the group's best energy known to this warp (absolute, image units)
@@ -720,46 +715,11 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
     for (int jj = 0; jj < kCPT; jj += 2) cols_sgn(jj, row[jj], row[jj + 1], sg);
   }
 
-  // Flip D of a block (0 <= D < kBlock - 1) on the kSkewCols columns from j0 (int32 walk).
-  template <int D>
-  __device__ __forceinline__ void flip_cols(int j0, VT sgn) {
-    constexpr int a = ctz_c(D + 1);
-    constexpr int bit = ((D >> a) ^ (D >> (a + 1))) & 1;
-#pragma unroll
-    for (int j = j0; j < j0 + kSkewCols; ++j) {
-      if constexpr (a == R - 1) {
-        asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(this->V[j]) : "r"(this->Row[a][j]), "r"(sgn));
-      } else if constexpr (bit) {
-        asm("mad.lo.s32 %0, %1, %2, %0;" : "+r"(this->V[j]) : "r"(this->Row[a][j]), "r"(mone));
-      } else {
-        this->V[j] = __viaddmin_s32(this->V[j], this->Row[a][j], big);
-      }
-    }
-  }
-  // Slot T of the skewed block walk: column group G takes flip T - kSkewLag * G.
-  template <int T, int G = 0>
-  __device__ __forceinline__ void skew_slot(VT sgn) {
-    if constexpr (G < kSkewGroups) {
-      constexpr int D = T - kSkewLag * G;
-      if constexpr (D >= 0 && D + 1 < kBlock) flip_cols<D>(G * kSkewCols, sgn);
-      skew_slot<T, G + 1>(sgn);
-    }
-  }
-  template <int T>
-  __device__ __forceinline__ void body_skew(VT sgn) {
-    if constexpr (T < kBlock - 1 + kSkewLag * (kSkewGroups - 1)) {
-      skew_slot<T>(sgn);
-      body_skew<T + 1>(sgn);
-    }
-  }
-
   // Flips of steps 0..kBlock-2 of a block; position R-1 flips once, with sign sgn (+1 in even
   // blocks, -1 in odd ones); the others with the sign their Gray bit fixes.
   template <int D>
   __device__ __forceinline__ void body(VT sgn) {
-    if constexpr (kInt && kSkewGroups > 1) {
-      if constexpr (D == 0) body_skew<0>(sgn);
-    } else if constexpr (D + 1 < kBlock) {
+    if constexpr (D + 1 < kBlock) {
       constexpr int a = ctz_c(D + 1);
       if constexpr (a == R - 1) {
         row_sgn(this->Row[a], sgn);
