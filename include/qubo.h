@@ -6,9 +6,13 @@
  * (Terastate-per-second QUBO Brute-Force on a Single GPU, §I objective), the minimiser with the
  * lowest rank, rank(x) = sum_i x_i 2^(n-1-i) (x_0 is the most significant bit: the lexicographic
  * order of the state space U_N in §II-B, Fig. 2), and the number of states attaining E_min.
- * Every one of the 2^n states is evaluated: the search is the prefix-suffix decomposition of
+ * Every one of the 2^n states is visited: the search is the prefix-suffix decomposition of
  * §II-A..C (eq. 4 and 8) walked in Gray-code order (§III-B, Algorithm 2, eq. 9), split into
- * independent fixed-prefix subproblems (§III-C1) and cached column segments (§III-C2).
+ * independent fixed-prefix subproblems (§III-C1) and cached column segments (§III-C2), and every
+ * state's column energy gets its one add (eq. 9). The comparison of a state's energy with the
+ * minimum is left out only for blocks of Gray steps whose lower bound proves that none of their
+ * states reaches the best energy found so far (block bounds, see qubo_enable_block_bounds); the
+ * results are exactly those of comparing every state.
  *
  * Conventions for every entry point:
  *  - Q is read only during the call; the caller owns all buffers; the library keeps no pointer.
