@@ -298,6 +298,12 @@ int make_plan(int n, int dtype, int k_prefix, int cache_bits, int K, uint64_t un
   }
   p.packed = p.packed_ok && !p.prune;
   p.packed_pruned = p.packed_ok && p.prune;
+  if (p.packed_pruned) {
+    p.packed_pruned_smem = packed_pruned_smem_bytes(p.C, p.w, p.prune_r);
+    int pocc = 0;
+    if (occupancy_packed_pruned(p.prune_r, p.packed_pruned_smem, &pocc) != cudaSuccess || pocc < 1) pocc = 1;
+    p.packed_pruned_blocks = std::max(1, di.sms) * pocc;
+  }
   *out = p;
   return QUBO_OK;
 }

@@ -103,6 +103,8 @@ struct Plan {
   bool packed = false;     // packed 16x2 minimum pass (fast variant, int32, C >= 10, w >= kPackedR + 1)
   bool packed_ok = false;  //   the packed pass fits this plan
   bool packed_pruned = false;  // the packed pass with block bounds runs (packed_ok and prune)
+  int packed_pruned_blocks = 0;     // its persistent grid (2 blocks of 128 threads per SM)
+  size_t packed_pruned_smem = 0;
   int packed_threads = 0;  // 2^C / 32
   int packed_blocks = 0;
   size_t packed_smem = 0;

@@ -145,28 +145,38 @@ __global__ void __launch_bounds__(128, 2) packed_pruned_kernel(const KParams p) 
 }
 
 template <int R>
-cudaError_t launch_pruned(const KParams& p, uint64_t nunits, cudaStream_t s) {
+cudaError_t launch_pruned(const KParams& p, int blocks, size_t smem, cudaStream_t s) {
   auto k = packed_pruned_kernel<R>;
-  const size_t smem = (size_t)(p.w - R) << (p.C + 1);
   cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int occ = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, PackedPrunedWalker<R>::kThreads, smem)) != cudaSuccess)
-    return e;
-  const uint64_t full = (uint64_t)device_info().sms * (uint64_t)(occ > 0 ? occ : 1);
-  const int blocks = (int)(nunits < full ? nunits : full);
   k<<<blocks, PackedPrunedWalker<R>::kThreads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int R>
+cudaError_t occupancy_pruned(size_t smem, int* blocks_per_sm) {
+  auto k = packed_pruned_kernel<R>;
+  cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k, PackedPrunedWalker<R>::kThreads, smem);
 }
 
 }  // namespace
 
 size_t packed_smem_bytes(int C, int w) { return (size_t)(w - kPackedR) << (C + 1); }
 
-cudaError_t launch_search_packed_pruned(int R, const KParams& p, uint64_t nunits, cudaStream_t s) {
+size_t packed_pruned_smem_bytes(int C, int w, int R) { return (size_t)(w - R) << (C + 1); }
+
+cudaError_t launch_search_packed_pruned(int R, const KParams& p, int blocks, size_t smem, cudaStream_t s) {
   if (p.C != 12) return cudaErrorInvalidConfiguration;  // 128 threads x 32 columns
-  if (R == kPruneRLong) return launch_pruned<kPruneRLong>(p, nunits, s);
-  if (R == kPruneRShort) return launch_pruned<kPruneRShort>(p, nunits, s);
+  if (R == kPruneRLong) return launch_pruned<kPruneRLong>(p, blocks, smem, s);
+  if (R == kPruneRShort) return launch_pruned<kPruneRShort>(p, blocks, smem, s);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t occupancy_packed_pruned(int R, size_t smem, int* blocks_per_sm) {
+  if (R == kPruneRLong) return occupancy_pruned<kPruneRLong>(smem, blocks_per_sm);
+  if (R == kPruneRShort) return occupancy_pruned<kPruneRShort>(smem, blocks_per_sm);
   return cudaErrorInvalidValue;
 }
 

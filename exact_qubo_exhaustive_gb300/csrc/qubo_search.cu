@@ -442,7 +442,8 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     if (p.packed_pruned) {
       // packed 16x2 CUDA-core pass with block bounds (exits at once unless it owns the minimum
       // pass) ...
-      if ((e = launch_search_packed_pruned(p.prune_r, kp, nunits, stream)) != cudaSuccess) return e;
+      const int pb = (int)(nunits < (uint64_t)p.packed_pruned_blocks ? nunits : (uint64_t)p.packed_pruned_blocks);
+      if ((e = launch_search_packed_pruned(p.prune_r, kp, pb, p.packed_pruned_smem, stream)) != cudaSuccess) return e;
       ++nl;
     } else if (p.packed) {
       // packed 16x2 CUDA-core pass (exits at once unless it owns the minimum pass) ...

@@ -257,7 +257,9 @@ cudaError_t launch_search_int_min5(const KParams& p, int blocks, int threads, si
 cudaError_t launch_search_biased_pruned(int R, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_int_pruned(int R, const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
 cudaError_t launch_search_packed(const KParams& p, int blocks, int threads, size_t smem, cudaStream_t s);
-cudaError_t launch_search_packed_pruned(int R, const KParams& p, uint64_t nunits, cudaStream_t s);
+cudaError_t launch_search_packed_pruned(int R, const KParams& p, int blocks, size_t smem, cudaStream_t s);
+cudaError_t occupancy_packed_pruned(int R, size_t smem, int* blocks_per_sm);
+size_t packed_pruned_smem_bytes(int C, int w, int R);
 cudaError_t occupancy_packed(int threads, size_t smem, int* blocks_per_sm);
 size_t packed_smem_bytes(int C, int w);
 
