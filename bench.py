@@ -547,8 +547,7 @@ def other_configs(q, torch, dev, stream):
                                               int(r["tie_count"]), tol)
         if name == "n40_narrow_int32":
             out[name]["workload"] = ("n=40 dense QUBO, int32 upper-triangular, entries uniform in [-4,4] "
-                                     "(sum |U| = 1822: the bounded biased pass; the packed 16x2 pass "
-                                     "runs without bounds, below)")
+                                     "(sum |U| = 1822: the packed 16x2 pass with block bounds)")
         if name == "n36_wide_int32":
             out[name]["workload"] = ("n=36 dense QUBO, int32 upper-triangular, entries uniform in "
                                      "[-2^20, 2^20] (sum |U| ~ 3.5e8 > 2^22: the int32 minimum pass)")
