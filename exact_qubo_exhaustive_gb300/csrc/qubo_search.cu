@@ -197,8 +197,13 @@ __global__ void tables_kernel(int n, int C, int F, int w, const DevHeader* __res
 // the energy of a state of that unit (prefix 0, cached variables 0), so min T may start it.
 // ------------------------------------------------------------------------------------------------
 __global__ void block_table_kernel(int n, int C, int w, int R, const DevHeader* __restrict__ hdr,
-                                   const int32_t* __restrict__ T, BlockCtl* blk, int32_t* seed) {
+                                   const int32_t* __restrict__ T, BlockCtl* blk, int32_t* seed,
+                                   int32_t* unit_min, uint64_t total_units) {
   if (hdr->status != QUBO_OK) return;
+  // the bounded passes publish unit minima with atomics: they start at INT_MAX
+  for (uint64_t u = blockIdx.x * (uint64_t)blockDim.x + threadIdx.x; u < total_units;
+       u += (uint64_t)gridDim.x * blockDim.x)
+    unit_min[u] = kIntInf;
   const uint32_t nb = 1u << (w - R);
   for (uint32_t m = blockIdx.x * blockDim.x + threadIdx.x; m <= nb; m += gridDim.x * blockDim.x) {
     const uint32_t mm = m < nb ? m : nb - 1;
@@ -377,7 +382,8 @@ static cudaError_t run_front(const Plan& p, const void* d_Q, const Work& w, qubo
     // states of unit 0)
     const bool from_unit0 = !p.host_gbase && p.gbase0 == 0 && p.ngroups == 1;
     int32_t* seed = from_unit0 ? w.gthr : nullptr;
-    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk, seed);
+    block_table_kernel<<<(nb + 1 + 127) / 128, 128, 0, stream>>>(p.n, p.C, p.w, p.prune_r, w.hdr, w.T, w.blk, seed,
+                                                                  w.unit_min, p.total_units);
     ++nl;
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (p.ngroups == 1) {

@@ -72,6 +72,27 @@ __device__ __forceinline__ void unit_linear_terms(const int32_t* __restrict__ U,
   }
 }
 
+// The same terms formed by one warp for its own use (lane l: variables l and l + 32; n <= 62),
+// with -L at 64 + v and a zero at 128 (the block-bounded walkers' signed linear terms).
+__device__ __forceinline__ void warp_linear_terms(const int32_t* __restrict__ U, int n, int F, uint64_t P, int* sl,
+                                                  int lane) {
+  for (int v = lane; v < 64; v += 32) {
+    int acc = 0;
+    if (v < n) {
+      if (v >= F) {
+        for (int f = 0; f < F; ++f)
+          if ((P >> (F - 1 - f)) & 1u) acc += U[f * n + v];
+      } else if ((P >> (F - 1 - v)) & 1u) {
+        for (int f2 = v; f2 < F; ++f2)
+          if ((P >> (F - 1 - f2)) & 1u) acc += U[v * n + f2];
+      }
+    }
+    sl[v] = acc;
+    sl[64 + v] = -acc;
+  }
+  if (lane == 0) sl[128] = 0;
+}
+
 // Minimum-pass walk of one unit in value type VT; returns this thread's best energy (int32).
 template <int CPT, int R, typename VT>
 __device__ __forceinline__ int min_walk(const WalkCtx& c, const KParams& p, int cP, int64_t niter) {
@@ -92,8 +113,10 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   static_assert(!BIASED || (MODE == kModeMin && CPT >= 4), "biased walk: fast layout, minimum pass");
   static_assert(!PRUNE || (MODE == kModeMin && CPT == 16), "pruned walk: minimum pass, fast layout");
   extern __shared__ __align__(16) int4 s_rows4[];
-  // linear terms; the block-bounded pass also keeps -L at 64 + v and a zero at 128
-  __shared__ int sL[PRUNE ? 129 : 64];
+  // linear terms of the current unit; the block-bounded pass keeps them per warp, with -L at
+  // 64 + v and a zero at 128
+  __shared__ int sL[PRUNE ? 1 : 64];
+  __shared__ int sLw[PRUNE ? (256 / 32) * 129 : 1];
   __shared__ int s_red[32];
   // resolve modes: per-thread slots for the out-of-line candidate scan
   __shared__ __align__(16) int s_slot[(MODE != kModeMin && CPT >= 4) ? kFastThreadsMax * CPT : 4];
@@ -155,6 +178,34 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
   if constexpr (MODE == kModeMin) nitems = p.unit_end - p.unit_begin;
   else nitems = static_cast<uint64_t>(p.hdr->tied_count) << p.seg_bits;
 
+  if constexpr (PRUNE) {
+    // The block-bounded minimum pass. Its warps share only the staged rows, which never change,
+    // so no block barrier comes between units: each warp forms the unit's linear terms itself and
+    // publishes its minimum with atomics (unit_min starts at INT_MAX: block_table_kernel).
+    using VT = typename std::conditional<BIASED, float, int>::type;
+    __syncthreads();  // the staged rows are visible
+    int* sl = sLw + warp * 129;
+    c.sL = sl;
+    for (uint64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
+      const uint64_t u = p.unit_begin + item;
+      const uint64_t g = u / p.upg;
+      const uint64_t P = p.gbase[g] + (u - g * p.upg);
+      warp_linear_terms(p.U, n, F, P, sl, lane);
+      __syncwarp();
+      int cP = 0;
+      for (int f = 0; f < F; ++f) cP += sl[f];
+      PrunedMinWalker<R, VT> W;
+      W.init(c, p.Ec, p.M, cP);
+      // two blocks per iteration
+      W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band + p.margin, p.one);
+      const int best = __reduce_min_sync(0xffffffffu, W.aux - VOps<VT>::kBiasBits + W.s);
+      if (lane == 0) {
+        atomicMin(p.unit_min + u, best);
+        atomicMin(p.gthr + g, best);
+      }
+      __syncwarp();  // the walk's last reads of this warp's linear terms are done
+    }
+  } else {
   for (uint64_t item = blockIdx.x; item < nitems; item += gridDim.x) {
     uint64_t u;
     int64_t it0 = 0, it1 = niter;
@@ -173,24 +224,13 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
 
     __syncthreads();  // previous item is done with sL; staged rows are visible
     unit_linear_terms(p.U, n, F, P, sL, tid, nthreads);
-    if constexpr (PRUNE) {
-      __syncthreads();
-      for (int v = tid; v <= 64; v += nthreads) sL[64 + v] = v < n ? -sL[v] : 0;
-    }
     __syncthreads();
     int cP = 0;
     for (int f = 0; f < F; ++f) cP += sL[f];
 
     if constexpr (MODE == kModeMin) {
       int best;
-      if constexpr (PRUNE) {
-        using VT = typename std::conditional<BIASED, float, int>::type;
-        PrunedMinWalker<R, VT> W;
-        W.init(c, p.Ec, p.M, cP);
-        // two blocks per iteration
-        W.walk(c, static_cast<int>(niter << 1), p.blk, p.gthr + g, p.hdr->band + p.margin, p.one);
-        best = W.aux - VOps<VT>::kBiasBits + W.s;
-      } else if (niter == 0) {
+      if (niter == 0) {
         // no walked variable (generic variant only): the single walked assignment is 0
         Walker<CPT, R, MODE> W;
         W.init(c, p.Ec, p.M, cP);
@@ -208,7 +248,6 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
         int b = s_red[0];
         for (int k = 1; k < (nthreads >> 5); ++k) b = min(b, s_red[k]);
         p.unit_min[u] = b;
-        if constexpr (PRUNE) atomicMin(p.gthr + g, b);
       }
     } else {
       Walker<CPT, R, MODE> W;
@@ -248,6 +287,7 @@ __global__ void __launch_bounds__(CPT == 1 ? 1024 : 256, 1) search_kernel(const 
       }
     }
   }
+  }  // not PRUNE
 }
 
 // Launch helpers (one translation unit per variant).
