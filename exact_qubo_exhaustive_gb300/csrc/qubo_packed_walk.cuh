@@ -592,11 +592,19 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, RS> {
       bool clear = __all_sync(0xffffffffu, lesser_half(pm0) + ctl.x + (odd ? dmin1 : dmin0) - band > thr);
       if constexpr (kColumnBound) {
         if (!clear && s_dw) clear = __all_sync(0xffffffffu, column_bound(odd) + ctl.x - band > thr);
-      }
-      if (clear) {
-        body<0>(sgn);
+        if (clear) {
+          body<0>(sgn);
+        } else {
+          exact_block(T2, m, pm0, sgn, s_seg);
+        }
       } else {
-        exact_block(T2, m, pm0, sgn, s_seg);
+        // long blocks: the adds first, overlapped with the test, and a second walk from the
+        // block's first state where the bound does not clear (as PrunedMinWalker::block)
+        body<0>(sgn);
+        if (!clear) {
+          words_sgn(this->Row[R - 1], 0u - sgn);
+          exact_block(T2, m, pm0, sgn, s_seg);
+        }
       }
       // the flip that follows (a no-op after the last block: sign 0, linear term 0)
       const uint32_t dsg = (uint32_t)static_cast<int>(__int_as_float(ctl.z));
