@@ -418,6 +418,7 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, RS> {
   // exactly), and the extra code cost 4 % (19.05 against 19.88 ms).
   static constexpr bool kColumnBound = R <= 6;
   int g_best;        // G: the group's best energy known to this warp
+  int g_pend;        // the group's published best, loaded a block ago and not yet folded into G
   int best;          // this thread's best energy minus s
   uint32_t big;      // UINT_MAX, the add-min's bound (from a kernel parameter)
   uint32_t mone;     // -1 modulo 2^32 (from a kernel parameter)
@@ -553,7 +554,7 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, RS> {
       if ((threadIdx.x & 31) == 0) atomicMin(gbest, v);
       g_best = v;
     }
-    if (read) g_best = min(g_best, __ldcg(gbest));
+    if (read) g_pend = __ldcg(gbest);  // folded into G after the next block (PrunedMinWalker)
   }
 
   // Whole unit: nblocks (even) blocks of 2^R steps, each but the last followed by a shared-row
@@ -570,6 +571,7 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, RS> {
     s_dw = dw;
     init_bounds();
     g_best = __ldcg(gbest);
+    g_pend = kIntInf;
     // a real best from the first state's columns
     best = lesser_half(__viaddmin_u16x2(pmin_all<kPW>(this->V), __ldg(T2), 0xffffffffu));
     const int4* ctl4 = reinterpret_cast<const int4*>(blk);
@@ -606,6 +608,8 @@ struct PackedPrunedWalker : PackedWalker<R, kModeMin, RS> {
           exact_block(T2, m, pm0, sgn, s_seg);
         }
       }
+      g_best = min(g_best, g_pend);  // loaded a block ago (kIntInf when nothing was loaded)
+      g_pend = kIntInf;
       // the flip that follows (a no-op after the last block: sign 0, linear term 0)
       const uint32_t dsg = (uint32_t)static_cast<int>(__int_as_float(ctl.z));
 #pragma unroll

@@ -676,6 +676,7 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
 
   int dmin0, dmin1;  // D_par of even and odd blocks
   int g_best;        // G: the group's best energy known to this warp (absolute, image units)
+  int g_pend;        // the group's published best, loaded a block ago and not yet folded into G
   int big;           // int32 walk: INT_MAX, the add-min's bound (from a kernel parameter)
   int mone;          // int32 walk: -1 (from a kernel parameter)
 
@@ -829,14 +830,15 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
   // The group's best. Every kRefreshMask + 1 blocks the warp publishes its best if it improved on
   // what it last published (a reduction whose result nobody waits for: after the first blocks
   // almost no warp improves, so the shared word sees few updates); every kReadMask + 1 blocks it
-  // also takes the grid's value with a plain load, first used a block later.
+  // also loads the grid's value, which walk() folds into G only after the next block's adds, so
+  // that the load's latency is hidden behind them.
   __device__ __forceinline__ void exchange_best(int* gbest, bool read) {
     const int v = __reduce_min_sync(0xffffffffu, this->aux - O::kBiasBits + this->s);
     if (v < g_best) {
       if ((threadIdx.x & 31) == 0) atomicMin(gbest, v);
       g_best = v;
     }
-    if (read) g_best = min(g_best, __ldcg(gbest));
+    if (read) g_pend = __ldcg(gbest);
   }
 
   // Whole unit: nblocks (even, < 2^31) blocks of 2^R steps, each but the last followed by a
@@ -850,6 +852,7 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
     init_bounds();
     const LB dmb0 = static_cast<LB>(dmin0) - band, dmb1 = static_cast<LB>(dmin1) - band;
     g_best = __ldcg(gbest);
+    g_pend = kIntInf;
     // a real best from the first state's columns, so the running best never leaves its range
     this->aux = __viaddmin_s32(vmin_bits<VT, kCPT>(this->V), __ldg(c.T), kIntInf);
     const int4* ctl4 = reinterpret_cast<const int4*>(blk);
@@ -866,6 +869,8 @@ struct PrunedMinWalker : Walker<16, R, kModeMin, VT> {
       const bool odd = m & 1;
       const int thr = min(this->aux, O::kBiasBits + g_best - this->s);
       block(c, m, static_cast<LB>(ctl.x) + (odd ? dmb1 : dmb0), thr, odd ? minus_one() : -minus_one());
+      g_best = min(g_best, g_pend);  // loaded a block ago (kIntInf when nothing was loaded)
+      g_pend = kIntInf;
       // the flip that follows (a no-op after the last block: sign 0, linear term 0)
       const float dsgn_f = __int_as_float(ctl.z);
       VT dsgn;
