@@ -146,7 +146,7 @@ const DevInfo& device_info() {
 }
 
 // ------------------------------------------------------------------------------------------------
-// A2: the decomposition planner. n = F (fixed, per unit) + w (Gray-walked) + C (cached).
+// The decomposition planner. n = F (fixed, per unit) + w (Gray-walked) + C (cached).
 // ------------------------------------------------------------------------------------------------
 namespace {
 

@@ -7,7 +7,7 @@
 namespace qgb {
 
 // ------------------------------------------------------------------------------------------------
-// A1: fold Q to the upper triangle and validate (one block).
+// Fold Q to the upper triangle and validate (one block).
 //   int32: U_ii = Q_ii, U_ij = Q_ij + Q_ji (i < j) in int64; S = sum |U_ij| must be <= 2^30 - 1.
 //   fp32/fp64: every entry finite; U64 folded in fp64; the int32 image is round(U64 * 2^s) with the
 //          largest s keeping sum |image| <= 2^22 - 1 (the range of the biased fp32 minimum pass).
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(256) prep_kernel(int n, int dtype, const void*
 }
 
 // ------------------------------------------------------------------------------------------------
-// A3: the energy-component cache (§II-C Table I, Alg. 2 preprocessing), computed directly:
+// The energy-component cache (§II-C Table I, Alg. 2 preprocessing), computed directly:
 //   M[v][j]  = sum_{cached b} U[v][b] x_b(j)        interaction rows M_int, v < n - C
 //   Ec[j]    = sum_{cached a <= b} U[a][b] x_a x_b  E(U_B), the suffix energies
 //   T[i]     = E of the walked variables at gray(i) (Gray-ordered prefix energies, §IV-B.3)
@@ -253,7 +253,7 @@ __global__ void __launch_bounds__(kSeedThreads) descent_seed_kernel(int n, int F
 }
 
 // ------------------------------------------------------------------------------------------------
-// A5: per-group minimum over its units (one block per group), and accumulator reset.
+// Per-group minimum over its units (one block per group), and accumulator reset.
 // ------------------------------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) group_min_kernel(KParams p) {
   __shared__ int s_red[8];

@@ -646,8 +646,10 @@ struct Walker {
 //
 // The threshold is min(this thread's best, G) + band (the fp32 resolution band, plus any margin a
 // driver asks for so that unit minima up to E* + margin stay exact). G is the best energy any
-// block of the grid has published for this group so far (or sum |U_ij|, which bounds every energy
-// from above).
+// warp of the grid has published for this group so far, starting from sum |U_ij| (which bounds
+// every energy from above) lowered by the seeds: the least walked energy (energies of states of
+// unit 0, when the group holds it) and the least energy reached by greedy one-flip descents
+// inside the group (qubo_seed.cuh).
 // Every value involved is an energy some state of the group attains, so the threshold is never
 // below the group's minimum E*: a state with E <= E* + band is never in a skipped block. Hence a
 // unit holding such a state reports its minimum exactly, every other unit reports the energy of
