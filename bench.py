@@ -75,11 +75,8 @@ class ResultMismatch(RuntimeError):
     pass
 
 
-def check_result(name: str, e, rank: int, ties: int, tol: float = 0.0, required: bool = True) -> str:
-    """Compares a timed search's answer with the stored full oracle search; raises on a mismatch
-    (and, when `required`, when no search is stored)."""
-    if not required and not os.path.exists(os.path.join(ROOT, "tests", "golden", f"full_oracle_{name}.txt")):
-        return "no stored full oracle search of this workload"
+def check_result(name: str, e, rank: int, ties: int, tol: float = 0.0) -> str:
+    """Compares a timed search's answer with the stored full oracle search; raises on a mismatch."""
     ge, grank, gties = golden(name)
     if abs(float(e) - float(ge)) > tol or int(rank) != grank or int(ties) != gties:
         raise ResultMismatch(f"{name}: got ({e}, {rank}, {ties}), full oracle search gave ({ge}, {grank}, {gties})")
