@@ -587,11 +587,13 @@ __global__ void __launch_bounds__(128, 2) bpacked_kernel(BatchTables b) {
       const int4* H4 = reinterpret_cast<const int4*>(b.H + (size_t)g * b.sh);
       for (int idx = tid; idx < (nh >> 2); idx += nthreads) reinterpret_cast<int4*>(sH)[idx] = H4[idx];
       __syncthreads();
-      const int lq = C - 2;  // log2 of the int4 quads per row (two words each)
-      for (int idx = tid; idx < (ndyn << lq); idx += nthreads) {
-        const int rr = idx >> lq, q = idx & ((1 << lq) - 1);
-        const int4 m = rows.quad(n - C - 1 - (R + rr), q);
-        reinterpret_cast<uint2*>(s_words)[idx] = make_uint2(packed::combine(m.x, m.y), packed::combine(m.z, m.w));
+      if constexpr (MODE == kModeMin) {  // the re-walk forms the few rows it flips itself
+        const int lq = C - 2;  // log2 of the int4 quads per row (two words each)
+        for (int idx = tid; idx < (ndyn << lq); idx += nthreads) {
+          const int rr = idx >> lq, q = idx & ((1 << lq) - 1);
+          const int4 m = rows.quad(n - C - 1 - (R + rr), q);
+          reinterpret_cast<uint2*>(s_words)[idx] = make_uint2(packed::combine(m.x, m.y), packed::combine(m.z, m.w));
+        }
       }
       staged = g;
     }

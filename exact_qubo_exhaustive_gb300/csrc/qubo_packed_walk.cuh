@@ -19,6 +19,8 @@
 // fast walk of the int32 pass (R register rows, shared rows and walked energies read ahead).
 #pragma once
 
+#include <type_traits>
+
 #include "qubo_walk.cuh"
 
 namespace qgb {
@@ -169,9 +171,15 @@ struct PackedWalker {
   struct RowBuf {
     uint4 q[kPW / 4];
   };
+  // The re-walk of a few iterations from half sums (kModeTiesInt with HalfRows) forms the shared
+  // rows it flips from the half sums, for its own columns, instead of reading rows staged for the
+  // whole block: it needs only the rows of the seek and two flips per iteration.
+  static constexpr bool kDirectRows = MODE == kModeTiesInt && std::is_same<RS, HalfRows>::value;
+  RS rs_;
 
   __device__ __forceinline__ void init(const WalkCtx& c, const int* __restrict__ Ec, const RS& rs, int cP) {
     const int t = c.thread, T = c.nthreads, n = c.n, C = c.C;
+    rs_ = rs;
     s = cP;
     aux = 0xffffffffu;
     const int lt = 31 - __clz(T);
@@ -213,6 +221,16 @@ struct PackedWalker {
   }
 
   __device__ __forceinline__ void load_dyn_row(const WalkCtx& c, int a, RowBuf& b) const {
+    if constexpr (kDirectRows) {
+      const int v = c.n - c.C - 1 - a;
+#pragma unroll
+      for (int k = 0; k < kPW / 4; ++k) {
+        const int qi = k * c.nthreads + c.thread;  // word quad: columns qi*8 .. qi*8+7
+        const int4 m0 = rs_.quad(v, 2 * qi), m1 = rs_.quad(v, 2 * qi + 1);
+        b.q[k] = make_uint4(combine(m0.x, m0.y), combine(m0.z, m0.w), combine(m1.x, m1.y), combine(m1.z, m1.w));
+      }
+      return;
+    }
     const int nq = (1 << c.C) >> 3;  // word quads per row
     const uint4* rp = reinterpret_cast<const uint4*>(c.rows4) + (size_t)(a - R) * nq + c.thread;
 #pragma unroll
